@@ -1,0 +1,208 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) exact-attention library.
+ *
+ * Exact scaled dot-product attention computed without materialising the score
+ * matrix S = QK^T: every query row carries an online-softmax state (running
+ * max m, normaliser l referenced to m, unnormalised accumulator O~), rescaled
+ * by exp(m_old - m_new) whenever the max rises, and disjoint key sets combine
+ * through the associative merge of two states.
+ *
+ * Sources (page title, then section):
+ *   [NA]  "Naive attention and the online softmax" -- opening section (shapes,
+ *         GQA broadcast), (3) "The online recurrence", "Extending the
+ *         recurrence to the output", "The state that gets passed around is the
+ *         log-sum-exp", "The base case is a NaN factory".
+ *   [OSR] "The Online Softmax Recurrence" -- "The recurrence", "Where it breaks".
+ *   [DEC] "Decode attention: FlashDecoding, split-K, paged kernels" -- "The
+ *         grid", "Segment length, and the early exit", "What the merge costs",
+ *         "Where GQA enters", paged addressing, "CUDA graphs need the split
+ *         count pinned".
+ *   [MRG] "Merge normalized attention without averaging tile outputs".
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers (cudaMalloc / PyTorch CUDA
+ *     memory) unless a parameter says otherwise; the caller owns every buffer.
+ *     The library never allocates, frees or synchronises: each call only
+ *     enqueues kernels on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and returns.
+ *   - Tensors are dense, row-major, with the shapes given below. Tensor base
+ *     pointers must be 16-byte aligned (TMA and 128-bit vector loads);
+ *     `workspace` must be 256-byte aligned.
+ *   - bf16 is IEEE-style bfloat16 (1-8-7); fp32 is IEEE binary32.
+ *   - LSE is the natural-log log-sum-exp m + ln(l) of the scaled logits, fp32.
+ *   - A query row with no allowed key yields output 0 and LSE = -inf ([MRG],
+ *     last paragraph: zero output is the extension chosen for empty rows).
+ *   - Errors: arguments are validated on the host before anything is
+ *     launched; an invalid call returns ATTN_ERR_INVALID_ARG (or
+ *     ATTN_ERR_UNSUPPORTED for a well-formed but unbuilt shape) and enqueues
+ *     nothing. ATTN_ERR_CUDA reports a failed launch (cudaGetLastError).
+ *     Kernels never trap: a bounded wait that gives up, or a page index
+ *     outside the cache, sets a device error word that
+ *     attn_get_device_error() reads.
+ */
+#ifndef ONLINE_SOFTMAX_ATTN_GB300_ATTN_H_
+#define ONLINE_SOFTMAX_ATTN_GB300_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,
+  ATTN_ERR_UNSUPPORTED = 2,
+  ATTN_ERR_CUDA = 3,
+  ATTN_ERR_DEVICE = 4
+} attn_status_t;
+
+typedef enum { ATTN_DTYPE_F32 = 0, ATTN_DTYPE_BF16 = 1 } attn_dtype_t;
+
+/* Device error bits reported by attn_get_device_error(). */
+#define ATTN_DEVERR_WAIT_TIMEOUT 0x1u /* a bounded mbarrier wait gave up      */
+#define ATTN_DEVERR_BAD_PAGE 0x2u     /* block_table entry outside the cache */
+#define ATTN_DEVERR_TMEM 0x4u         /* tensor-memory allocation failed     */
+#define ATTN_DEVERR_BAD_SEQ_LEN 0x8u  /* seq_len < 0 or beyond the table row  */
+
+/* Human-readable name of a status code; never NULL. */
+const char* attn_status_string(attn_status_t status);
+
+/* Library ABI version (major * 100 + minor). */
+int attn_version(void);
+
+/*
+ * attn_prefill -- exact attention of T queries over the same T keys, per head.
+ * Follows [NA] opening section (Q [h,T,d_h], K/V [h_kv,T,d_h] broadcast to
+ * g = h/h_kv query heads: query head hq reads KV head hq / g) and [NA] (3) /
+ * "Extending the recurrence to the output" (one pass over key tiles, divide
+ * once at the end).
+ *
+ *   q     [h, T, d_h]     dtype                          (read)
+ *   k, v  [h_kv, T, d_h]  dtype                          (read)
+ *   o     [h, T, d_h]     dtype                          (written)
+ *   lse   [h, T]          fp32, may be NULL               (written)
+ *   causal: nonzero -> key j is allowed for query i iff j <= i.
+ *   scale : multiplies q.k before the softmax (normally 1/sqrt(d_h)); must be
+ *           finite and > 0.
+ *   dtype : ATTN_DTYPE_BF16 -> tcgen05 tensor-core path (d_h = 128 or 64),
+ *           fp32 accumulation and statistics;
+ *           ATTN_DTYPE_F32  -> fp32 SIMT path (d_h = 64 or 128), fp32 throughout.
+ * Errors: INVALID_ARG for NULL q/k/v/o (T > 0), T < 0, h < 1, h > 65535,
+ * h_kv < 1, h % h_kv != 0, misaligned pointers, scale not finite and > 0;
+ * UNSUPPORTED for other
+ * d_h. T == 0 is a no-op returning ATTN_OK.
+ */
+attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int T, int h, int h_kv, int d_h, int causal, float scale,
+                           attn_dtype_t dtype, void* stream);
+
+/*
+ * attn_decode_split_plan -- how one row's keys are cut into splits.
+ * Follows [DEC] "Segment length, and the early exit": a row of seq_len keys
+ * has n_pages = ceil(seq_len / page_size) pages; with at most num_splits
+ * splits each split covers pages_per_split = ceil(n_pages / num_splits)
+ * consecutive pages and the number of splits that do work is
+ * ceil(n_pages / pages_per_split) (0 for an empty row); surplus splits return
+ * at once. The decode kernel and its reduce use this same function.
+ * Host-only, pure. Returns the active split count; writes pages_per_split if
+ * the pointer is non-NULL. Returns -1 on invalid arguments.
+ */
+int attn_decode_split_plan(int seq_len, int page_size, int num_splits, int* pages_per_split);
+
+/*
+ * attn_recommended_splits -- split count for a decode batch on a GPU with
+ * num_sms SMs. Follows [DEC] "The grid" (fill the first wave:
+ * S* = ceil(N_SM / G_2D) with G_2D = B * h_kv) and, for ragged batches, caps
+ * the largest split so that the longest row does not dominate: with the total
+ * page count known, splits are also raised until the longest row's split is
+ * no larger than a quarter of the mean work per CTA slot. Result in
+ * [1, ATTN_MAX_SPLITS]. Host-only, pure; -1 on invalid arguments.
+ * total_seq_len may be 0 when unknown (then only the first-wave rule applies).
+ */
+#define ATTN_MAX_SPLITS 1024
+int attn_recommended_splits(int B, int h_kv, int max_seq_len, long long total_seq_len,
+                            int num_sms);
+
+/*
+ * attn_decode_workspace_bytes -- bytes of scratch that attn_decode_paged needs
+ * for the split partial states ([DEC] "What the merge costs": one fp32
+ * d_h-vector plus two fp32 scalars per (row, head, split)):
+ *   O~ fp32 [B*h, num_splits, d_h], then m fp32 [B*h, num_splits], then
+ *   l fp32 [B*h, num_splits], each region starting on a 256-byte boundary.
+ * Host-only, pure; 0 on invalid arguments.
+ */
+size_t attn_decode_workspace_bytes(int B, int h, int d_h, int num_splits);
+
+/*
+ * attn_decode_paged -- split-KV (FlashDecoding) attention of one query token
+ * per row over a paged KV cache, then the reduce of the split partials.
+ * Follows [DEC] throughout: stage 1 gives each (row, KV head, split) its own
+ * CTA, which runs the online recurrence over its pages for all g query heads
+ * of the KV head ("Where GQA enters") and stores the unnormalised partial
+ * (O~, m, l); stage 2 (the same kernel as attn_merge_states) takes the
+ * overall max, rescales, sums and divides once. Page translation ([DEC],
+ * paged addressing): key position p of row b is slot p % page_size of
+ * physical page block_table[b * max_blocks_per_seq + p / page_size].
+ *
+ *   q           [B, h, d_h]                              bf16 (read)
+ *   k_cache,
+ *   v_cache     [num_blocks, page_size, h_kv, d_h]       bf16 (read)
+ *   block_table [B, max_blocks_per_seq]                  int32 (read); entries
+ *               for pages >= ceil(seq_len/page_size) are never read
+ *   seq_lens    [B]                                      int32 (read), >= 0
+ *   workspace   attn_decode_workspace_bytes(B,h,d_h,num_splits) bytes (scratch)
+ *   o           [B, h, d_h]                              bf16 (written)
+ *   lse         [B, h]                 fp32, may be NULL (written)
+ * page_size must be 16; d_h must be 128 or 64; g = h / h_kv in {1,2,4,8};
+ * 1 <= num_splits <= ATTN_MAX_SPLITS; B <= 65535; scale finite and > 0. The launch geometry depends only on
+ * (B, h_kv, num_splits), never on the lengths, so the call can be captured
+ * in a CUDA graph and replayed with new lengths ([DEC] "CUDA graphs need the
+ * split count pinned"). A row with seq_len 0 gives o = 0, lse = -inf. A
+ * table entry outside [0, num_blocks) is treated as a page of zeros and sets
+ * ATTN_DEVERR_BAD_PAGE. A seq_len below 0 or above max_blocks_per_seq *
+ * page_size is clamped into that range and sets ATTN_DEVERR_BAD_SEQ_LEN.
+ * Errors: INVALID_ARG for NULL pointers (B > 0), bad sizes, misalignment or
+ * workspace_bytes too small; UNSUPPORTED for other d_h / g / page_size.
+ */
+attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* v_cache,
+                                const int32_t* block_table, const int32_t* seq_lens,
+                                int B, int h, int h_kv, int d_h, int page_size, int num_blocks,
+                                int max_blocks_per_seq, int num_splits, float scale,
+                                void* workspace, size_t workspace_bytes,
+                                void* o, float* lse, void* stream);
+
+/*
+ * attn_merge_states -- N-way merge of split partial states, one output row
+ * per input row. Follows [DEC] stage 2 ("reduce_segments") and [MRG]: over
+ * the row's active splits i < n_active[row], M = max m_i, w_i = exp(m_i - M),
+ * L = sum w_i l_i, o = (sum w_i O~_i) / L, lse = M + ln L. A row with no
+ * active split or with M = -inf takes a branch (no -inf - -inf) and yields
+ * o = 0, lse = -inf ([NA] "The base case is a NaN factory").
+ *
+ *   o_part   [rows, num_splits, d_h]  fp32 unnormalised accumulators (read)
+ *   m_part   [rows, num_splits]       fp32 running max, natural-log units (read)
+ *   l_part   [rows, num_splits]       fp32 normaliser referenced to m (read)
+ *   n_active [rows] int32, may be NULL (= all num_splits active); splits at
+ *            or past n_active[row] are never read
+ *   o        [rows, d_h]  out_dtype (bf16 or fp32)          (written)
+ *   lse      [rows]       fp32, may be NULL                 (written)
+ * d_h must be 64 or 128. rows == 0 is a no-op.
+ */
+attn_status_t attn_merge_states(const float* o_part, const float* m_part, const float* l_part,
+                                const int32_t* n_active, int rows, int num_splits, int d_h,
+                                void* o, float* lse, attn_dtype_t out_dtype, void* stream);
+
+/*
+ * attn_get_device_error -- synchronise `stream`, then read and clear the
+ * device error word of every kernel module (ATTN_DEVERR_* bits, 0 = none)
+ * into *bits. Returns ATTN_ERR_CUDA if the synchronisation fails.
+ */
+attn_status_t attn_get_device_error(void* stream, unsigned int* bits);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ONLINE_SOFTMAX_ATTN_GB300_ATTN_H_ */

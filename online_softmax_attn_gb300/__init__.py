@@ -1,0 +1,214 @@
+"""Thin Python binding of the GB300 exact-attention C ABI (``include/attn.h``).
+
+Every function here only marshals arguments: it checks tensor shapes/dtypes,
+allocates outputs with PyTorch (device memory is PyTorch's job), and calls the
+C entry point of the same name on the current CUDA stream. All arithmetic runs
+in the library's CUDA kernels; there is no CPU fallback. If the compiled
+library is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+from .build import LIB_PATH
+
+__all__ = [
+    "AttnError",
+    "attn_prefill",
+    "attn_decode_paged",
+    "attn_merge_states",
+    "attn_decode_split_plan",
+    "attn_recommended_splits",
+    "attn_decode_workspace_bytes",
+    "attn_get_device_error",
+    "attn_status_string",
+    "library",
+    "ATTN_MAX_SPLITS",
+]
+
+ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_DEVICE = range(5)
+ATTN_DTYPE_F32, ATTN_DTYPE_BF16 = 0, 1
+ATTN_MAX_SPLITS = 1024
+DEVERR_NAMES = {0x1: "wait timeout", 0x2: "page index outside cache",
+                0x4: "tensor-memory allocation", 0x8: "seq_len outside table row"}
+
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn} failed: {attn_status_string(status)} (status {status})")
+
+
+def library() -> ctypes.CDLL:
+    """Load the compiled library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            f"CUDA library not built: {LIB_PATH} is missing "
+            "(run `python -m online_softmax_attn_gb300.build`)")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I, F, S, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_longlong
+    lib.attn_status_string.argtypes = [I]
+    lib.attn_status_string.restype = ctypes.c_char_p
+    lib.attn_version.restype = I
+    lib.attn_prefill.argtypes = [P, P, P, P, P, I, I, I, I, I, F, I, P]
+    lib.attn_prefill.restype = I
+    lib.attn_decode_split_plan.argtypes = [I, I, I, ctypes.POINTER(I)]
+    lib.attn_decode_split_plan.restype = I
+    lib.attn_recommended_splits.argtypes = [I, I, I, Z, I]
+    lib.attn_recommended_splits.restype = I
+    lib.attn_decode_workspace_bytes.argtypes = [I, I, I, I]
+    lib.attn_decode_workspace_bytes.restype = S
+    lib.attn_decode_paged.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, F, P, S, P, P, P]
+    lib.attn_decode_paged.restype = I
+    lib.attn_merge_states.argtypes = [P, P, P, P, I, I, I, P, P, I, P]
+    lib.attn_merge_states.restype = I
+    lib.attn_get_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint)]
+    lib.attn_get_device_error.restype = I
+    _lib = lib
+    return lib
+
+
+def attn_status_string(status: int) -> str:
+    return library().attn_status_string(int(status)).decode()
+
+
+def _check(fn, status):
+    if status != ATTN_OK:
+        raise AttnError(fn, status)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(cond, msg):
+    if not cond:
+        raise ValueError(msg)
+
+
+def attn_prefill(q, k, v, causal: bool, scale: float | None = None, o=None, lse=None,
+                 return_lse: bool = True, stream=None):
+    """Exact attention prefill. q [h,T,d], k/v [h_kv,T,d] (bf16 or fp32, CUDA,
+    contiguous). Returns (o [h,T,d] in q's dtype, lse [h,T] fp32 or None)."""
+    _need(q.is_cuda and k.is_cuda and v.is_cuda, "tensors must be on a CUDA device")
+    _need(q.dim() == 3 and k.dim() == 3 and v.shape == k.shape, "expected q [h,T,d], k/v [h_kv,T,d]")
+    _need(q.dtype == k.dtype == v.dtype and q.dtype in (torch.bfloat16, torch.float32),
+          "q, k, v must share dtype bf16 or fp32")
+    _need(q.is_contiguous() and k.is_contiguous() and v.is_contiguous(), "tensors must be contiguous")
+    h, T, d = q.shape
+    h_kv = k.shape[0]
+    _need(k.shape[1] == T and k.shape[2] == d, "q and k/v disagree in T or d")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((h, T), dtype=torch.float32, device=q.device)
+    dt = ATTN_DTYPE_BF16 if q.dtype == torch.bfloat16 else ATTN_DTYPE_F32
+    st = library().attn_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), T, h, h_kv, d,
+                                int(bool(causal)), scale, dt, _stream(stream))
+    _check("attn_prefill", st)
+    return o, lse
+
+
+def attn_decode_split_plan(seq_len: int, num_splits: int, page_size: int = 16):
+    """(active splits, pages per split) for one row; pure host logic."""
+    pps = ctypes.c_int(0)
+    n = library().attn_decode_split_plan(int(seq_len), int(page_size), int(num_splits),
+                                         ctypes.byref(pps))
+    if n < 0:
+        raise ValueError("invalid split-plan arguments")
+    return n, pps.value
+
+
+def attn_recommended_splits(B: int, h_kv: int, max_seq_len: int, total_seq_len: int = 0,
+                            num_sms: int | None = None) -> int:
+    if num_sms is None:
+        num_sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    s = library().attn_recommended_splits(int(B), int(h_kv), int(max_seq_len), int(total_seq_len),
+                                          int(num_sms))
+    if s < 1:
+        raise ValueError("invalid arguments to attn_recommended_splits")
+    return s
+
+
+def attn_decode_workspace_bytes(B: int, h: int, d_h: int, num_splits: int) -> int:
+    return int(library().attn_decode_workspace_bytes(int(B), int(h), int(d_h), int(num_splits)))
+
+
+def attn_decode_paged(q, k_cache, v_cache, block_table, seq_lens, num_splits: int,
+                      scale: float | None = None, workspace=None, o=None, lse=None,
+                      return_lse: bool = True, stream=None):
+    """Split-KV paged decode. q [B,h,d] bf16; caches [num_blocks,16,h_kv,d] bf16;
+    block_table [B,max_blocks] int32; seq_lens [B] int32 (all CUDA, contiguous).
+    Returns (o [B,h,d] bf16, lse [B,h] fp32 or None)."""
+    for t in (q, k_cache, v_cache, block_table, seq_lens):
+        _need(t.is_cuda and t.is_contiguous(), "decode tensors must be contiguous CUDA tensors")
+    _need(q.dtype == k_cache.dtype == v_cache.dtype == torch.bfloat16, "q and caches must be bf16")
+    _need(block_table.dtype == torch.int32 and seq_lens.dtype == torch.int32,
+          "block_table and seq_lens must be int32")
+    B, h, d = q.shape
+    nb, page, h_kv, d2 = k_cache.shape
+    _need(d2 == d and v_cache.shape == k_cache.shape, "cache shape mismatch")
+    _need(block_table.dim() == 2 and block_table.shape[0] == B and seq_lens.shape == (B,),
+          "block_table [B,max_blocks] and seq_lens [B] expected")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    need = attn_decode_workspace_bytes(B, h, d, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, h), dtype=torch.float32, device=q.device)
+    st = library().attn_decode_paged(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens), B, h, h_kv, d,
+        page, nb, block_table.shape[1], int(num_splits), scale, _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(o), _ptr(lse), _stream(stream))
+    _check("attn_decode_paged", st)
+    return o, lse
+
+
+def attn_merge_states(o_part, m_part, l_part, n_active=None, out_dtype=torch.bfloat16, o=None,
+                      lse=None, return_lse: bool = True, stream=None):
+    """N-way merge of split partials: o_part [rows,S,d] fp32, m_part/l_part
+    [rows,S] fp32, n_active [rows] int32 or None. Returns (o [rows,d], lse [rows])."""
+    for t in (o_part, m_part, l_part):
+        _need(t.is_cuda and t.is_contiguous() and t.dtype == torch.float32,
+              "partials must be contiguous fp32 CUDA tensors")
+    rows, S, d = o_part.shape
+    _need(m_part.shape == (rows, S) and l_part.shape == (rows, S), "m/l must be [rows, S]")
+    if n_active is not None:
+        _need(n_active.is_cuda and n_active.dtype == torch.int32 and n_active.shape == (rows,),
+              "n_active must be int32 [rows] on the device")
+    _need(out_dtype in (torch.bfloat16, torch.float32), "out_dtype must be bf16 or fp32")
+    if o is None:
+        o = torch.empty((rows, d), dtype=out_dtype, device=o_part.device)
+    if lse is None and return_lse:
+        lse = torch.empty((rows,), dtype=torch.float32, device=o_part.device)
+    dt = ATTN_DTYPE_BF16 if out_dtype == torch.bfloat16 else ATTN_DTYPE_F32
+    st = library().attn_merge_states(_ptr(o_part), _ptr(m_part), _ptr(l_part), _ptr(n_active),
+                                     rows, S, d, _ptr(o), _ptr(lse), dt, _stream(stream))
+    _check("attn_merge_states", st)
+    return o, lse
+
+
+def attn_get_device_error(stream=None) -> int:
+    """Synchronise the stream; return and clear the device error bits."""
+    bits = ctypes.c_uint(0)
+    st = library().attn_get_device_error(_stream(stream), ctypes.byref(bits))
+    _check("attn_get_device_error", st)
+    return bits.value

@@ -1,0 +1,204 @@
+// api.cu -- the C ABI declared in include/attn.h: host-side validation,
+// workspace carve-up, tensor-map encoding and kernel launches. No entry point
+// allocates, frees or synchronises (except attn_get_device_error, which is a
+// synchronising query by contract).
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace attn {
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+attn_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
+
+}  // namespace
+
+CUresult encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, int rank, void* base,
+                           const uint64_t* dims, const uint64_t* strides_bytes,
+                           const uint32_t* box, CUtensorMapSwizzle swizzle) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return CUDA_ERROR_NOT_FOUND;
+  uint32_t elem_strides[5] = {1, 1, 1, 1, 1};
+  return fn(map, dtype, rank, base, dims, strides_bytes, box, elem_strides,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" {
+
+const char* attn_status_string(attn_status_t status) {
+  switch (status) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case ATTN_ERR_CUDA: return "CUDA error";
+    case ATTN_ERR_DEVICE: return "device-side error";
+  }
+  return "unknown status";
+}
+
+int attn_version(void) { return 100; }
+
+int attn_decode_split_plan(int seq_len, int page_size, int num_splits, int* pages_per_split) {
+  if (seq_len < 0 || page_size < 1 || num_splits < 1) return -1;
+  return split_plan(seq_len, page_size, num_splits, pages_per_split);
+}
+
+int attn_recommended_splits(int B, int h_kv, int max_seq_len, long long total_seq_len,
+                            int num_sms) {
+  if (B < 1 || h_kv < 1 || max_seq_len < 0 || total_seq_len < 0 || num_sms < 1) return -1;
+  const long long g2d = static_cast<long long>(B) * h_kv;
+  long long s = (num_sms + g2d - 1) / g2d;  // first-wave coverage
+  const long long max_pages = (max_seq_len + 15) / 16;
+  if (total_seq_len > 0) {
+    // Ragged batch: keep the longest row's split below a quarter of the mean
+    // work per SM, so that the tail of the longest rows stays short.
+    const long long total_pages = ((total_seq_len + 15) / 16) * h_kv;
+    const long long mean_per_sm = (total_pages + num_sms - 1) / num_sms;
+    const long long target = mean_per_sm / 4 > 0 ? mean_per_sm / 4 : 1;
+    const long long s_bal = (max_pages + target - 1) / target;
+    if (s_bal > s) s = s_bal;
+  }
+  if (max_pages > 0 && s > max_pages) s = max_pages;
+  if (s < 1) s = 1;
+  if (s > ATTN_MAX_SPLITS) s = ATTN_MAX_SPLITS;
+  return static_cast<int>(s);
+}
+
+size_t attn_decode_workspace_bytes(int B, int h, int d_h, int num_splits) {
+  if (B < 0 || h < 1 || d_h < 1 || num_splits < 1) return 0;
+  return partial_layout(static_cast<long long>(B) * h, num_splits, d_h).total;
+}
+
+attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int T, int h, int h_kv, int d_h, int causal, float scale,
+                           attn_dtype_t dtype, void* stream) {
+  if (T < 0 || h < 1 || h_kv < 1 || h % h_kv != 0 || !std::isfinite(scale) || !(scale > 0.f))
+    return ATTN_ERR_INVALID_ARG;
+  if (h > 65535) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_DTYPE_F32 && dtype != ATTN_DTYPE_BF16) return ATTN_ERR_INVALID_ARG;
+  if (d_h != 64 && d_h != 128) return ATTN_ERR_UNSUPPORTED;
+  if (T == 0) return ATTN_OK;
+  if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(lse, 4))
+    return ATTN_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dtype == ATTN_DTYPE_F32)
+    return from_cuda(launch_prefill_f32(static_cast<const float*>(q),
+                                        static_cast<const float*>(k),
+                                        static_cast<const float*>(v), static_cast<float*>(o), lse,
+                                        T, h, h_kv, d_h, causal != 0, scale, s));
+  const cudaError_t e = launch_prefill_bf16(q, k, v, o, lse, T, h, h_kv, d_h, causal != 0, scale, s);
+  if (e == cudaErrorNotSupported) return ATTN_ERR_UNSUPPORTED;
+  return from_cuda(e);
+}
+
+attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* v_cache,
+                                const int32_t* block_table, const int32_t* seq_lens, int B, int h,
+                                int h_kv, int d_h, int page_size, int num_blocks,
+                                int max_blocks_per_seq, int num_splits, float scale,
+                                void* workspace, size_t workspace_bytes, void* o, float* lse,
+                                void* stream) {
+  if (B < 0 || h < 1 || h_kv < 1 || h % h_kv != 0 || num_blocks < 1 || max_blocks_per_seq < 1 ||
+      num_splits < 1 || num_splits > ATTN_MAX_SPLITS || !std::isfinite(scale) || !(scale > 0.f))
+    return ATTN_ERR_INVALID_ARG;
+  if (B > 65535 || h_kv > 65535) return ATTN_ERR_INVALID_ARG;
+  const int g = h / h_kv;
+  if ((d_h != 64 && d_h != 128) || page_size != 16 || (g != 1 && g != 2 && g != 4 && g != 8))
+    return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(max_blocks_per_seq) * page_size > (1ll << 30))
+    return ATTN_ERR_INVALID_ARG;
+  if (B == 0) return ATTN_OK;
+  if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !workspace || !o)
+    return ATTN_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(o, 16) ||
+      !aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(lse, 4) ||
+      !aligned(workspace, 256))
+    return ATTN_ERR_INVALID_ARG;
+  const long long rows = static_cast<long long>(B) * h;
+  const PartialLayout L = partial_layout(rows, num_splits, d_h);
+  if (workspace_bytes < L.total) return ATTN_ERR_INVALID_ARG;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  DecodeArgs a;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.B = B;
+  a.h = h;
+  a.h_kv = h_kv;
+  a.d_h = d_h;
+  a.page_size = page_size;
+  a.num_blocks = num_blocks;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.num_splits = num_splits;
+  a.scale = scale;
+  a.o_part = reinterpret_cast<float*>(ws + L.o_off);
+  a.m_part = reinterpret_cast<float*>(ws + L.m_off);
+  a.l_part = reinterpret_cast<float*>(ws + L.l_off);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_decode_split(a, s);
+  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  e = launch_merge(a.o_part, a.m_part, a.l_part, nullptr, seq_lens, h, page_size,
+                   max_blocks_per_seq * page_size, static_cast<int>(rows), num_splits, d_h, o, lse,
+                   ATTN_DTYPE_BF16, s);
+  return from_cuda(e);
+}
+
+attn_status_t attn_merge_states(const float* o_part, const float* m_part, const float* l_part,
+                                const int32_t* n_active, int rows, int num_splits, int d_h,
+                                void* o, float* lse, attn_dtype_t out_dtype, void* stream) {
+  if (rows < 0 || num_splits < 1) return ATTN_ERR_INVALID_ARG;
+  if (out_dtype != ATTN_DTYPE_F32 && out_dtype != ATTN_DTYPE_BF16) return ATTN_ERR_INVALID_ARG;
+  if (d_h != 64 && d_h != 128) return ATTN_ERR_UNSUPPORTED;
+  if (rows == 0) return ATTN_OK;
+  if (!o_part || !m_part || !l_part || !o) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(o_part, 16) || !aligned(m_part, 4) || !aligned(l_part, 4) || !aligned(o, 16) ||
+      !aligned(n_active, 4) || !aligned(lse, 4))
+    return ATTN_ERR_INVALID_ARG;
+  return from_cuda(launch_merge(o_part, m_part, l_part, n_active, nullptr, 1, 16, 0, rows,
+                                num_splits, d_h, o, lse, out_dtype,
+                                static_cast<cudaStream_t>(stream)));
+}
+
+attn_status_t attn_get_device_error(void* stream, unsigned int* bits) {
+  if (bits == nullptr) return ATTN_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e1 = cudaSuccess, e2 = cudaSuccess, e3 = cudaSuccess;
+  unsigned int v = decode_read_and_clear_error(s, &e1);
+  v |= merge_read_and_clear_error(s, &e2);
+  v |= prefill_read_and_clear_error(s, &e3);
+  *bits = v;
+  if (e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess) return ATTN_ERR_CUDA;
+  return ATTN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,73 @@
+// internal.h -- launchers between the C-ABI layer (api.cu) and the kernel
+// translation units. Arguments are already validated when these are called.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "attn.h"
+
+namespace attn {
+
+// Partial-state workspace carve-up: O~ [rows, S, d], m [rows, S], l [rows, S].
+struct PartialLayout {
+  size_t o_off, m_off, l_off, total;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+inline PartialLayout partial_layout(long long rows, int num_splits, int d_h) {
+  PartialLayout L;
+  L.o_off = 0;
+  L.m_off = align256(size_t(rows) * num_splits * d_h * sizeof(float));
+  L.l_off = L.m_off + align256(size_t(rows) * num_splits * sizeof(float));
+  L.total = L.l_off + align256(size_t(rows) * num_splits * sizeof(float));
+  return L;
+}
+
+// merge.cu -----------------------------------------------------------------
+// n_active == nullptr and seq_lens == nullptr: all splits active.
+// seq_lens != nullptr: n_active(row) = split_plan(seq_lens[row / heads_per_seq]),
+// with the length clamped into [0, max_len] exactly as the decode kernel does.
+cudaError_t launch_merge(const float* o_part, const float* m_part, const float* l_part,
+                         const int32_t* n_active, const int32_t* seq_lens, int heads_per_seq,
+                         int page_size, int max_len, int rows, int num_splits, int d_h, void* o, float* lse,
+                         attn_dtype_t out_dtype, cudaStream_t stream);
+unsigned int merge_read_and_clear_error(cudaStream_t stream, cudaError_t* st);
+
+// decode.cu ----------------------------------------------------------------
+struct DecodeArgs {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  int B, h, h_kv, d_h, page_size, num_blocks, max_blocks_per_seq, num_splits;
+  float scale;
+  float* o_part;
+  float* m_part;
+  float* l_part;
+};
+cudaError_t launch_decode_split(const DecodeArgs& a, cudaStream_t stream);
+unsigned int decode_read_and_clear_error(cudaStream_t stream, cudaError_t* st);
+
+// prefill_simt.cu ----------------------------------------------------------
+cudaError_t launch_prefill_f32(const float* q, const float* k, const float* v, float* o,
+                               float* lse, int T, int h, int h_kv, int d_h, int causal,
+                               float scale, cudaStream_t stream);
+
+// prefill_tc.cu --------------------------------------------------------------
+cudaError_t launch_prefill_bf16(const void* q, const void* k, const void* v, void* o, float* lse,
+                                int T, int h, int h_kv, int d_h, int causal, float scale,
+                                cudaStream_t stream);
+unsigned int prefill_read_and_clear_error(cudaStream_t stream, cudaError_t* st);
+
+// tensor maps ---------------------------------------------------------------
+// Encodes a tiled tensor map through the driver entry point (no libcuda link).
+CUresult encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, int rank, void* base,
+                           const uint64_t* dims, const uint64_t* strides_bytes,
+                           const uint32_t* box, CUtensorMapSwizzle swizzle);
+
+}  // namespace attn

@@ -1,0 +1,152 @@
+// merge.cu -- N-way merge of split partial states (the reduce stage of
+// split-KV decoding, also exported on its own as attn_merge_states).
+//
+// Math ("Decode attention: FlashDecoding, split-K, paged kernels", stage 2 of
+// the split: take the overall max, rescale each split's l_i and O~_i by
+// exp(m_i - M), sum, divide once; and "Merge normalized attention without
+// averaging tile outputs": branch around the all-empty case instead of
+// evaluating -inf - (-inf)).
+//
+// Layout: one warp per output row; lane j owns d_h/32 consecutive output
+// elements, so each split's O~ row is read as one coalesced 128-bit (d_h=128)
+// or 64-bit (d_h=64) access per lane. The split weights are computed 32 at a
+// time, one per lane, and broadcast with shuffles, so the loop over splits
+// carries no dependent global load.
+#include "common.cuh"
+#include "internal.h"
+
+namespace attn {
+
+static __device__ unsigned int g_merge_err;
+
+template <int D, bool kOutBf16>
+__global__ void __launch_bounds__(256)
+    merge_states_kernel(const float* __restrict__ o_part, const float* __restrict__ m_part,
+                        const float* __restrict__ l_part, const int32_t* __restrict__ n_active,
+                        const int32_t* __restrict__ seq_lens, int heads_per_seq, int page_size,
+                        int max_len, int rows, int S, void* __restrict__ o_out, float* __restrict__ lse_out) {
+  constexpr int VEC = D / 32;
+  static_assert(VEC == 2 || VEC == 4, "d_h must be 64 or 128");
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= rows) return;
+
+  int n;
+  if (n_active != nullptr) {
+    n = n_active[row];
+  } else if (seq_lens != nullptr) {
+    const int len = clamp_seq_len(seq_lens[row / heads_per_seq], max_len, &g_merge_err);
+    n = split_plan(len, page_size, S, nullptr);
+  } else {
+    n = S;
+  }
+  n = max(0, min(n, S));
+
+  const float* mrow = m_part + size_t(row) * S;
+  const float* lrow = l_part + size_t(row) * S;
+  const float* orow = o_part + size_t(row) * S * D + lane * VEC;
+
+  // Overall max over the active splits.
+  float M = -INFINITY;
+  for (int i = lane; i < n; i += 32) M = fmaxf(M, mrow[i]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+
+  float acc[VEC];
+#pragma unroll
+  for (int e = 0; e < VEC; ++e) acc[e] = 0.f;
+  float L = 0.f;
+  if (M != -INFINITY) {  // at least one non-empty split; no -inf - -inf below
+    const float Mb = M * kLog2e;
+    for (int c = 0; c < n; c += 32) {
+      const int i = c + lane;
+      float w = 0.f;
+      if (i < n) {
+        const float mi = mrow[i];
+        w = (mi == -INFINITY) ? 0.f : ex2_approx(fmaf(mi, kLog2e, -Mb));
+        L = fmaf(w, lrow[i], L);
+      }
+      const int cnt = min(32, n - c);
+#pragma unroll 4
+      for (int j = 0; j < cnt; ++j) {
+        const float wj = __shfl_sync(0xffffffffu, w, j);
+        const float* src = orow + size_t(c + j) * D;
+        if constexpr (VEC == 4) {
+          const float4 t = __ldg(reinterpret_cast<const float4*>(src));
+          acc[0] = fmaf(wj, t.x, acc[0]);
+          acc[1] = fmaf(wj, t.y, acc[1]);
+          acc[2] = fmaf(wj, t.z, acc[2]);
+          acc[3] = fmaf(wj, t.w, acc[3]);
+        } else {
+          const float2 t = __ldg(reinterpret_cast<const float2*>(src));
+          acc[0] = fmaf(wj, t.x, acc[0]);
+          acc[1] = fmaf(wj, t.y, acc[1]);
+        }
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+  }
+
+  const bool empty = !(L > 0.f);  // also catches NaN mass
+  const float inv = empty ? 0.f : 1.f / L;
+#pragma unroll
+  for (int e = 0; e < VEC; ++e) acc[e] = empty ? 0.f : acc[e] * inv;
+
+  if constexpr (kOutBf16) {
+    uint32_t* dst = reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(o_out) +
+                                                size_t(row) * D + lane * VEC);
+    if constexpr (VEC == 4) {
+      uint2 pk;
+      pk.x = pack_bf16x2(acc[0], acc[1]);
+      pk.y = pack_bf16x2(acc[2], acc[3]);
+      *reinterpret_cast<uint2*>(dst) = pk;
+    } else {
+      dst[0] = pack_bf16x2(acc[0], acc[1]);
+    }
+  } else {
+    float* dst = static_cast<float*>(o_out) + size_t(row) * D + lane * VEC;
+    if constexpr (VEC == 4) {
+      *reinterpret_cast<float4*>(dst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    } else {
+      *reinterpret_cast<float2*>(dst) = make_float2(acc[0], acc[1]);
+    }
+  }
+  if (lse_out != nullptr && lane == 0) lse_out[row] = empty ? -INFINITY : M + logf(L);
+}
+
+cudaError_t launch_merge(const float* o_part, const float* m_part, const float* l_part,
+                         const int32_t* n_active, const int32_t* seq_lens, int heads_per_seq,
+                         int page_size, int max_len, int rows, int num_splits, int d_h, void* o, float* lse,
+                         attn_dtype_t out_dtype, cudaStream_t stream) {
+  if (rows <= 0) return cudaSuccess;
+  const int warps = 8;
+  const dim3 grid((rows + warps - 1) / warps);
+  const dim3 block(32 * warps);
+  const bool bf = out_dtype == ATTN_DTYPE_BF16;
+#define ATTN_MERGE_LAUNCH(D, BF)                                                            \
+  merge_states_kernel<D, BF><<<grid, block, 0, stream>>>(o_part, m_part, l_part, n_active, \
+                                                         seq_lens, heads_per_seq, page_size, \
+                                                         max_len, rows, num_splits, o, lse)
+  if (d_h == 128) {
+    if (bf) ATTN_MERGE_LAUNCH(128, true); else ATTN_MERGE_LAUNCH(128, false);
+  } else {
+    if (bf) ATTN_MERGE_LAUNCH(64, true); else ATTN_MERGE_LAUNCH(64, false);
+  }
+#undef ATTN_MERGE_LAUNCH
+  return cudaGetLastError();
+}
+
+unsigned int merge_read_and_clear_error(cudaStream_t stream, cudaError_t* st) {
+  unsigned int v = 0, zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_merge_err, sizeof(v), 0,
+                                            cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess)
+    e = cudaMemcpyToSymbolAsync(g_merge_err, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice,
+                                stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (st) *st = e;
+  return v;
+}
+
+}  // namespace attn

@@ -128,36 +128,43 @@ def attention_rows_ref(q, k, v, scale: float, causal: bool, heads, rows):
     return O, LSE
 
 
-def decode_paged_ref(q, k_cache, v_cache, block_table, seq_lens, scale: float):
+def decode_paged_ref(q, k_cache, v_cache, block_table, seq_lens, scale: float, rows=None):
     """One query token per row attending to its row's keys through a page table.
 
     [DEC] paged addressing: logical key position p of row b lives in physical
     page block_table[b][p // page_size] at slot p % page_size; the cache is
     laid out [page, slot, kv_head, d_h].  The keys 0 .. seq_len-1 are gathered
-    into a contiguous [h_kv, s, d_h] block, then the definition is applied.
+    into a contiguous [h_kv, s, d_h] block (upcast after gathering, so a large
+    pool is never widened as a whole), then the definition is applied.
     A row with seq_len 0 has no keys: zero output, LSE = -inf.
 
-    q [B, h, d_h] -> O [B, h, d_h], LSE [B, h] (float64).
+    q [B, h, d_h] -> O [B, h, d_h], LSE [B, h] (float64). With ``rows`` only
+    those rows are evaluated (the others stay 0 / -inf).
     """
     q64 = to_f64(q)
-    kc = to_f64(k_cache)
-    vc = to_f64(v_cache)
     table = np.asarray(block_table.cpu() if hasattr(block_table, "cpu") else block_table)
     lens = np.asarray(seq_lens.cpu() if hasattr(seq_lens, "cpu") else seq_lens).tolist()
     B, h, _ = q64.shape
-    d = vc.shape[3]
-    page = kc.shape[1]
+    d = v_cache.shape[3]
+    page = k_cache.shape[1]
     O = np.zeros((B, h, d), dtype=np.float64)
     LSE = np.full((B, h), EMPTY_M, dtype=np.float64)
-    for b in range(B):
+    for b in (range(B) if rows is None else rows):
         s = int(lens[b])
         if s == 0:
             continue
         pos = np.arange(s)
         phys = table[b, pos // page].astype(np.int64)
         slot = pos % page
-        K = kc[phys, slot].transpose(1, 0, 2)  # [h_kv, s, d]
-        V = vc[phys, slot].transpose(1, 0, 2)
+        if hasattr(k_cache, "detach"):
+            import torch  # the caches may be CPU torch tensors (bf16)
+
+            ip, isl = torch.from_numpy(phys), torch.from_numpy(slot)
+            K = to_f64(k_cache[ip, isl]).transpose(1, 0, 2)  # [h_kv, s, d]
+            V = to_f64(v_cache[ip, isl]).transpose(1, 0, 2)
+        else:
+            K = to_f64(k_cache[phys, slot]).transpose(1, 0, 2)
+            V = to_f64(v_cache[phys, slot]).transpose(1, 0, 2)
         o, lse = attention_ref(q64[b][:, None, :], K, V, scale, causal=False)
         O[b] = o[:, 0]
         LSE[b] = lse[:, 0]

@@ -1,0 +1,144 @@
+"""The C-ABI library builds, loads and exports what include/attn.h declares;
+host-only logic (split plan, split sizing, workspace size, argument
+validation) checked without a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import online_softmax_attn_gb300 as attn
+from online_softmax_attn_gb300 import build as attn_build
+from pins import golden
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    attn_build.build()
+    return attn.library()
+
+
+def declared_functions():
+    names = set()
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", f)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(attn_\w+)\s*\(", src))
+    return sorted(names)
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert "attn_prefill" in names and "attn_decode_paged" in names and "attn_merge_states" in names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+
+
+def test_exports_nothing_undeclared(lib):
+    import subprocess
+
+    out = subprocess.run(["nm", "-D", "--defined-only", attn_build.LIB_PATH],
+                         capture_output=True, text=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if " T attn_" in l}
+    assert exported == set(declared_functions())
+
+
+def test_status_strings(lib):
+    for s in range(5):
+        assert attn.attn_status_string(s)
+    assert attn.attn_status_string(99) == "unknown status"
+
+
+def test_split_plan_matches_pages():
+    g = golden("split_sizing.json")
+    for seg in g["segments"]:
+        n, pps = attn.attn_decode_split_plan(seg["seq_len"], seg["max_splits"])
+        assert n == seg["active"]
+        if "pages_per_split" in seg:
+            assert pps == seg["pages_per_split"]
+            first = (0, pps * 16 - 1)
+            last = ((n - 1) * pps * 16, seg["seq_len"] - 1)
+            assert list(first) == seg["first_split_keys"]
+            assert list(last) == seg["last_split_keys"]
+
+
+def test_split_plan_covers_every_page_once():
+    for s in [0, 1, 15, 16, 17, 255, 256, 257, 2560, 32768, 16384]:
+        for S in [1, 2, 3, 16, 17, 64, 132, 1024]:
+            n, pps = attn.attn_decode_split_plan(s, S)
+            pages = (s + 15) // 16
+            assert n <= S
+            if pages == 0:
+                assert n == 0
+                continue
+            covered = [p for i in range(n) for p in range(i * pps, min((i + 1) * pps, pages))]
+            assert covered == list(range(pages))
+            assert all(i * pps < pages for i in range(n))  # every active split has work
+
+
+def test_workspace_bytes_match_pages():
+    g = golden("split_sizing.json")
+    p = g["partial_bytes_B1_h32"]
+    assert attn.attn_decode_workspace_bytes(p["B"], p["h"], p["d_h"], p["S"]) == p["bytes"]
+    per = g["partial_bytes_per_token_head"]
+    assert attn.attn_decode_workspace_bytes(1, 1, per["d_h"], per["S"]) >= per["bytes"]
+    assert attn.attn_decode_workspace_bytes(0, 1, 128, 1) == 0
+
+
+def test_first_wave_split_count():
+    g = golden("split_sizing.json")
+    for case in g["first_wave_splits"]:
+        # G_2D = B * h_kv at B = 1
+        assert attn.attn_recommended_splits(1, case["g2d"], 1 << 20, 0, case["n_sm"]) == case["splits"]
+
+
+def test_recommended_splits_ragged_batch_balances():
+    s = attn.attn_recommended_splits(66, 8, 16384, 64 * 8192, 152)
+    assert s >= 2
+    # Longest row's split is at most a quarter of the mean work per SM.
+    pages_max = 16384 // 16
+    mean_per_sm = (64 * 8192 // 16) * 8 / 152
+    assert pages_max / s <= mean_per_sm / 4 + 1
+
+
+def test_invalid_arguments_rejected_before_launch(lib):
+    P = ctypes.c_void_p
+    dummy = P(256)  # never dereferenced: validation fails first
+    S = attn.attn_status_string
+    bad = attn.ATTN_ERR_INVALID_ARG
+    # h not a multiple of h_kv
+    assert lib.attn_prefill(dummy, dummy, dummy, dummy, None, 64, 6, 4, 128, 1, 0.1, 1, None) == bad
+    # negative T, non-positive scale, NaN scale
+    assert lib.attn_prefill(dummy, dummy, dummy, dummy, None, -1, 4, 4, 128, 1, 0.1, 1, None) == bad
+    assert lib.attn_prefill(dummy, dummy, dummy, dummy, None, 64, 4, 4, 128, 1, 0.0, 1, None) == bad
+    assert lib.attn_prefill(dummy, dummy, dummy, dummy, None, 64, 4, 4, 128, 1, float("nan"), 1, None) == bad
+    # misaligned pointer
+    assert lib.attn_prefill(P(258), dummy, dummy, dummy, None, 64, 4, 4, 128, 1, 0.1, 1, None) == bad
+    # unsupported head size
+    assert lib.attn_prefill(dummy, dummy, dummy, dummy, None, 64, 4, 4, 96, 1, 0.1, 1, None) == \
+        attn.ATTN_ERR_UNSUPPORTED
+    # T = 0 is a no-op
+    assert lib.attn_prefill(None, None, None, None, None, 0, 4, 4, 128, 1, 0.1, 1, None) == 0
+    # decode: workspace too small, page size, group size, split count
+    args = [dummy, dummy, dummy, dummy, dummy, 2, 32, 8, 128, 16, 100, 10, 16, 0.1, dummy, 16,
+            dummy, None, None]
+    assert lib.attn_decode_paged(*args) == bad
+    a2 = list(args); a2[9] = 32
+    assert lib.attn_decode_paged(*a2) == attn.ATTN_ERR_UNSUPPORTED
+    a3 = list(args); a3[6] = 3
+    assert lib.attn_decode_paged(*a3) == bad  # 32 % 3 != 0
+    a4 = list(args); a4[12] = 0
+    assert lib.attn_decode_paged(*a4) == bad
+    a5 = list(args); a5[12] = attn.ATTN_MAX_SPLITS + 1
+    assert lib.attn_decode_paged(*a5) == bad
+    a6 = list(args); a6[5] = 0
+    assert lib.attn_decode_paged(*a6) == 0  # B = 0 is a no-op
+    # merge: bad dtype, bad d_h, rows 0
+    assert lib.attn_merge_states(dummy, dummy, dummy, None, 4, 2, 128, dummy, None, 7, None) == bad
+    assert lib.attn_merge_states(dummy, dummy, dummy, None, 4, 2, 80, dummy, None, 1, None) == \
+        attn.ATTN_ERR_UNSUPPORTED
+    assert lib.attn_merge_states(None, None, None, None, 0, 2, 128, None, None, 1, None) == 0
+    assert S(bad) == "invalid argument"

@@ -1,0 +1,126 @@
+"""attn_prefill (CUDA: tcgen05 bf16 path and fp32 SIMT path) against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import online_softmax_attn_gb300 as attn
+import oracle
+import workloads as W
+from parity import check_lse, check_out
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from online_softmax_attn_gb300 import build
+
+    build.build()
+
+
+def run(q, k, v, causal, scale):
+    o, lse = attn.attn_prefill(q.cuda(), k.cuda(), v.cuda(), causal, scale)
+    torch.cuda.synchronize()
+    return o, lse
+
+
+def test_single_head_fp32_T256():
+    """The fp32 single-head workload, exactly as specified, full comparison."""
+    shape = W.SINGLE_HEAD_T256
+    for seed in range(3):
+        q, k, v = W.prefill_inputs(shape, seed)
+        O_ref, L_ref = oracle.attention_ref(q, k, v, shape.scale, causal=False)
+        o, lse = run(q, k, v, False, shape.scale)
+        check_out(o, O_ref, torch.float32)
+        check_lse(lse, L_ref)
+
+
+@pytest.mark.parametrize("h,h_kv,d,T,causal", [
+    (4, 2, 128, 300, True),
+    (4, 2, 64, 257, False),
+    (2, 2, 128, 129, True),
+    (3, 1, 64, 64, True),
+])
+def test_fp32_path_shapes(h, h_kv, d, T, causal):
+    shape = W.PrefillShape("t", h, h_kv, d, T, torch.float32, causal)
+    q, k, v = W.prefill_inputs(shape, 7)
+    O_ref, L_ref = oracle.attention_ref(q, k, v, shape.scale, causal)
+    o, lse = run(q, k, v, causal, shape.scale)
+    check_out(o, O_ref, torch.float32)
+    check_lse(lse, L_ref)
+
+
+@pytest.mark.parametrize("h,h_kv,d,T,causal", [
+    (8, 2, 128, 640, True),    # GQA g=4, several tiles, head pairs
+    (8, 2, 128, 333, True),    # ragged tail
+    (8, 2, 128, 333, False),
+    (2, 2, 128, 300, True),    # g=1: one head per CTA
+    (6, 2, 128, 200, False),   # g=3: one head per CTA
+    (4, 2, 64, 257, True),     # d_h = 64
+    (4, 4, 64, 130, False),
+    (4, 1, 128, 1, True),      # T = 1
+    (4, 1, 128, 127, True),
+    (4, 1, 128, 128, False),
+    (4, 1, 128, 129, True),
+])
+def test_bf16_tc_shapes(h, h_kv, d, T, causal):
+    shape = W.PrefillShape("t", h, h_kv, d, T, torch.bfloat16, causal)
+    q, k, v = W.prefill_inputs(shape, 11)
+    O_ref, L_ref = oracle.attention_ref(q, k, v, shape.scale, causal)
+    o, lse = run(q, k, v, causal, shape.scale)
+    check_out(o, O_ref, torch.bfloat16)
+    check_lse(lse, L_ref)
+    assert attn.attn_get_device_error() == 0
+
+
+def test_bf16_late_outlier_forces_rescale():
+    """A key near the end of the row dominates: the running max jumps late."""
+    shape = W.PrefillShape("t", 4, 2, 128, 512, torch.bfloat16, False)
+    q, k, v = W.prefill_inputs(shape, 3)
+    k[:, 500] = (q[0, :1].float() * 3).to(torch.bfloat16)
+    O_ref, L_ref = oracle.attention_ref(q, k, v, shape.scale, False)
+    o, lse = run(q, k, v, False, shape.scale)
+    check_out(o, O_ref, torch.bfloat16)
+    check_lse(lse, L_ref)
+
+
+def test_gqa_T2048_causal_full():
+    """The Llama-3-8B GQA layer at T = 2048, causal; full comparison."""
+    shape = W.GQA_T2048_CAUSAL
+    q, k, v = W.prefill_inputs(shape, 0)
+    O_ref, L_ref = oracle.attention_ref(q, k, v, shape.scale, True)
+    o, lse = run(q, k, v, True, shape.scale)
+    err = check_out(o, O_ref, torch.bfloat16)
+    check_lse(lse, L_ref)
+    print(f"max abs err {err:.3e}")
+
+
+@pytest.mark.parametrize("shape", [W.GQA_T8192_CAUSAL, W.GQA_T8192_FULL], ids=lambda s: s.name)
+def test_gqa_T8192_sampled_rows(shape):
+    """T = 8192 with logits widened (Q, K x3); oracle on sampled rows that
+    include the first and last rows and rows in the last tile."""
+    q, k, v = W.prefill_inputs(shape, 0)
+    o, lse = run(q, k, v, shape.causal, shape.scale)
+    rng = np.random.default_rng(1)
+    rows = [0, 1, 127, 128, 4095, 8063, 8191] + rng.integers(0, shape.T, 25).tolist()
+    heads = [(i * 7) % shape.h for i in range(len(rows))]
+    O_ref, L_ref = oracle.attention_rows_ref(q, k, v, shape.scale, shape.causal, heads, rows)
+    check_out(o[heads, rows], O_ref, torch.bfloat16)
+    check_lse(lse[heads, rows], L_ref)
+
+
+def test_bf16_output_guard_bands_untouched():
+    shape = W.PrefillShape("t", 4, 2, 128, 200, torch.bfloat16, True)
+    q, k, v = W.prefill_inputs(shape, 5)
+    n = q.numel()
+    buf = torch.full((n + 4096,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    o = buf[2048:2048 + n].view_as(q)
+    lbuf = torch.full((4 * 200 + 256,), float("nan"), device="cuda")
+    lse = lbuf[128:128 + 800].view(4, 200)
+    attn.attn_prefill(q.cuda(), k.cuda(), v.cuda(), True, shape.scale, o=o, lse=lse)
+    torch.cuda.synchronize()
+    assert torch.all(torch.isnan(buf[:2048].float())) and torch.all(torch.isnan(buf[-2048:].float()))
+    assert torch.all(torch.isnan(lbuf[:128])) and torch.all(torch.isnan(lbuf[-128:]))
+    O_ref, L_ref = oracle.attention_ref(q, k, v, shape.scale, True)
+    check_out(o, O_ref, torch.bfloat16)
+    check_lse(lse, L_ref)
