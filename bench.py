@@ -1,0 +1,502 @@
+"""Benchmark of the exact-attention hot path on GB300.
+
+One step = one pass of the whole path over one batch of synthetic input:
+  1. prefill: Llama-3-8B GQA layer, h=32, h_kv=8, d_h=128, T=8192, causal,
+     bf16 Q/K/V ~ N(0,1) with Q and K x3 (widened logits);   [attn_prefill]
+  2. paged decode: 64 rows with lengths U[1,16384] plus 2 empty rows, h=32,
+     h_kv=8, d_h=128, bf16 KV in 16-token pages, shuffled physical pages,
+     split count from attn_recommended_splits;              [attn_decode_paged
+                                                            = split kernel + merge]
+L2 is flushed (a 512 MiB write) before each prefill; the decode streams a
+2.15 GB cache, far larger than L2.
+
+Prints ONE JSON line. `value` is prefill attention TFLOP/s (algorithmic FLOPs
+4*h*d_h*T(T+1)/2 over the prefill kernel's CUDA-event time, summed over all
+ranks); the `decode` object carries paged-decode KV GB/s.
+`--impl reference` times the float64 CPU oracle on a bounded sample instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "prefill attention TFLOP/s; paged decode KV GB/s (fraction of GB300 roofline)"
+PREFILL = W.GQA_T8192_CAUSAL
+DECODE = W.DECODE_PAGED_B64
+
+# DRAM traffic per launch from one ncu capture of the kernel (see profiles/),
+# valid only for the kernel source it was taken on (hash of its files).
+KERNEL_FILES = {
+    "prefill": ["online_softmax_attn_gb300/csrc/prefill_tc.cu", "online_softmax_attn_gb300/csrc/tc.cuh",
+                "online_softmax_attn_gb300/csrc/common.cuh"],
+    "decode": ["online_softmax_attn_gb300/csrc/decode.cu", "online_softmax_attn_gb300/csrc/common.cuh"],
+}
+NCU_TRAFFIC = {
+    # kind: (dram read + write bytes per launch, sha256[:16] of the kernel's files)
+    "prefill": (131.76e6, "22c37d609a8434e4"),  # profiles/prefill_bf16_T8192_causal.md
+}
+
+
+def src_hash(kind: str) -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_FILES[kind]:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kind: str):
+    rec = NCU_TRAFFIC.get(kind)
+    if rec is None or rec[1] != src_hash(kind):
+        return None
+    return rec[0]
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d["hbm_gbs"], d["bf16_tflops"], "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def prefill_flops(shape) -> float:
+    T = shape.T
+    pairs = T * (T + 1) / 2 if shape.causal else T * T
+    return 4.0 * shape.h * shape.d_h * pairs
+
+
+def decode_bytes(lens, shape) -> int:
+    """Algorithmic decode bytes: K and V of every attended key, q, o, and the
+    block-table entries of the attended pages (partials are overhead)."""
+    kv = 2 * sum(lens) * shape.h_kv * shape.d_h * 2
+    qo = 2 * len(lens) * shape.h * shape.d_h * 2
+    bt = sum((s + 15) // 16 for s in lens) * 4
+    return kv + qo + bt
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+
+    def _gpu_id(self):
+        """nvidia-smi index of this rank's GPU (None: the only one visible)."""
+        try:
+            n = len(subprocess.run(["nvidia-smi", "-L"], capture_output=True, text=True,
+                                   timeout=30).stdout.strip().splitlines())
+        except (OSError, subprocess.SubprocessError):
+            return None
+        if n <= 1:
+            return None
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        if vis:
+            ids = [x.strip() for x in vis.split(",") if x.strip()]
+            if self.index < len(ids):
+                return ids[self.index]
+        return str(self.index)
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            gid = self._gpu_id()
+            cmd = ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits", "-lms", "50"]
+            if gid is not None:
+                cmd.insert(1, f"--id={gid}")
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(cmd, stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], None, set()
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx = float(parts[2])
+                except ValueError:
+                    continue
+                for name, col in (("hw_slowdown", 5), ("hw_thermal_slowdown", 6),
+                                  ("sw_thermal_slowdown", 7), ("sw_power_cap", 8)):
+                    if parts[col].lower().startswith("active"):
+                        reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle legs (float64, host cores)
+# ---------------------------------------------------------------------------
+
+def oracle_prefill_sample(q, k, v, rows_per_call: int, seed: int):
+    """Oracle on a bounded sample: `rows_per_call` causal rows of one head near
+    the end of the sequence (the costliest rows). Returns (seconds, FLOPs)."""
+    import oracle
+
+    rng = np.random.default_rng(seed)
+    hq = int(rng.integers(0, PREFILL.h))
+    r0 = PREFILL.T - rows_per_call - int(rng.integers(0, 64))
+    rows = list(range(r0, r0 + rows_per_call))
+    t0 = time.perf_counter()
+    oracle.attention_rows_ref(q, k, v, PREFILL.scale, True, [hq] * len(rows), rows)
+    dt = time.perf_counter() - t0
+    flops = sum(4.0 * PREFILL.d_h * (r + 1) for r in rows)
+    return dt, flops
+
+
+def oracle_decode_sample(q, kc, vc, table, seq, rows):
+    import oracle
+
+    t0 = time.perf_counter()
+    oracle.decode_paged_ref(q, kc, vc, table, seq, DECODE.scale, rows=rows)
+    dt = time.perf_counter() - t0
+    lens = seq.tolist()
+    return dt, decode_bytes([lens[r] for r in rows], DECODE)
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, world, rank):
+    """--impl reference: the float64 CPU oracle on bounded samples, rank 0 only."""
+    if rank != 0:
+        return
+    torch.set_num_threads(cpu_cores())
+    q, k, v = W.prefill_inputs(PREFILL, 0)
+    rows_per_step = 64
+    for i in range(args.warmup):
+        oracle_prefill_sample(q, k, v, rows_per_step, seed=1000 + i)
+    tot_t, tot_f = 0.0, 0.0
+    for i in range(args.steps):
+        dt, fl = oracle_prefill_sample(q, k, v, rows_per_step, seed=i)
+        tot_t += dt
+        tot_f += fl
+    value = tot_f / tot_t / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_t / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": "float64 CPU oracle (materialised safe softmax) on a bounded sample of "
+                               "the causal GQA T=8192 prefill: per step 64 query rows of one head "
+                               "near the end of the sequence", "prefill": PREFILL.name},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": f"{rows_per_step} causal rows x {args.steps} steps of one head at T=8192"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_gpu(args, world, rank, local):
+    import online_softmax_attn_gb300 as attn
+    from online_softmax_attn_gb300 import build as attn_build
+
+    attn_build.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    hbm_peak, tc_peak, peak_kind = peaks()
+    stream = torch.cuda.current_stream()
+
+    # ---- inputs, resident in HBM before the timed region ----
+    q, k, v = W.prefill_inputs(PREFILL, seed=rank, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((PREFILL.h, PREFILL.T), dtype=torch.float32, device=dev)
+    lens = W.decode_seq_lens(DECODE, seed=rank)
+    if args.decode_rows:
+        lens = lens[:args.decode_rows]  # smaller batch, for profiler captures only
+    dq, kc, vc, table, seq = W.decode_inputs(DECODE, seed=rank, device=dev, seq_lens=lens)
+    table, seq = table.to(dev), seq.to(dev)
+    B = len(lens)
+    S = attn.attn_recommended_splits(B, DECODE.h_kv, max(lens), sum(lens))
+    ws = torch.empty(attn.attn_decode_workspace_bytes(B, DECODE.h, DECODE.d_h, S), dtype=torch.uint8, device=dev)
+    do = torch.empty_like(dq)
+    dlse = torch.empty((B, DECODE.h), dtype=torch.float32, device=dev)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    do_pre = args.only in (None, "prefill")
+    do_dec = args.only in (None, "decode")
+
+    def step(ev):
+        flush.fill_(1)
+        ev[0].record(stream)
+        if do_pre:
+            attn.attn_prefill(q, k, v, True, PREFILL.scale, o=o, lse=lse)
+        ev[1].record(stream)
+        if do_dec:
+            attn.attn_decode_paged(dq, kc, vc, table, seq, S, DECODE.scale, workspace=ws, o=do, lse=dlse)
+        ev[2].record(stream)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    for _ in range(args.warmup):
+        step([torch.cuda.Event(enable_timing=True) for _ in range(3)])
+    torch.cuda.synchronize()
+    if attn.attn_get_device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+
+    total_ms = t_start.elapsed_time(t_end)
+    pre_ms = [evs[i][0].elapsed_time(evs[i][1]) for i in range(args.steps)]
+    dec_ms = [evs[i][1].elapsed_time(evs[i][2]) for i in range(args.steps)]
+    pre_avg = max_over_ranks(sum(pre_ms) / len(pre_ms), world)
+    dec_avg = max_over_ranks(sum(dec_ms) / len(dec_ms), world)
+    step_ms = max_over_ranks(total_ms / args.steps, world)
+    err = attn.attn_get_device_error()
+    if err:
+        raise RuntimeError(f"device error bits {err:#x} during the timed region")
+
+    pf = prefill_flops(PREFILL)
+    db = decode_bytes(lens, DECODE)
+    value = world * pf / (pre_avg * 1e-3) / 1e12
+    dec_value = world * db / (dec_avg * 1e-3) / 1e9
+    pre_achieved = pf / (pre_avg * 1e-3) / 1e12
+    dec_achieved = db / (dec_avg * 1e-3) / 1e9
+
+    # ---- end to end through the public API, host buffers ----
+    e2e = None
+    dec_e2e = None
+    if not args.no_e2e:
+        hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
+        ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        dq_, dk_, dv_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        hdq = dq.cpu().pin_memory()
+        htab, hseq = table.cpu().pin_memory(), seq.cpu().pin_memory()
+        hdo = torch.empty(do.shape, dtype=do.dtype).pin_memory()
+        hdl = torch.empty(dlse.shape, dtype=dlse.dtype).pin_memory()
+        ddq, dtab, dseq = torch.empty_like(dq), torch.empty_like(table), torch.empty_like(seq)
+
+        def e2e_prefill():
+            dq_.copy_(hq, non_blocking=True)
+            dk_.copy_(hk, non_blocking=True)
+            dv_.copy_(hv, non_blocking=True)
+            attn.attn_prefill(dq_, dk_, dv_, True, PREFILL.scale, o=o, lse=lse)
+            ho.copy_(o, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+
+        def e2e_decode():
+            ddq.copy_(hdq, non_blocking=True)
+            dtab.copy_(htab, non_blocking=True)
+            dseq.copy_(hseq, non_blocking=True)
+            attn.attn_decode_paged(ddq, kc, vc, dtab, dseq, S, DECODE.scale, workspace=ws, o=do, lse=dlse)
+            hdo.copy_(do, non_blocking=True)
+            hdl.copy_(dlse, non_blocking=True)
+
+        n_e2e = max(3, min(args.steps, 20))
+        for fn, name in ((e2e_prefill, "p"), (e2e_decode, "d")):
+            for _ in range(2):
+                flush.fill_(1)
+                fn()
+            torch.cuda.synchronize()
+            ms = []
+            for _ in range(n_e2e):
+                flush.fill_(1)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                b.record(stream)
+                b.synchronize()
+                ms.append(a.elapsed_time(b))
+            avg = max_over_ranks(sum(ms) / len(ms), world)
+            if name == "p":
+                e2e = {"value": world * pf / (avg * 1e-3) / 1e12, "unit": "TFLOP/s",
+                       "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in (hq, hk, hv)),
+                       "d2h_bytes_per_step": ho.numel() * ho.element_size() + hl.numel() * hl.element_size(),
+                       "ms": avg}
+            else:
+                dec_e2e = {"value": world * db / (avg * 1e-3) / 1e9, "unit": "GB/s",
+                           "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in (hdq, htab, hseq)),
+                           "d2h_bytes_per_step": hdo.numel() * hdo.element_size() + hdl.numel() * hdl.element_size(),
+                           "ms": avg}
+
+    # ---- CPU oracle baseline (rank 0, N = 1 only) ----
+    cpu = None
+    dec_cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        torch.set_num_threads(cpu_cores())
+        qc, kc_, vc_ = q.cpu(), k.cpu(), v.cpu()
+        t_tot, f_tot, n = 0.0, 0.0, 0
+        while t_tot < args.cpu_seconds / 2 and n < 200:
+            dt, fl = oracle_prefill_sample(qc, kc_, vc_, 64, seed=n)
+            t_tot += dt
+            f_tot += fl
+            n += 1
+        cpu = {"value": f_tot / t_tot / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+               "sample": f"{n} x 64 causal query rows of one head at T=8192 (float64 materialised softmax)"}
+        order = np.argsort(lens)
+        rows = [int(order[len(order) // 2])]
+        kcc, vcc, dqc, tabc, seqc = kc.cpu(), vc.cpu(), dq.cpu(), table.cpu(), seq.cpu()
+        tt, bb, m = 0.0, 0, 0
+        while tt < args.cpu_seconds / 2 and m < 64:
+            dt, by = oracle_decode_sample(dqc, kcc, vcc, tabc, seqc, rows)
+            tt += dt
+            bb += by
+            m += 1
+        dec_cpu = {"value": bb / tt / 1e9, "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
+                   "sample": f"{m} x one median-length row of the paged batch (float64)"}
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": step_ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": "causal GQA prefill T=8192 (h=32, h_kv=8, d_h=128, Q,K x3) + paged split-KV "
+                        "decode (64 rows U[1,16384] + 2 empty, 16-token pages)",
+            "prefill": {"h": PREFILL.h, "h_kv": PREFILL.h_kv, "d_h": PREFILL.d_h, "T": PREFILL.T,
+                        "causal": True, "flops": pf},
+            "decode": {"B": B, "h": DECODE.h, "h_kv": DECODE.h_kv, "d_h": DECODE.d_h, "page": 16,
+                       "num_splits": S, "kv_tokens": sum(lens), "bytes": db},
+            "l2": "flushed (512 MiB write) before each prefill; decode cache 2.15 GB > L2",
+            "parallelism": f"replicas x{world}",
+        },
+        "roofline": {"bound": "tensor", "achieved": pre_achieved, "peak": tc_peak, "unit": "TFLOP/s",
+                     "frac": pre_achieved / tc_peak, "traffic": traffic_for("prefill"),
+                     "kernel": "prefill_bf16_kernel", "peak_source": f"{peak_kind} bf16 burst"},
+        "decode": {
+            "value": dec_value, "unit": "GB/s", "ms": dec_avg,
+            "roofline": {"bound": "hbm", "achieved": dec_achieved, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": dec_achieved / hbm_peak, "traffic": traffic_for("decode"),
+                         "kernel": "decode_split_kernel + merge_states_kernel",
+                         "peak_source": f"{peak_kind} copy bandwidth"},
+            "e2e": dec_e2e,
+            "cpu_baseline": dec_cpu,
+        },
+        "prefill_ms": pre_avg,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "gpu_launches": (int(do_pre) + 2 * int(do_dec)) * args.steps,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=16.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["prefill", "decode"], default=None,
+                    help="run one half of the step (profiler captures; not a bench line)")
+    ap.add_argument("--decode-rows", type=int, default=0,
+                    help="truncate the decode batch (profiler captures; not a bench line)")
+    args = ap.parse_args()
+    if args.only or args.decode_rows:
+        args.no_e2e = True
+        args.no_cpu_baseline = True
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_gpu(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
