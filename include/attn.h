@@ -174,6 +174,39 @@ attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* 
                                 void* o, float* lse, void* stream);
 
 /*
+ * attn_decode_paged_static -- attn_decode_paged without a workspace argument
+ * and without any allocation. The pages have no counterpart of this entry
+ * point; it exists for callers that cannot obtain device memory at the call
+ * site: for example a plugin loaded into a host program that owns all device
+ * memory and offers it no allocation hook, or a serving hot loop that must not
+ * call cudaMalloc (which can synchronise the device and takes allocator locks).
+ *
+ * The split partials live in a fixed array inside the library's device image
+ * (ATTN_DECODE_STATIC_SCRATCH_BYTES on every GPU that loads the library, held
+ * until the process exits). Arguments, layouts, results and errors are those
+ * of attn_decode_paged, plus:
+ *   - the partials, attn_decode_workspace_bytes(B, h, d_h, num_splits) bytes,
+ *     must fit in ATTN_DECODE_STATIC_SCRATCH_BYTES; a larger request returns
+ *     ATTN_ERR_INVALID_ARG before anything is launched (use fewer splits, a
+ *     smaller batch, or attn_decode_paged);
+ *   - the first call on each device looks up the array's device address with
+ *     cudaGetSymbolAddress (with that device current) and caches it; make that
+ *     first call on a device before any stream capture;
+ *   - every call on a device shares the one array, which keeps the last
+ *     call's partials. Nothing in it needs to start at zero. Calls whose
+ *     kernels can overlap on the GPU (different streams with no ordering
+ *     between them, or several host threads) race on it and give wrong
+ *     results: order them, e.g. issue them on one stream;
+ *   - it calls no cudaMalloc, cudaFree or other allocating routine.
+ */
+#define ATTN_DECODE_STATIC_SCRATCH_BYTES (16u * 1024u * 1024u)
+attn_status_t attn_decode_paged_static(const void* q, const void* k_cache, const void* v_cache,
+                                       const int32_t* block_table, const int32_t* seq_lens,
+                                       int B, int h, int h_kv, int d_h, int page_size,
+                                       int num_blocks, int max_blocks_per_seq, int num_splits,
+                                       float scale, void* o, float* lse, void* stream);
+
+/*
  * attn_merge_states -- N-way merge of split partial states, one output row
  * per input row. Follows [DEC] stage 2 ("reduce_segments") and [MRG]: over
  * the row's active splits i < n_active[row], M = max m_i, w_i = exp(m_i - M),

@@ -212,3 +212,40 @@ def attn_get_device_error(stream=None) -> int:
     st = library().attn_get_device_error(_stream(stream), ctypes.byref(bits))
     _check("attn_get_device_error", st)
     return bits.value
+
+
+ATTN_DECODE_STATIC_SCRATCH_BYTES = 16 * 1024 * 1024
+_static_ready = False
+
+
+def attn_decode_paged_static(q, k_cache, v_cache, block_table, seq_lens, num_splits: int,
+                             scale: float | None = None, o=None, lse=None, return_lse: bool = True,
+                             stream=None):
+    """attn_decode_paged without a workspace, for callers that cannot allocate
+    device memory at the call site: the split partials live in a fixed
+    ATTN_DECODE_STATIC_SCRATCH_BYTES array inside the library on each GPU.
+    Calls on one device share that array, so they must not overlap on the GPU
+    (issue them on one stream). The first call on a device resolves the
+    array's address; make it before any stream capture. Outputs are allocated
+    here only when o / lse are not given."""
+    global _static_ready
+    lib = library()
+    if not _static_ready:
+        P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        lib.attn_decode_paged_static.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, F, P, P, P]
+        lib.attn_decode_paged_static.restype = I
+        _static_ready = True
+    for t in (q, k_cache, v_cache, block_table, seq_lens):
+        _need(t.is_cuda and t.is_contiguous(), "decode tensors must be contiguous CUDA tensors")
+    B, h, d = q.shape
+    nb, page, h_kv, _ = k_cache.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, h), dtype=torch.float32, device=q.device)
+    st = lib.attn_decode_paged_static(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens), B, h, h_kv, d,
+        page, nb, block_table.shape[1], int(num_splits), scale, _ptr(o), _ptr(lse), _stream(stream))
+    _check("attn_decode_paged_static", st)
+    return o, lse
