@@ -45,7 +45,7 @@ constexpr int kBM = 128;  // query rows per tile (tensor-memory lanes)
 constexpr int kBN = 128;  // keys per tile
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when max rises > 2^8
 
-template <int D, int NQ, int NS>
+template <int D, int NQ, int NSK, int NSV>
 struct PfCfg {
   static constexpr int SUBS = D / 64;                // 64-element swizzle atoms along d_h
   static constexpr int SUB_BYTES = 128 * 128;        // one atom column of a 128-row tile
@@ -53,30 +53,88 @@ struct PfCfg {
   static constexpr int KTILE = kBN * D * 2;
   static constexpr int Q_OFF = 0;
   static constexpr int K_OFF = Q_OFF + NQ * QTILE;
-  static constexpr int V_OFF = K_OFF + NS * KTILE;
-  static constexpr int BAR_OFF = V_OFF + NS * KTILE;
-  // q_full, k_full[NS], v_full[NS], kv_empty[NS], s_full[NQ], p_full[NQ],
-  // o_final[NQ], mma_done
-  static constexpr int NBAR = 1 + 3 * NS + 3 * NQ + 1;
+  static constexpr int V_OFF = K_OFF + NSK * KTILE;
+  static constexpr int BAR_OFF = V_OFF + NSV * KTILE;
+  // q_full, k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV], s_full[NQ],
+  // p_full[NQ], o_final[NQ], mma_done
+  static constexpr int NBAR = 1 + 2 * NSK + 2 * NSV + 3 * NQ + 1;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int SMEM = MISC_OFF + 16 + 1024;  // + alignment slack
   static constexpr int TMEM_COLS = NQ == 1 ? 256 : 512;
-  static constexpr int THREADS = NQ * 128 + 64;
+  // NQ softmax warpgroups + one control warpgroup (TMA warp, MMA warp, two
+  // idle warps), so that register shares can be moved per warpgroup.
+  static constexpr int THREADS = NQ * 128 + 128;
   static constexpr int PRODUCER_WARP = NQ * 4;
   static constexpr int MMA_WARP = NQ * 4 + 1;
+  // Register split (NQ = 2): launched at 168/thread (384 x 168 = 64512);
+  // control warpgroup drops to 88, softmax warpgroups rise to 208:
+  // 2 x 128 x 208 + 128 x 88 = 64512 <= 64512.
+  static constexpr int REG_LAUNCH = 168;
+  static constexpr int REG_CONTROL = 88;
+  static constexpr int REG_SOFTMAX = 208;
+  static_assert(NQ != 2 || 2 * 128 * REG_SOFTMAX + 128 * REG_CONTROL <= THREADS * REG_LAUNCH,
+                "register split exceeds the launch allocation");
 };
+
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Packed fp32 pairs (two lanes of one 64-bit register pair).
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unf2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
 
 struct Bars {
   uint32_t base;
-  int ns, nq;
+  int nsk, nsv, nq;
   __device__ uint32_t q_full() const { return base; }
   __device__ uint32_t k_full(int s) const { return base + 8 * (1 + s); }
-  __device__ uint32_t v_full(int s) const { return base + 8 * (1 + ns + s); }
-  __device__ uint32_t kv_empty(int s) const { return base + 8 * (1 + 2 * ns + s); }
-  __device__ uint32_t s_full(int t) const { return base + 8 * (1 + 3 * ns + t); }
-  __device__ uint32_t p_full(int t) const { return base + 8 * (1 + 3 * ns + nq + t); }
-  __device__ uint32_t o_final(int t) const { return base + 8 * (1 + 3 * ns + 2 * nq + t); }
-  __device__ uint32_t mma_done() const { return base + 8 * (1 + 3 * ns + 3 * nq); }
+  __device__ uint32_t k_empty(int s) const { return base + 8 * (1 + nsk + s); }
+  __device__ uint32_t v_full(int s) const { return base + 8 * (1 + 2 * nsk + s); }
+  __device__ uint32_t v_empty(int s) const { return base + 8 * (1 + 2 * nsk + nsv + s); }
+  __device__ uint32_t s_full(int t) const { return base + 8 * (1 + 2 * nsk + 2 * nsv + t); }
+  __device__ uint32_t p_full(int t) const { return base + 8 * (1 + 2 * nsk + 2 * nsv + nq + t); }
+  __device__ uint32_t o_final(int t) const {
+    return base + 8 * (1 + 2 * nsk + 2 * nsv + 2 * nq + t);
+  }
+  __device__ uint32_t mma_done() const { return base + 8 * (1 + 2 * nsk + 2 * nsv + 3 * nq); }
 };
 
 // Bounded wait that also gives up at once when another role has aborted.
@@ -97,19 +155,19 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
   }
 }
 
-template <int D, int NQ, int NS>
-__global__ void __launch_bounds__(PfCfg<D, NQ, NS>::THREADS, 1)
+template <int D, int NQ, int NSK, int NSV>
+__global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
     prefill_bf16_kernel(const __grid_constant__ CUtensorMap tmap_q,
                         const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v,
                         __nv_bfloat16* __restrict__ o, float* __restrict__ lse, int T, int h,
                         int h_kv, int causal, float scale_log2, int n_qblk) {
-  using C = PfCfg<D, NQ, NS>;
+  using C = PfCfg<D, NQ, NSK, NSV>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
-  Bars bars{sbase + C::BAR_OFF, NS, NQ};
+  Bars bars{sbase + C::BAR_OFF, NSK, NSV, NQ};
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
 
@@ -137,6 +195,10 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NS>::THREADS, 1)
   tc::fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // Register shares move per warpgroup: every warp of a warpgroup executes
+  // the same setmaxnreg, at the top of its role's code.
+  if (warp >= C::PRODUCER_WARP) {
+  if constexpr (NQ == 2) regs_dec<C::REG_CONTROL>();
   if (warp == C::PRODUCER_WARP) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -148,88 +210,112 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NS>::THREADS, 1)
         for (int s = 0; s < C::SUBS; ++s)
           tma_load_3d(sbase + C::Q_OFF + t * C::QTILE + s * C::SUB_BYTES, &tmap_q, bars.q_full(),
                       s * 64, qb * kBM, hq0 + t);
-      int issued = 0;
+      // K and V have rings of their own: a K stage frees as soon as the last
+      // head's S MMA on it completes, a V stage after the last P V MMA.
+      int k_issued = 0, v_issued = 0;
       for (int j = 0; j < nkv; ++j) {
-        const int st = j % NS;
-        if (j >= NS && !wait_or_abort(bars.kv_empty(st), ((j / NS) - 1) & 1, abort_flag)) break;
-        mbar_arrive_expect_tx(bars.k_full(st), C::KTILE);
+        const int sk = j % NSK, sv = j % NSV;
+        if (j >= NSK && !wait_or_abort(bars.k_empty(sk), ((j / NSK) - 1) & 1, abort_flag)) break;
+        mbar_arrive_expect_tx(bars.k_full(sk), C::KTILE);
         for (int s = 0; s < C::SUBS; ++s)
-          tma_load_3d(sbase + C::K_OFF + st * C::KTILE + s * C::SUB_BYTES, &tmap_k,
-                      bars.k_full(st), s * 64, j * kBN, kvh);
-        mbar_arrive_expect_tx(bars.v_full(st), C::KTILE);
+          tma_load_3d(sbase + C::K_OFF + sk * C::KTILE + s * C::SUB_BYTES, &tmap_k,
+                      bars.k_full(sk), s * 64, j * kBN, kvh);
+        k_issued = j + 1;
+        if (j >= NSV && !wait_or_abort(bars.v_empty(sv), ((j / NSV) - 1) & 1, abort_flag)) break;
+        mbar_arrive_expect_tx(bars.v_full(sv), C::KTILE);
         for (int s = 0; s < C::SUBS; ++s)
-          tma_load_3d(sbase + C::V_OFF + st * C::KTILE + s * C::SUB_BYTES, &tmap_v,
-                      bars.v_full(st), s * 64, j * kBN, kvh);
-        issued = j + 1;
+          tma_load_3d(sbase + C::V_OFF + sv * C::KTILE + s * C::SUB_BYTES, &tmap_v,
+                      bars.v_full(sv), s * 64, j * kBN, kvh);
+        v_issued = j + 1;
       }
       if (*abort_flag) {
         // Drain: the newest load of each stage is the only one that can still
         // be in flight. Bounded waits, error already recorded.
         (void)mbar_wait(bars.q_full(), 0, &g_prefill_err);
-        for (int j = max(0, issued - NS); j < issued; ++j) {
-          (void)mbar_wait(bars.k_full(j % NS), (j / NS) & 1, &g_prefill_err);
-          (void)mbar_wait(bars.v_full(j % NS), (j / NS) & 1, &g_prefill_err);
-        }
+        for (int j = max(0, k_issued - NSK); j < k_issued; ++j)
+          (void)mbar_wait(bars.k_full(j % NSK), (j / NSK) & 1, &g_prefill_err);
+        for (int j = max(0, v_issued - NSV); j < v_issued; ++j)
+          (void)mbar_wait(bars.v_full(j % NSV), (j / NSV) & 1, &g_prefill_err);
       }
     }
   } else if (warp == C::MMA_WARP) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs this loop (operands warp-uniform); elect.sync picks
+    // the lane that issues each MMA / commit. Wait outcomes are made
+    // warp-uniform before any warp-collective instruction.
+    {
       constexpr uint32_t idS = tc::idesc_bf16_f32(kBM, kBN, false, false);
       constexpr uint32_t idO = tc::idesc_bf16_f32(kBM, D, false, true);
-      const uint32_t q_s = sbase + C::Q_OFF, k_s = sbase + C::K_OFF, v_s = sbase + C::V_OFF;
+      // Base descriptors once; per MMA only the start-address field (address
+      // >> 4, 14 bits) advances. Shared addresses stay below 256 KB, so the
+      // field never carries into its neighbour.
+      const uint64_t dq0 = tc::sw128_desc(sbase + C::Q_OFF, 16, 1024);
+      const uint64_t dk0 = tc::sw128_desc(sbase + C::K_OFF, 16, 1024);
+      const uint64_t dv0 = tc::sw128_desc(sbase + C::V_OFF, C::SUB_BYTES, 1024);
       auto issue_s = [&](int t, int st) {
+        const uint64_t da = dq0 + uint64_t((t * C::QTILE) >> 4);
+        const uint64_t db = dk0 + uint64_t((st * C::KTILE) >> 4);
+        const uint32_t dS = tmem + t * 256;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::SUB_BYTES + (kk & 3) * 32;
-          const uint64_t a = tc::sw128_desc(q_s + t * C::QTILE + off, 16, 1024);
-          const uint64_t b = tc::sw128_desc(k_s + st * C::KTILE + off, 16, 1024);
-          tc::mma_ss(tmem + t * 256, a, b, idS, kk > 0 ? 1u : 0u);
+          const uint32_t off16 = ((kk >> 2) * C::SUB_BYTES + (kk & 3) * 32) >> 4;
+          tc::mma_ss_elect(dS, da + off16, db + off16, idS, kk > 0 ? 1u : 0u);
         }
       };
       // O_t += P_hi V + P_lo V (P_hi in S columns 0-63, P_lo in 64-127).
       auto issue_pv = [&](int t, int st, bool acc) {
+        const uint64_t dvb = dv0 + uint64_t((st * C::KTILE) >> 4);
+        const uint32_t dO = tmem + t * 256 + 128;
+        const uint32_t aP = tmem + t * 256;
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint64_t b = tc::sw128_desc(v_s + st * C::KTILE + kk * 16 * 128, C::SUB_BYTES, 1024);
-          tc::mma_ts(tmem + t * 256 + 128, tmem + t * 256 + kk * 8, b, idO,
-                     (acc || kk > 0) ? 1u : 0u);
-          tc::mma_ts(tmem + t * 256 + 128, tmem + t * 256 + 64 + kk * 8, b, idO, 1u);
+          const uint64_t b = dvb + uint64_t((kk * 16 * 128) >> 4);
+          tc::mma_ts_elect(dO, aP + kk * 8, b, idO, (acc || kk > 0) ? 1u : 0u);
+          tc::mma_ts_elect(dO, aP + 64 + kk * 8, b, idO, 1u);
         }
       };
-      bool ok = wait_or_abort(bars.q_full(), 0, abort_flag) &&
-                wait_or_abort(bars.k_full(0), 0, abort_flag);
+      auto wait = [&](uint32_t bar, uint32_t parity) {
+        return __all_sync(0xffffffffu, wait_or_abort(bar, parity, abort_flag));
+      };
+      bool ok = wait(bars.q_full(), 0) && wait(bars.k_full(0), 0);
       if (ok) {
         tc::fence_after();
         for (int t = 0; t < NQ; ++t) {
           issue_s(t, 0);
-          tc::commit(bars.s_full(t));
+          tc::commit_elect(bars.s_full(t));
         }
+        tc::commit_elect(bars.k_empty(0));
       }
+      // Order per key tile j: P_0 V_j, S_0(j+1), P_1 V_j, S_1(j+1): each head's
+      // next QK^T follows its own P V (P aliases S in tensor memory), and the
+      // other head's softmax runs while these MMAs execute.
       for (int j = 0; ok && j < nkv; ++j) {
-        const int st = j % NS;
+        const int sv = j % NSV;
+        const int sk1 = (j + 1) % NSK;
         for (int t = 0; t < NQ && ok; ++t) {
-          if (!wait_or_abort(bars.p_full(t), j & 1, abort_flag)) { ok = false; break; }
-          if (t == 0 && !wait_or_abort(bars.v_full(st), (j / NS) & 1, abort_flag)) { ok = false; break; }
+          if (!wait(bars.p_full(t), j & 1)) { ok = false; break; }
+          if (t == 0 && !wait(bars.v_full(sv), (j / NSV) & 1)) { ok = false; break; }
           tc::fence_after();
-          issue_pv(t, st, j > 0);
-          if (j == nkv - 1) tc::commit(bars.o_final(t));
+          issue_pv(t, sv, j > 0);
+          if (j == nkv - 1) tc::commit_elect(bars.o_final(t));
+          if (t == NQ - 1) tc::commit_elect(bars.v_empty(sv));
           if (j + 1 < nkv) {
-            const int st1 = (j + 1) % NS;
-            if (t == 0 && !wait_or_abort(bars.k_full(st1), ((j + 1) / NS) & 1, abort_flag)) { ok = false; break; }
+            if (t == 0 && !wait(bars.k_full(sk1), ((j + 1) / NSK) & 1)) { ok = false; break; }
             tc::fence_after();
-            issue_s(t, st1);
-            tc::commit(bars.s_full(t));
+            issue_s(t, sk1);
+            tc::commit_elect(bars.s_full(t));
+            if (t == NQ - 1) tc::commit_elect(bars.k_empty(sk1));
           }
         }
-        if (ok) tc::commit(bars.kv_empty(st));
       }
-      // Everything issued by this thread has completed once mma_done flips.
-      tc::commit(bars.mma_done());
-      (void)mbar_wait(bars.mma_done(), 0, &g_prefill_err);
+      // Everything issued has completed once mma_done flips.
+      tc::commit_elect(bars.mma_done());
+      (void)__all_sync(0xffffffffu, mbar_wait(bars.mma_done(), 0, &g_prefill_err));
     }
+  }
   } else {
     // ------------------------------------------------------------ softmax
+    if constexpr (NQ == 2) regs_inc<C::REG_SOFTMAX>();
     const int t = warp >> 2;
     const int wq = warp & 3;
     const int r = wq * 32 + lane;
@@ -255,7 +341,6 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NS>::THREADS, 1)
       int lim = kBN;
       if (j * kBN + kBN > T) lim = T - j * kBN;
       if (causal && j == qb) lim = min(lim, r + 1);
-      float mx = -INFINITY;
       if (lim < kBN) {
 #pragma unroll
         for (int c = 0; c < 4; ++c)
@@ -263,10 +348,17 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NS>::THREADS, 1)
           for (int i = 0; i < 32; ++i)
             if (c * 32 + i >= lim) sr[c][i] = __float_as_uint(-INFINITY);
       }
+      // Row max: four independent chains of 3-input max, then combine.
+      float mxc[4];
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+      for (int c = 0; c < 4; ++c) {
+        mxc[c] = __uint_as_float(sr[c][0]);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(sr[c][i]));
+        for (int i = 1; i < 31; i += 2)
+          mxc[c] = max3f(mxc[c], __uint_as_float(sr[c][i]), __uint_as_float(sr[c][i + 1]));
+        mxc[c] = fmaxf(mxc[c], __uint_as_float(sr[c][31]));
+      }
+      const float mx = fmaxf(fmaxf(mxc[0], mxc[1]), fmaxf(mxc[2], mxc[3]));
 
       const float m_cand = mx * scale_log2;
       const bool need = m_cand > m_ref + kRescaleThreshold;
@@ -276,52 +368,57 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NS>::THREADS, 1)
         m_ref = m_cand;
       }
       const float bias = (m_ref == -INFINITY) ? 0.f : m_ref;
-      // P = P_hi + P_lo, both bf16: P_hi = bf16(p), P_lo = bf16(p - P_hi).
-      // The pair carries ~16 significant bits, so the rounding of P no longer
-      // limits the output error (a single bf16 P costs up to 2^-8 relative
-      // per weight, which rows dominated by a few keys do not average away).
-      // Key pair (2i, 2i+1) of chunk c lands in P column 16c + i; P_hi fills
-      // columns 0-63 and P_lo columns 64-127 of the S tile just read.
-      float sum = 0.f;
+      // P = P_hi + P_lo, both bf16. P_hi is p truncated to bf16 (its upper 16
+      // bits), P_lo = bf16(p - P_hi) (the difference is exact in fp32), so
+      // the pair carries ~16 significant bits and the rounding of P no longer
+      // limits the output error (a single bf16 P costs up to 2^-8 relative per
+      // weight, which rows dominated by a few keys do not average away).
+      // Key pair (2i, 2i+1) of chunk c goes to P column 16c + i; P_hi fills
+      // columns 0-63 and P_lo columns 64-127 of the S tile just read. Within
+      // chunk c, sr[c][2i] is reused for the P_hi pair, sr[c][2i+1] for P_lo.
+      const uint64_t c2 = f2(scale_log2, scale_log2);
+      const uint64_t nb2 = f2(-bias, -bias);
+      uint64_t sumA = f2(0.f, 0.f), sumB = f2(0.f, 0.f);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        uint32_t ph[16], pl[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c][2 * i]), scale_log2, -bias));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c][2 * i + 1]), scale_log2, -bias));
-          sum += p0 + p1;
-          ph[i] = pack_bf16x2(p0, p1);
-          pl[i] = pack_bf16x2(p0 - bf16lo(ph[i]), p1 - bf16hi(ph[i]));
-        }
-        // sr[c] is consumed: reuse it to stage [P_hi | P_lo] of this chunk.
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          sr[c][i] = ph[i];
-          sr[c][16 + i] = pl[i];
+          float y0, y1;
+          unf2(fma2(f2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])), c2, nb2),
+               y0, y1);
+          const float p0 = ex2_approx(y0);
+          const float p1 = ex2_approx(y1);
+          const uint64_t pp = f2(p0, p1);
+          if (i & 1) sumB = add2(sumB, pp); else sumA = add2(sumA, pp);
+          const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
+          uint32_t hi;
+          asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(hi) : "r"(u0), "r"(u1));
+          float d0, d1;
+          unf2(sub2(pp, f2(__uint_as_float(u0 & 0xffff0000u), __uint_as_float(u1 & 0xffff0000u))),
+               d0, d1);
+          sr[c][2 * i] = hi;
+          sr[c][2 * i + 1] = pack_bf16x2(d0, d1);
         }
       }
-      l = fmaf(l, alpha, sum);
+      float sa0, sa1, sb0, sb1;
+      unf2(add2(sumA, sumB), sa0, sa1);
+      (void)sb0;
+      (void)sb1;
+      l = fmaf(l, alpha, sa0 + sa1);
       {
         uint32_t hi[32], lo[32];
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
+        for (int half = 0; half < 2; ++half) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            hi[16 * c + i] = sr[c][i];
-            lo[16 * c + i] = sr[c][16 + i];
-          }
-        tc::st32(tS, hi);        // P_hi keys 0..63
-        tc::st32(tS + 64, lo);   // P_lo keys 0..63
+          for (int c = 0; c < 2; ++c)
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            hi[16 * c + i] = sr[2 + c][i];
-            lo[16 * c + i] = sr[2 + c][16 + i];
-          }
-        tc::st32(tS + 32, hi);   // P_hi keys 64..127
-        tc::st32(tS + 96, lo);   // P_lo keys 64..127
+            for (int i = 0; i < 16; ++i) {
+              hi[16 * c + i] = sr[2 * half + c][2 * i];
+              lo[16 * c + i] = sr[2 * half + c][2 * i + 1];
+            }
+          tc::st32(tS + 32 * half, hi);       // P_hi keys 64*half .. +63
+          tc::st32(tS + 64 + 32 * half, lo);  // P_lo keys 64*half .. +63
+        }
       }
       if (j > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll
@@ -329,8 +426,14 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NS>::THREADS, 1)
           uint32_t ov[32];
           tc::ld32(tO + c * 32, ov);
           tc::wait_ld();
+          const uint64_t a2 = f2(alpha, alpha);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+          for (int i = 0; i < 16; ++i) {
+            float x0, x1;
+            unf2(mul2(f2(__uint_as_float(ov[2 * i]), __uint_as_float(ov[2 * i + 1])), a2), x0, x1);
+            ov[2 * i] = __float_as_uint(x0);
+            ov[2 * i + 1] = __float_as_uint(x1);
+          }
           tc::st32(tO + c * 32, ov);
         }
       }
@@ -372,10 +475,11 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NS>::THREADS, 1)
   if (warp == C::MMA_WARP) tc::dealloc(tmem, C::TMEM_COLS);
 }
 
-template <int D, int NQ, int NS>
+template <int D, int NQ, int NSK, int NSV>
 cudaError_t launch(const void* q, const void* k, const void* v, void* o, float* lse, int T, int h,
                    int h_kv, int causal, float scale, cudaStream_t stream) {
-  using C = PfCfg<D, NQ, NS>;
+  using C = PfCfg<D, NQ, NSK, NSV>;
+  static_assert(C::SMEM <= 232448, "shared memory budget");
   CUtensorMap tq, tk, tv;
   const uint32_t box[3] = {64u, 128u, 1u};
   {
@@ -395,7 +499,7 @@ cudaError_t launch(const void* q, const void* k, const void* v, void* o, float* 
                           strides, box, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  auto kern = prefill_bf16_kernel<D, NQ, NS>;
+  auto kern = prefill_bf16_kernel<D, NQ, NSK, NSV>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   const int n_qblk = (T + kBM - 1) / kBM;
@@ -412,12 +516,13 @@ cudaError_t launch_prefill_bf16(const void* q, const void* k, const void* v, voi
                                 cudaStream_t stream) {
   const int g = h / h_kv;
   const bool pair = (g % 2) == 0;
+  // Stage counts fill the shared memory next to the Q tiles (<= 227 KB).
   if (d_h == 128) {
-    return pair ? launch<128, 2, 2>(q, k, v, o, lse, T, h, h_kv, causal, scale, stream)
-                : launch<128, 1, 3>(q, k, v, o, lse, T, h, h_kv, causal, scale, stream);
+    return pair ? launch<128, 2, 3, 2>(q, k, v, o, lse, T, h, h_kv, causal, scale, stream)
+                : launch<128, 1, 3, 3>(q, k, v, o, lse, T, h, h_kv, causal, scale, stream);
   }
-  return pair ? launch<64, 2, 3>(q, k, v, o, lse, T, h, h_kv, causal, scale, stream)
-              : launch<64, 1, 4>(q, k, v, o, lse, T, h, h_kv, causal, scale, stream);
+  return pair ? launch<64, 2, 4, 4>(q, k, v, o, lse, T, h, h_kv, causal, scale, stream)
+              : launch<64, 1, 4, 4>(q, k, v, o, lse, T, h, h_kv, causal, scale, stream);
 }
 
 unsigned int prefill_read_and_clear_error(cudaStream_t stream, cudaError_t* st) {
