@@ -56,16 +56,20 @@ struct PfCfg {
   static constexpr int V_OFF = K_OFF + NSK * KTILE;
   static constexpr int BAR_OFF = V_OFF + NSV * KTILE;
   // q_full, k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV], s_full[NQ],
-  // p_full[NQ], o_final[NQ], mma_done
-  static constexpr int NBAR = 1 + 2 * NSK + 2 * NSV + 3 * NQ + 1;
+  // p_full[NQ], o_final[NQ], mma_done, v_check[NSV], v_conv[NSV]
+  static constexpr int NBAR = 1 + 2 * NSK + 2 * NSV + 3 * NQ + 1 + 2 * NSV;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
-  static constexpr int SMEM = MISC_OFF + 16 + 1024;  // + alignment slack
+  // tensor-memory slot, abort flag, then V-format flags: per stage one
+  // "wide" bit per converter warp [NSV][2] and the stage's verdict [NSV].
+  static constexpr int FLAG_OFF = MISC_OFF + 16;
+  static constexpr int SMEM = FLAG_OFF + 3 * NSV * 4 + 1024;  // + alignment slack
   static constexpr int TMEM_COLS = NQ == 1 ? 256 : 512;
   // NQ softmax warpgroups + one control warpgroup (TMA warp, MMA warp, two
   // idle warps), so that register shares can be moved per warpgroup.
   static constexpr int THREADS = NQ * 128 + 128;
   static constexpr int PRODUCER_WARP = NQ * 4;
   static constexpr int MMA_WARP = NQ * 4 + 1;
+  static constexpr int CONV_WARP0 = NQ * 4 + 2;  // two V-conversion warps
   // Register split (NQ = 2): launched at 168/thread (384 x 168 = 64512);
   // control warpgroup drops to 88, softmax warpgroups rise to 208:
   // 2 x 128 x 208 + 128 x 88 = 64512 <= 64512.
@@ -135,6 +139,12 @@ struct Bars {
     return base + 8 * (1 + 2 * nsk + 2 * nsv + 2 * nq + t);
   }
   __device__ uint32_t mma_done() const { return base + 8 * (1 + 2 * nsk + 2 * nsv + 3 * nq); }
+  __device__ uint32_t v_check(int s) const {
+    return base + 8 * (2 + 2 * nsk + 2 * nsv + 3 * nq + s);
+  }
+  __device__ uint32_t v_conv(int s) const {
+    return base + 8 * (2 + 2 * nsk + 3 * nsv + 3 * nq + s);
+  }
 };
 
 // Bounded wait that also gives up at once when another role has aborted.
@@ -179,12 +189,16 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
   const int n_kv_all = (T + kBN - 1) / kBN;
   const int nkv = causal ? min(qb + 1, n_kv_all) : n_kv_all;
 
+  int* vflags = reinterpret_cast<int*>(smem + C::FLAG_OFF);  // [NSV][2] then [NSV]
+
   if (threadIdx.x == 0) {
-    // p_full collects one arrival per softmax thread; the others take one.
+    // p_full collects one arrival per softmax thread, v_check and v_conv one
+    // per conversion warp; the others take one.
     for (int i = 0; i < C::NBAR; ++i) {
       const uint32_t bar = bars.base + 8 * i;
       const bool is_p = bar >= bars.p_full(0) && bar < bars.p_full(0) + 8 * NQ;
-      mbar_init(bar, is_p ? 128u : 1u);
+      const bool is_v = bar >= bars.v_check(0) && bar < bars.v_check(0) + 16 * NSV;
+      mbar_init(bar, is_p ? 128u : (is_v ? 2u : 1u));
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -262,16 +276,27 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
           tc::mma_ss_elect(dS, da + off16, db + off16, idS, kk > 0 ? 1u : 0u);
         }
       };
-      // O_t += P_hi V + P_lo V (P_hi in S columns 0-63, P_lo in 64-127).
-      auto issue_pv = [&](int t, int st, bool acc) {
+      constexpr uint32_t idO16 = tc::idesc_f16_f32(kBM, D, false, true);
+      // O_t += P V. Normal tiles: P fp16 (S columns 0-63) times the fp16 copy
+      // of V made by the conversion warps. Wide tiles (some |v| >= 2^16, kept
+      // bf16): O_t += P_hi V + P_lo V with P_hi in columns 0-63, P_lo 64-127.
+      auto issue_pv = [&](int t, int st, bool acc, bool wide) {
         const uint64_t dvb = dv0 + uint64_t((st * C::KTILE) >> 4);
         const uint32_t dO = tmem + t * 256 + 128;
         const uint32_t aP = tmem + t * 256;
+        if (!wide) {
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint64_t b = dvb + uint64_t((kk * 16 * 128) >> 4);
-          tc::mma_ts_elect(dO, aP + kk * 8, b, idO, (acc || kk > 0) ? 1u : 0u);
-          tc::mma_ts_elect(dO, aP + 64 + kk * 8, b, idO, 1u);
+          for (int kk = 0; kk < kBN / 16; ++kk) {
+            const uint64_t b = dvb + uint64_t((kk * 16 * 128) >> 4);
+            tc::mma_ts_elect(dO, aP + kk * 8, b, idO16, (acc || kk > 0) ? 1u : 0u);
+          }
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk) {
+            const uint64_t b = dvb + uint64_t((kk * 16 * 128) >> 4);
+            tc::mma_ts_elect(dO, aP + kk * 8, b, idO, (acc || kk > 0) ? 1u : 0u);
+            tc::mma_ts_elect(dO, aP + 64 + kk * 8, b, idO, 1u);
+          }
         }
       };
       auto wait = [&](uint32_t bar, uint32_t parity) {
@@ -289,14 +314,19 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
       // Order per key tile j: P_0 V_j, S_0(j+1), P_1 V_j, S_1(j+1): each head's
       // next QK^T follows its own P V (P aliases S in tensor memory), and the
       // other head's softmax runs while these MMAs execute.
+      bool wide = false;
       for (int j = 0; ok && j < nkv; ++j) {
         const int sv = j % NSV;
         const int sk1 = (j + 1) % NSK;
         for (int t = 0; t < NQ && ok; ++t) {
           if (!wait(bars.p_full(t), j & 1)) { ok = false; break; }
-          if (t == 0 && !wait(bars.v_full(sv), (j / NSV) & 1)) { ok = false; break; }
+          if (t == 0) {
+            // V tile j converted (or found wide and left bf16).
+            if (!wait(bars.v_conv(sv), (j / NSV) & 1)) { ok = false; break; }
+            wide = *reinterpret_cast<volatile int*>(&vflags[2 * NSV + sv]) != 0;
+          }
           tc::fence_after();
-          issue_pv(t, sv, j > 0);
+          issue_pv(t, sv, j > 0, wide);
           if (j == nkv - 1) tc::commit_elect(bars.o_final(t));
           if (t == NQ - 1) tc::commit_elect(bars.v_empty(sv));
           if (j + 1 < nkv) {
@@ -311,6 +341,58 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
       // Everything issued has completed once mma_done flips.
       tc::commit_elect(bars.mma_done());
       (void)__all_sync(0xffffffffu, mbar_wait(bars.mma_done(), 0, &g_prefill_err));
+    }
+  } else {
+    // ------------------------------------------------------------ V conversion
+    // Two warps turn each V tile from bf16 into fp16 in place, so that P can
+    // be an fp16 operand (11 significant bits) and P V a single MMA. bf16
+    // values convert exactly while |v| < 2^16 (fp16's top binade; values below
+    // 2^-17 round with an absolute error under 2^-25). A tile holding any
+    // |v| >= 2^16 (or inf/NaN) is "wide": it stays bf16 and takes the
+    // P_hi + P_lo path. Pass 1 checks the range of each warp's half, the two
+    // warps agree through v_check, pass 2 converts.
+    const int cw = warp - C::CONV_WARP0;
+    constexpr int CHUNKS = kBN * D * 2 / 16;  // 16-byte chunks per V tile
+    constexpr int HALF = CHUNKS / 2;
+    for (int j = 0; j < nkv; ++j) {
+      const int sv = j % NSV;
+      if (!__all_sync(0xffffffffu, wait_or_abort(bars.v_full(sv), (j / NSV) & 1, abort_flag)))
+        break;
+      uint4* tile = reinterpret_cast<uint4*>(smem + C::V_OFF + sv * C::KTILE);
+      uint32_t mx = 0;
+      for (int i = cw * HALF + lane; i < (cw + 1) * HALF; i += 32) {
+        const uint4 x = tile[i];
+        uint32_t m2;
+        asm("max.u16x2 %0, %1, %2;" : "=r"(m2) : "r"(x.x & 0x7fff7fffu), "r"(x.y & 0x7fff7fffu));
+        asm("max.u16x2 %0, %0, %1;" : "+r"(m2) : "r"(x.z & 0x7fff7fffu));
+        asm("max.u16x2 %0, %0, %1;" : "+r"(m2) : "r"(x.w & 0x7fff7fffu));
+        asm("max.u16x2 %0, %0, %1;" : "+r"(mx) : "r"(m2));
+      }
+      // bf16 bits 0x4780 = 2^16: the first magnitude fp16 cannot hold.
+      const bool my_wide =
+          __any_sync(0xffffffffu, (mx & 0xffffu) >= 0x4780u || (mx >> 16) >= 0x4780u);
+      if (lane == 0) vflags[sv * 2 + cw] = my_wide ? 1 : 0;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars.v_check(sv));
+      if (!__all_sync(0xffffffffu, wait_or_abort(bars.v_check(sv), (j / NSV) & 1, abort_flag)))
+        break;
+      const volatile int* vf = vflags;
+      const bool wide = (vf[sv * 2] | vf[sv * 2 + 1]) != 0;
+      if (!wide) {
+        for (int i = cw * HALF + lane; i < (cw + 1) * HALF; i += 32) {
+          const uint4 x = tile[i];
+          uint4 y;
+          y.x = pack_f16x2(bf16lo(x.x), bf16hi(x.x));
+          y.y = pack_f16x2(bf16lo(x.y), bf16hi(x.y));
+          y.z = pack_f16x2(bf16lo(x.z), bf16hi(x.z));
+          y.w = pack_f16x2(bf16lo(x.w), bf16hi(x.w));
+          tile[i] = y;
+        }
+        fence_proxy_async_smem();  // generic stores -> visible to the tensor core
+      }
+      if (cw == 0 && lane == 0) vflags[2 * NSV + sv] = wide ? 1 : 0;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars.v_conv(sv));
     }
   }
   } else {
@@ -368,44 +450,75 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
         m_ref = m_cand;
       }
       const float bias = (m_ref == -INFINITY) ? 0.f : m_ref;
-      // P = P_hi + P_lo, both bf16. P_hi is p truncated to bf16 (its upper 16
-      // bits), P_lo = bf16(p - P_hi) (the difference is exact in fp32), so
-      // the pair carries ~16 significant bits and the rounding of P no longer
-      // limits the output error (a single bf16 P costs up to 2^-8 relative per
-      // weight, which rows dominated by a few keys do not average away).
-      // Key pair (2i, 2i+1) of chunk c goes to P column 16c + i; P_hi fills
-      // columns 0-63 and P_lo columns 64-127 of the S tile just read. Within
-      // chunk c, sr[c][2i] is reused for the P_hi pair, sr[c][2i+1] for P_lo.
+      // The format of P follows the format of this key tile's V (decided by
+      // the conversion warps, long done by now).
+      const int sv = j % NSV;
+      if (!__all_sync(0xffffffffu, wait_or_abort(bars.v_conv(sv), (j / NSV) & 1, abort_flag))) {
+        ok = false;
+        break;
+      }
+      const bool wide = *reinterpret_cast<volatile int*>(&vflags[2 * NSV + sv]) != 0;
       const uint64_t c2 = f2(scale_log2, scale_log2);
       const uint64_t nb2 = f2(-bias, -bias);
       uint64_t sumA = f2(0.f, 0.f), sumB = f2(0.f, 0.f);
+      if (!wide) {
+        // P in fp16 (11 significant bits, p <= 2^8 with the lazy rescale).
+        // Key pair (2i, 2i+1) of chunk c goes to P column 16c + i, i.e. the
+        // first 64 columns of the S tile just read; sr[c][i] is reused to
+        // stage that pair (its S values were consumed at step i/2).
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 4; ++c) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float y0, y1;
-          unf2(fma2(f2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])), c2, nb2),
-               y0, y1);
-          const float p0 = ex2_approx(y0);
-          const float p1 = ex2_approx(y1);
-          const uint64_t pp = f2(p0, p1);
-          if (i & 1) sumB = add2(sumB, pp); else sumA = add2(sumA, pp);
-          const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
-          uint32_t hi;
-          asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(hi) : "r"(u0), "r"(u1));
-          float d0, d1;
-          unf2(sub2(pp, f2(__uint_as_float(u0 & 0xffff0000u), __uint_as_float(u1 & 0xffff0000u))),
-               d0, d1);
-          sr[c][2 * i] = hi;
-          sr[c][2 * i + 1] = pack_bf16x2(d0, d1);
+          for (int i = 0; i < 16; ++i) {
+            float y0, y1;
+            unf2(fma2(f2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])), c2,
+                      nb2),
+                 y0, y1);
+            const float p0 = ex2_approx(y0);
+            const float p1 = ex2_approx(y1);
+            if (i & 1) sumB = add2(sumB, f2(p0, p1)); else sumA = add2(sumA, f2(p0, p1));
+            sr[c][i] = pack_f16x2(p0, p1);
+          }
         }
-      }
-      float sa0, sa1, sb0, sb1;
-      unf2(add2(sumA, sumB), sa0, sa1);
-      (void)sb0;
-      (void)sb1;
-      l = fmaf(l, alpha, sa0 + sa1);
-      {
+        uint32_t pw[32];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int i = 0; i < 16; ++i) pw[16 * c + i] = sr[2 * half + c][i];
+          tc::st32(tS + 32 * half, pw);  // P keys 64*half .. +63
+        }
+      } else {
+        // P = P_hi + P_lo, both bf16. P_hi is p truncated to bf16 (its upper
+        // 16 bits), P_lo = bf16(p - P_hi) (the difference is exact in fp32),
+        // so the pair carries ~16 significant bits (a single bf16 P costs up
+        // to 2^-8 relative per weight, which rows dominated by a few keys do
+        // not average away). Key pair (2i, 2i+1) of chunk c goes to P column
+        // 16c + i; P_hi fills columns 0-63 and P_lo columns 64-127. Within
+        // chunk c, sr[c][2i] is reused for the P_hi pair, sr[c][2i+1] for P_lo.
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            float y0, y1;
+            unf2(fma2(f2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])), c2,
+                      nb2),
+                 y0, y1);
+            const float p0 = ex2_approx(y0);
+            const float p1 = ex2_approx(y1);
+            const uint64_t pp = f2(p0, p1);
+            if (i & 1) sumB = add2(sumB, pp); else sumA = add2(sumA, pp);
+            const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
+            uint32_t hi;
+            asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(hi) : "r"(u0), "r"(u1));
+            float d0, d1;
+            unf2(sub2(pp, f2(__uint_as_float(u0 & 0xffff0000u), __uint_as_float(u1 & 0xffff0000u))),
+                 d0, d1);
+            sr[c][2 * i] = hi;
+            sr[c][2 * i + 1] = pack_bf16x2(d0, d1);
+          }
+        }
         uint32_t hi[32], lo[32];
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
@@ -420,6 +533,9 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
           tc::st32(tS + 64 + 32 * half, lo);  // P_lo keys 64*half .. +63
         }
       }
+      float sa0, sa1;
+      unf2(add2(sumA, sumB), sa0, sa1);
+      l = fmaf(l, alpha, sa0 + sa1);
       if (j > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
@@ -518,7 +634,7 @@ cudaError_t launch_prefill_bf16(const void* q, const void* k, const void* v, voi
   const bool pair = (g % 2) == 0;
   // Stage counts fill the shared memory next to the Q tiles (<= 227 KB).
   if (d_h == 128) {
-    return pair ? launch<128, 2, 3, 2>(q, k, v, o, lse, T, h, h_kv, causal, scale, stream)
+    return pair ? launch<128, 2, 2, 3>(q, k, v, o, lse, T, h, h_kv, causal, scale, stream)
                 : launch<128, 1, 3, 3>(q, k, v, o, lse, T, h, h_kv, causal, scale, stream);
   }
   return pair ? launch<64, 2, 4, 4>(q, k, v, o, lse, T, h, h_kv, causal, scale, stream)

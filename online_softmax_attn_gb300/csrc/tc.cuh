@@ -39,6 +39,18 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
          | (uint32_t(M >> 4) << 24);      // M / 16
 }
 
+// Instruction descriptor, kind::f16 with fp16 A/B and fp32 accumulation.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool a_mn_major,
+                                                     bool b_mn_major) {
+  return (1u << 4)                        // D format: f32
+         | (0u << 7)                      // A format: f16
+         | (0u << 10)                     // B format: f16
+         | (uint32_t(a_mn_major) << 15)
+         | (uint32_t(b_mn_major) << 16)
+         | (uint32_t(N >> 3) << 17)
+         | (uint32_t(M >> 4) << 24);
+}
+
 // D[tmem] (+)= A[smem] * B[smem]
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                        uint32_t idesc, uint32_t accumulate) {

@@ -84,6 +84,22 @@ def test_bf16_late_outlier_forces_rescale():
     check_lse(lse, L_ref)
 
 
+@pytest.mark.parametrize("d", [128, 64])
+def test_bf16_wide_values_keep_exact_path(d):
+    """Key tiles whose V holds a value beyond fp16's range (|v| >= 2^16) stay
+    bf16 and use the P_hi + P_lo product; the other tiles of the same rows use
+    fp16. The output matches the oracle either way."""
+    shape = W.PrefillShape("t", 4, 2, d, 400, torch.bfloat16, True)
+    q, k, v = W.prefill_inputs(shape, 21)
+    v[0, 130, 5] = 3.0e5     # key tile 1 of KV head 0
+    v[1, 300, 7] = -7.0e4    # key tile 2 of KV head 1
+    v[1, 20, 0] = 65504.0    # largest fp16 value: tile 0 stays fp16
+    O_ref, L_ref = oracle.attention_ref(q, k, v, shape.scale, True)
+    o, lse = run(q, k, v, True, shape.scale)
+    check_out(o, O_ref, torch.bfloat16)
+    check_lse(lse, L_ref)
+
+
 def test_gqa_T2048_causal_full():
     """The Llama-3-8B GQA layer at T = 2048, causal; full comparison."""
     shape = W.GQA_T2048_CAUSAL
