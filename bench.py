@@ -276,6 +276,8 @@ def run_gpu(args, world, rank, local):
     q, k, v = W.prefill_inputs(PREFILL, seed=rank, device=dev)
     o = torch.empty_like(q)
     lse = torch.empty((PREFILL.h, PREFILL.T), dtype=torch.float32, device=dev)
+    pws = torch.empty(attn.attn_prefill_workspace_bytes(PREFILL.T, PREFILL.h_kv, PREFILL.d_h),
+                      dtype=torch.uint8, device=dev)
     lens = W.decode_seq_lens(DECODE, seed=rank)
     if args.decode_rows:
         lens = lens[:args.decode_rows]  # smaller batch, for profiler captures only
@@ -295,7 +297,7 @@ def run_gpu(args, world, rank, local):
         flush.fill_(1)
         ev[0].record(stream)
         if do_pre:
-            attn.attn_prefill(q, k, v, True, PREFILL.scale, o=o, lse=lse)
+            attn.attn_prefill(q, k, v, True, PREFILL.scale, o=o, lse=lse, workspace=pws)
         ev[1].record(stream)
         if do_dec:
             attn.attn_decode_paged(dq, kc, vc, table, seq, S, DECODE.scale, workspace=ws, o=do, lse=dlse)
@@ -357,7 +359,7 @@ def run_gpu(args, world, rank, local):
             dq_.copy_(hq, non_blocking=True)
             dk_.copy_(hk, non_blocking=True)
             dv_.copy_(hv, non_blocking=True)
-            attn.attn_prefill(dq_, dk_, dv_, True, PREFILL.scale, o=o, lse=lse)
+            attn.attn_prefill(dq_, dk_, dv_, True, PREFILL.scale, o=o, lse=lse, workspace=pws)
             ho.copy_(o, non_blocking=True)
             hl.copy_(lse, non_blocking=True)
 
@@ -462,7 +464,8 @@ def run_gpu(args, world, rank, local):
         "prefill_ms": pre_avg,
         "e2e": e2e,
         "cpu_baseline": cpu,
-        "gpu_launches": (int(do_pre) + 2 * int(do_dec)) * args.steps,
+        # prefill: V-to-fp16 pass + attention kernel; decode: split kernel + merge
+        "gpu_launches": (2 * int(do_pre) + 2 * int(do_dec)) * args.steps,
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)

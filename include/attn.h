@@ -73,6 +73,15 @@ const char* attn_status_string(attn_status_t status);
 int attn_version(void);
 
 /*
+ * attn_prefill_workspace_bytes -- scratch attn_prefill can use for the given
+ * shape: an fp16 copy of V ([h_kv, T, d_h]) and one int per (KV head, 128-key
+ * tile) saying whether that tile fits fp16. Host-only, pure. 0 for
+ * ATTN_DTYPE_F32 (the SIMT path needs none) and for T == 0; (size_t)-1 on
+ * invalid arguments (T < 0, h_kv < 1, d_h not 64 or 128, unknown dtype).
+ */
+size_t attn_prefill_workspace_bytes(int T, int h_kv, int d_h, attn_dtype_t dtype);
+
+/*
  * attn_prefill -- exact attention of T queries over the same T keys, per head.
  * Follows [NA] opening section (Q [h,T,d_h], K/V [h_kv,T,d_h] broadcast to
  * g = h/h_kv query heads: query head hq reads KV head hq / g) and [NA] (3) /
@@ -89,14 +98,23 @@ int attn_version(void);
  *   dtype : ATTN_DTYPE_BF16 -> tcgen05 tensor-core path (d_h = 128 or 64),
  *           fp32 accumulation and statistics;
  *           ATTN_DTYPE_F32  -> fp32 SIMT path (d_h = 64 or 128), fp32 throughout.
+ *   workspace, workspace_bytes: caller-owned device scratch, 256-byte
+ *           aligned, at least attn_prefill_workspace_bytes(T, h_kv, d_h,
+ *           dtype) bytes; overwritten by the call (stream-ordered), so calls
+ *           sharing one workspace must not overlap on the GPU. May be NULL
+ *           (workspace_bytes ignored): the bf16 path then forms every P V
+ *           product as P_hi V + P_lo V in bf16, exact but slower. With a
+ *           workspace, V is first copied to fp16 (one extra kernel) and
+ *           P V is a single fp16 product wherever V fits fp16.
  * Errors: INVALID_ARG for NULL q/k/v/o (T > 0), T < 0, h < 1, h > 65535,
- * h_kv < 1, h % h_kv != 0, misaligned pointers, scale not finite and > 0;
- * UNSUPPORTED for other
- * d_h. T == 0 is a no-op returning ATTN_OK.
+ * h_kv < 1, h % h_kv != 0, misaligned pointers, scale not finite and > 0, a
+ * non-NULL workspace that is misaligned or smaller than required;
+ * UNSUPPORTED for other d_h. T == 0 is a no-op returning ATTN_OK.
  */
 attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o, float* lse,
                            int T, int h, int h_kv, int d_h, int causal, float scale,
-                           attn_dtype_t dtype, void* stream);
+                           attn_dtype_t dtype, void* workspace, size_t workspace_bytes,
+                           void* stream);
 
 /*
  * attn_decode_split_plan -- how one row's keys are cut into splits.

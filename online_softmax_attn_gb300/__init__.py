@@ -59,7 +59,9 @@ def library() -> ctypes.CDLL:
     lib.attn_status_string.argtypes = [I]
     lib.attn_status_string.restype = ctypes.c_char_p
     lib.attn_version.restype = I
-    lib.attn_prefill.argtypes = [P, P, P, P, P, I, I, I, I, I, F, I, P]
+    lib.attn_prefill_workspace_bytes.argtypes = [I, I, I, I]
+    lib.attn_prefill_workspace_bytes.restype = S
+    lib.attn_prefill.argtypes = [P, P, P, P, P, I, I, I, I, I, F, I, P, S, P]
     lib.attn_prefill.restype = I
     lib.attn_decode_split_plan.argtypes = [I, I, I, ctypes.POINTER(I)]
     lib.attn_decode_split_plan.restype = I
@@ -101,10 +103,23 @@ def _need(cond, msg):
         raise ValueError(msg)
 
 
+def attn_prefill_workspace_bytes(T: int, h_kv: int, d_h: int, dtype=torch.bfloat16) -> int:
+    """Bytes of scratch attn_prefill uses (fp16 copy of V + per-tile flags)."""
+    dt = ATTN_DTYPE_BF16 if dtype == torch.bfloat16 else ATTN_DTYPE_F32
+    n = library().attn_prefill_workspace_bytes(T, h_kv, d_h, dt)
+    if n == (1 << 64) - 1:
+        raise ValueError("invalid arguments to attn_prefill_workspace_bytes")
+    return n
+
+
 def attn_prefill(q, k, v, causal: bool, scale: float | None = None, o=None, lse=None,
-                 return_lse: bool = True, stream=None):
+                 return_lse: bool = True, stream=None, workspace="auto"):
     """Exact attention prefill. q [h,T,d], k/v [h_kv,T,d] (bf16 or fp32, CUDA,
-    contiguous). Returns (o [h,T,d] in q's dtype, lse [h,T] fp32 or None)."""
+    contiguous). Returns (o [h,T,d] in q's dtype, lse [h,T] fp32 or None).
+
+    workspace: a uint8 CUDA tensor of at least attn_prefill_workspace_bytes()
+    bytes, "auto" (allocated here through torch), or None (no scratch: every
+    P V product of the bf16 path takes the exact two-term bf16 form)."""
     _need(q.is_cuda and k.is_cuda and v.is_cuda, "tensors must be on a CUDA device")
     _need(q.dim() == 3 and k.dim() == 3 and v.shape == k.shape, "expected q [h,T,d], k/v [h_kv,T,d]")
     _need(q.dtype == k.dtype == v.dtype and q.dtype in (torch.bfloat16, torch.float32),
@@ -119,8 +134,18 @@ def attn_prefill(q, k, v, causal: bool, scale: float | None = None, o=None, lse=
     if lse is None and return_lse:
         lse = torch.empty((h, T), dtype=torch.float32, device=q.device)
     dt = ATTN_DTYPE_BF16 if q.dtype == torch.bfloat16 else ATTN_DTYPE_F32
+    if isinstance(workspace, str):
+        _need(workspace == "auto", 'workspace must be a tensor, "auto" or None')
+        n = attn_prefill_workspace_bytes(T, h_kv, d, q.dtype) if T > 0 else 0
+        workspace = torch.empty(n, dtype=torch.uint8, device=q.device) if n else None
+    ws_bytes = 0
+    if workspace is not None:
+        _need(workspace.is_cuda and workspace.dtype == torch.uint8 and workspace.is_contiguous(),
+              "workspace must be a contiguous uint8 CUDA tensor")
+        ws_bytes = workspace.numel()
     st = library().attn_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), T, h, h_kv, d,
-                                int(bool(causal)), scale, dt, _stream(stream))
+                                int(bool(causal)), scale, dt, _ptr(workspace), ws_bytes,
+                                _stream(stream))
     _check("attn_prefill", st)
     return o, lse
 

@@ -62,7 +62,7 @@ const char* attn_status_string(attn_status_t status) {
   return "unknown status";
 }
 
-int attn_version(void) { return 100; }
+int attn_version(void) { return 200; }
 
 int attn_decode_split_plan(int seq_len, int page_size, int num_splits, int* pages_per_split) {
   if (seq_len < 0 || page_size < 1 || num_splits < 1) return -1;
@@ -95,9 +95,17 @@ size_t attn_decode_workspace_bytes(int B, int h, int d_h, int num_splits) {
   return partial_layout(static_cast<long long>(B) * h, num_splits, d_h).total;
 }
 
+size_t attn_prefill_workspace_bytes(int T, int h_kv, int d_h, attn_dtype_t dtype) {
+  if (T < 0 || h_kv < 1 || (d_h != 64 && d_h != 128)) return static_cast<size_t>(-1);
+  if (dtype != ATTN_DTYPE_F32 && dtype != ATTN_DTYPE_BF16) return static_cast<size_t>(-1);
+  if (dtype == ATTN_DTYPE_F32 || T == 0) return 0;
+  return attn::prefill_layout(T, h_kv, d_h).total;
+}
+
 attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o, float* lse,
                            int T, int h, int h_kv, int d_h, int causal, float scale,
-                           attn_dtype_t dtype, void* stream) {
+                           attn_dtype_t dtype, void* workspace, size_t workspace_bytes,
+                           void* stream) {
   if (T < 0 || h < 1 || h_kv < 1 || h % h_kv != 0 || !std::isfinite(scale) || !(scale > 0.f))
     return ATTN_ERR_INVALID_ARG;
   if (h > 65535) return ATTN_ERR_INVALID_ARG;
@@ -108,13 +116,17 @@ attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o,
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
       !aligned(lse, 4))
     return ATTN_ERR_INVALID_ARG;
+  if (workspace && (!aligned(workspace, 256) ||
+                    workspace_bytes < attn_prefill_workspace_bytes(T, h_kv, d_h, dtype)))
+    return ATTN_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (dtype == ATTN_DTYPE_F32)
     return from_cuda(launch_prefill_f32(static_cast<const float*>(q),
                                         static_cast<const float*>(k),
                                         static_cast<const float*>(v), static_cast<float*>(o), lse,
                                         T, h, h_kv, d_h, causal != 0, scale, s));
-  const cudaError_t e = launch_prefill_bf16(q, k, v, o, lse, T, h, h_kv, d_h, causal != 0, scale, s);
+  const cudaError_t e =
+      launch_prefill_bf16(q, k, v, o, lse, T, h, h_kv, d_h, causal != 0, scale, workspace, s);
   if (e == cudaErrorNotSupported) return ATTN_ERR_UNSUPPORTED;
   return from_cuda(e);
 }

@@ -59,9 +59,16 @@ cudaError_t launch_prefill_f32(const float* q, const float* k, const float* v, f
                                float scale, cudaStream_t stream);
 
 // prefill_tc.cu --------------------------------------------------------------
+// Workspace carve-up: fp16 copy of V [h_kv, T, d_h], then one int flag per
+// (KV head, 128-key tile).
+struct PrefillLayout {
+  size_t v16_off, flags_off, total;
+};
+PrefillLayout prefill_layout(int T, int h_kv, int d_h);
+// workspace == nullptr: every key tile takes the exact bf16 P_hi + P_lo path.
 cudaError_t launch_prefill_bf16(const void* q, const void* k, const void* v, void* o, float* lse,
                                 int T, int h, int h_kv, int d_h, int causal, float scale,
-                                cudaStream_t stream);
+                                void* workspace, cudaStream_t stream);
 unsigned int prefill_read_and_clear_error(cudaStream_t stream, cudaError_t* st);
 
 // tensor maps ---------------------------------------------------------------

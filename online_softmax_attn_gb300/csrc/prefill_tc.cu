@@ -6,25 +6,30 @@
 // two dense contractions; the row max only ever rises, and when it does the
 // old l and O~ are multiplied by exp(m_old - m_new); O = O~ / l at the end,
 // LSE = m + ln l. "The Online Softmax Recurrence" / "Where it breaks": the
-// statistics stay fp32 while P and the operands are bf16. The pages' own
-// remark that any common shift is legal ("The state that gets passed around
-// is the log-sum-exp") licenses the lazy rescale used here: the reference max
-// is only moved when the row max exceeds it by more than 2^8 (in exp2 units),
-// so most tiles skip the O~ rescale; O~ and l always share one reference, so
-// the result is unchanged.
+// statistics stay fp32 while the operands are 16-bit. The pages' remark that
+// any common shift is legal ("The state that gets passed around is the
+// log-sum-exp") licenses the reference used here: l, O~ and each tile's
+// weights P share one exp2-domain reference m_ref, which need not be the row
+// max. A tile is exponentiated against the reference of the tiles before it
+// (no row max on the common path); only the first tile, or one whose weights
+// would leave fp16's range, takes its row max first. The reference rises by
+// log2 of a tile's weight sum once that sum passes 2^10, so O~ is rescaled
+// rarely; O = O~ / l and LSE are independent of the reference.
 //
 // GB300 design (one CTA per (KV head, 128-query block, pair of query heads)):
-//   * warp 8      : TMA producer. Q tiles of both heads once, then K and V
-//                   tiles of the shared KV head through an NS-stage ring
-//                   (128-byte swizzle, 64-element boxes).
-//   * warp 9      : tensor-memory allocator and MMA issuer (one thread).
-//                   S_t = Q_t K^T (SS MMA, M=N=128, K=d_h) into tensor memory,
-//                   O_t += P_t V (TS MMA: P read from tensor memory, V from
-//                   shared memory, V consumed MN-major as stored).
-//   * warps 0-3, 4-7 : one softmax warpgroup per query head; thread = row
-//                   (tensor-memory lane), so the row max and sum need no
-//                   shuffles. P (bf16) is written over the first 64 columns
-//                   of its own S tile.
+//   * softmax warpgroups (warps 0-3, 4-7), one per query head; thread = row
+//     (tensor-memory lane), so row sums and maxima need no shuffles. P is
+//     written over the first columns of its own S tile: fp16 for a V tile
+//     that converts to fp16 exactly, else bf16 P_hi and P_lo.
+//   * control warpgroup: warp 8 is the TMA producer (Q of both heads once,
+//     then K and V of the shared KV head through rings of their own, 128-byte
+//     swizzle, 64-element boxes); warp 9 allocates tensor memory and issues
+//     the MMAs as a whole warp (elect.sync picks the issuing lane):
+//     S_t = Q_t K^T (SS, M=N=128, K=d_h) and O_t += P_t V (TS: P from tensor
+//     memory, V from shared memory, MN-major as stored); warps 10-11 idle.
+//   * before it, v_to_f16_kernel converts V once per KV head into an fp16
+//     copy (exact for |v| < 2^16) and flags each 128-key tile holding a value
+//     fp16 cannot carry; flagged tiles are read as bf16 and take P_hi + P_lo.
 //   The two heads ping-pong: while one warpgroup exponentiates its S tile,
 //   the tensor core runs the other head's P V and next Q K^T.
 //   Causal CTAs visit only key tiles up to the diagonal (the masked half of
@@ -43,7 +48,11 @@ namespace {
 
 constexpr int kBM = 128;  // query rows per tile (tensor-memory lanes)
 constexpr int kBN = 128;  // keys per tile
-constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when max rises > 2^8
+// A tile's weights are accepted in fp16 while their sum stays <= 2^15 (each
+// weight then fits fp16, whose largest finite value is 65504); the reference
+// moves once a tile's weights sum past 2^10.
+constexpr float kOverflowSum = 32768.0f;
+constexpr float kMoveSum = 1024.0f;
 
 template <int D, int NQ, int NSK, int NSV>
 struct PfCfg {
@@ -56,20 +65,16 @@ struct PfCfg {
   static constexpr int V_OFF = K_OFF + NSK * KTILE;
   static constexpr int BAR_OFF = V_OFF + NSV * KTILE;
   // q_full, k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV], s_full[NQ],
-  // p_full[NQ], o_final[NQ], mma_done, v_check[NSV], v_conv[NSV]
-  static constexpr int NBAR = 1 + 2 * NSK + 2 * NSV + 3 * NQ + 1 + 2 * NSV;
-  static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
-  // tensor-memory slot, abort flag, then V-format flags: per stage one
-  // "wide" bit per converter warp [NSV][2] and the stage's verdict [NSV].
-  static constexpr int FLAG_OFF = MISC_OFF + 16;
-  static constexpr int SMEM = FLAG_OFF + 3 * NSV * 4 + 1024;  // + alignment slack
+  // p_full[NQ], o_final[NQ], mma_done
+  static constexpr int NBAR = 1 + 2 * NSK + 2 * NSV + 3 * NQ + 1;
+  static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;  // tensor-memory slot, abort flag
+  static constexpr int SMEM = MISC_OFF + 16 + 1024;    // + alignment slack
   static constexpr int TMEM_COLS = NQ == 1 ? 256 : 512;
   // NQ softmax warpgroups + one control warpgroup (TMA warp, MMA warp, two
-  // idle warps), so that register shares can be moved per warpgroup.
+  // idle warps: setmaxnreg moves registers per whole warpgroup).
   static constexpr int THREADS = NQ * 128 + 128;
   static constexpr int PRODUCER_WARP = NQ * 4;
   static constexpr int MMA_WARP = NQ * 4 + 1;
-  static constexpr int CONV_WARP0 = NQ * 4 + 2;  // two V-conversion warps
   // Register split (NQ = 2): launched at 168/thread (384 x 168 = 64512);
   // control warpgroup drops to 88, softmax warpgroups rise to 208:
   // 2 x 128 x 208 + 128 x 88 = 64512 <= 64512.
@@ -139,12 +144,6 @@ struct Bars {
     return base + 8 * (1 + 2 * nsk + 2 * nsv + 2 * nq + t);
   }
   __device__ uint32_t mma_done() const { return base + 8 * (1 + 2 * nsk + 2 * nsv + 3 * nq); }
-  __device__ uint32_t v_check(int s) const {
-    return base + 8 * (2 + 2 * nsk + 2 * nsv + 3 * nq + s);
-  }
-  __device__ uint32_t v_conv(int s) const {
-    return base + 8 * (2 + 2 * nsk + 3 * nsv + 3 * nq + s);
-  }
 };
 
 // Bounded wait that also gives up at once when another role has aborted.
@@ -170,7 +169,8 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
     prefill_bf16_kernel(const __grid_constant__ CUtensorMap tmap_q,
                         const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v,
-                        __nv_bfloat16* __restrict__ o, float* __restrict__ lse, int T, int h,
+                        const __grid_constant__ CUtensorMap tmap_v16,
+                        const int* __restrict__ vwide, __nv_bfloat16* __restrict__ o, float* __restrict__ lse, int T, int h,
                         int h_kv, int causal, float scale_log2, int n_qblk) {
   using C = PfCfg<D, NQ, NSK, NSV>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -188,17 +188,18 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
   const int kvh = hq0 / (h / h_kv);
   const int n_kv_all = (T + kBN - 1) / kBN;
   const int nkv = causal ? min(qb + 1, n_kv_all) : n_kv_all;
-
-  int* vflags = reinterpret_cast<int*>(smem + C::FLAG_OFF);  // [NSV][2] then [NSV]
+  // Per key tile of this KV head: nonzero -> V stays bf16 (exact P_hi + P_lo
+  // product); zero -> V is read from its fp16 copy (fp16 P). No flags: all
+  // tiles bf16.
+  const int* tile_wide = vwide ? vwide + size_t(kvh) * n_kv_all : nullptr;
+  auto is_wide = [&](int j) { return tile_wide ? (__ldg(tile_wide + j) != 0) : true; };
 
   if (threadIdx.x == 0) {
-    // p_full collects one arrival per softmax thread, v_check and v_conv one
-    // per conversion warp; the others take one.
+    // p_full collects one arrival per softmax thread; the others take one.
     for (int i = 0; i < C::NBAR; ++i) {
       const uint32_t bar = bars.base + 8 * i;
       const bool is_p = bar >= bars.p_full(0) && bar < bars.p_full(0) + 8 * NQ;
-      const bool is_v = bar >= bars.v_check(0) && bar < bars.v_check(0) + 16 * NSV;
-      mbar_init(bar, is_p ? 128u : (is_v ? 2u : 1u));
+      mbar_init(bar, is_p ? 128u : 1u);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -219,6 +220,7 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
       prefetch_tmap(&tmap_q);
       prefetch_tmap(&tmap_k);
       prefetch_tmap(&tmap_v);
+      if (tile_wide) prefetch_tmap(&tmap_v16);
       mbar_arrive_expect_tx(bars.q_full(), NQ * C::QTILE);
       for (int t = 0; t < NQ; ++t)
         for (int s = 0; s < C::SUBS; ++s)
@@ -237,8 +239,9 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
         k_issued = j + 1;
         if (j >= NSV && !wait_or_abort(bars.v_empty(sv), ((j / NSV) - 1) & 1, abort_flag)) break;
         mbar_arrive_expect_tx(bars.v_full(sv), C::KTILE);
+        const CUtensorMap* vmap = is_wide(j) ? &tmap_v : &tmap_v16;
         for (int s = 0; s < C::SUBS; ++s)
-          tma_load_3d(sbase + C::V_OFF + sv * C::KTILE + s * C::SUB_BYTES, &tmap_v,
+          tma_load_3d(sbase + C::V_OFF + sv * C::KTILE + s * C::SUB_BYTES, vmap,
                       bars.v_full(sv), s * 64, j * kBN, kvh);
         v_issued = j + 1;
       }
@@ -278,8 +281,8 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
       };
       constexpr uint32_t idO16 = tc::idesc_f16_f32(kBM, D, false, true);
       // O_t += P V. Normal tiles: P fp16 (S columns 0-63) times the fp16 copy
-      // of V made by the conversion warps. Wide tiles (some |v| >= 2^16, kept
-      // bf16): O_t += P_hi V + P_lo V with P_hi in columns 0-63, P_lo 64-127.
+      // of V. Wide tiles (some |v| >= 2^16, kept bf16): O_t += P_hi V + P_lo V
+      // with P_hi in columns 0-63, P_lo in columns 64-127.
       auto issue_pv = [&](int t, int st, bool acc, bool wide) {
         const uint64_t dvb = dv0 + uint64_t((st * C::KTILE) >> 4);
         const uint32_t dO = tmem + t * 256 + 128;
@@ -314,17 +317,13 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
       // Order per key tile j: P_0 V_j, S_0(j+1), P_1 V_j, S_1(j+1): each head's
       // next QK^T follows its own P V (P aliases S in tensor memory), and the
       // other head's softmax runs while these MMAs execute.
-      bool wide = false;
       for (int j = 0; ok && j < nkv; ++j) {
         const int sv = j % NSV;
         const int sk1 = (j + 1) % NSK;
+        const bool wide = is_wide(j);
         for (int t = 0; t < NQ && ok; ++t) {
           if (!wait(bars.p_full(t), j & 1)) { ok = false; break; }
-          if (t == 0) {
-            // V tile j converted (or found wide and left bf16).
-            if (!wait(bars.v_conv(sv), (j / NSV) & 1)) { ok = false; break; }
-            wide = *reinterpret_cast<volatile int*>(&vflags[2 * NSV + sv]) != 0;
-          }
+          if (t == 0 && !wait(bars.v_full(sv), (j / NSV) & 1)) { ok = false; break; }
           tc::fence_after();
           issue_pv(t, sv, j > 0, wide);
           if (j == nkv - 1) tc::commit_elect(bars.o_final(t));
@@ -342,58 +341,6 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
       tc::commit_elect(bars.mma_done());
       (void)__all_sync(0xffffffffu, mbar_wait(bars.mma_done(), 0, &g_prefill_err));
     }
-  } else {
-    // ------------------------------------------------------------ V conversion
-    // Two warps turn each V tile from bf16 into fp16 in place, so that P can
-    // be an fp16 operand (11 significant bits) and P V a single MMA. bf16
-    // values convert exactly while |v| < 2^16 (fp16's top binade; values below
-    // 2^-17 round with an absolute error under 2^-25). A tile holding any
-    // |v| >= 2^16 (or inf/NaN) is "wide": it stays bf16 and takes the
-    // P_hi + P_lo path. Pass 1 checks the range of each warp's half, the two
-    // warps agree through v_check, pass 2 converts.
-    const int cw = warp - C::CONV_WARP0;
-    constexpr int CHUNKS = kBN * D * 2 / 16;  // 16-byte chunks per V tile
-    constexpr int HALF = CHUNKS / 2;
-    for (int j = 0; j < nkv; ++j) {
-      const int sv = j % NSV;
-      if (!__all_sync(0xffffffffu, wait_or_abort(bars.v_full(sv), (j / NSV) & 1, abort_flag)))
-        break;
-      uint4* tile = reinterpret_cast<uint4*>(smem + C::V_OFF + sv * C::KTILE);
-      uint32_t mx = 0;
-      for (int i = cw * HALF + lane; i < (cw + 1) * HALF; i += 32) {
-        const uint4 x = tile[i];
-        uint32_t m2;
-        asm("max.u16x2 %0, %1, %2;" : "=r"(m2) : "r"(x.x & 0x7fff7fffu), "r"(x.y & 0x7fff7fffu));
-        asm("max.u16x2 %0, %0, %1;" : "+r"(m2) : "r"(x.z & 0x7fff7fffu));
-        asm("max.u16x2 %0, %0, %1;" : "+r"(m2) : "r"(x.w & 0x7fff7fffu));
-        asm("max.u16x2 %0, %0, %1;" : "+r"(mx) : "r"(m2));
-      }
-      // bf16 bits 0x4780 = 2^16: the first magnitude fp16 cannot hold.
-      const bool my_wide =
-          __any_sync(0xffffffffu, (mx & 0xffffu) >= 0x4780u || (mx >> 16) >= 0x4780u);
-      if (lane == 0) vflags[sv * 2 + cw] = my_wide ? 1 : 0;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bars.v_check(sv));
-      if (!__all_sync(0xffffffffu, wait_or_abort(bars.v_check(sv), (j / NSV) & 1, abort_flag)))
-        break;
-      const volatile int* vf = vflags;
-      const bool wide = (vf[sv * 2] | vf[sv * 2 + 1]) != 0;
-      if (!wide) {
-        for (int i = cw * HALF + lane; i < (cw + 1) * HALF; i += 32) {
-          const uint4 x = tile[i];
-          uint4 y;
-          y.x = pack_f16x2(bf16lo(x.x), bf16hi(x.x));
-          y.y = pack_f16x2(bf16lo(x.y), bf16hi(x.y));
-          y.z = pack_f16x2(bf16lo(x.z), bf16hi(x.z));
-          y.w = pack_f16x2(bf16lo(x.w), bf16hi(x.w));
-          tile[i] = y;
-        }
-        fence_proxy_async_smem();  // generic stores -> visible to the tensor core
-      }
-      if (cw == 0 && lane == 0) vflags[2 * NSV + sv] = wide ? 1 : 0;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bars.v_conv(sv));
-    }
   }
   } else {
     // ------------------------------------------------------------ softmax
@@ -405,80 +352,99 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
     const int hq = hq0 + t;
     const uint32_t tS = tmem + (uint32_t(wq * 32) << 16) + t * 256;
     const uint32_t tO = tS + 128;
-    float m_ref = -INFINITY;  // exp2-domain reference max shared by l and O~
+    // m_ref: exp2-domain reference that l, O~ and this tile's P are relative
+    // to. pend: factor O~ still owes after a reference move (applied once the
+    // P V MMA of the tile that moved it has completed, or at the end).
+    float m_ref = -INFINITY;
     float l = 0.f;
+    float pend = 1.f;
     bool ok = true;
     for (int j = 0; j < nkv; ++j) {
+      // The format of P follows the format of this key tile's V.
+      const bool wide = is_wide(j);
       // Warp-uniform outcome: the tensor-memory loads below are warp-collective.
       if (!__all_sync(0xffffffffu, wait_or_abort(bars.s_full(t), j & 1, abort_flag))) {
         ok = false;
         break;
       }
       tc::fence_after();
-      uint32_t sr[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tc::ld32(tS + c * 32, sr[c]);
-      tc::wait_ld();
-
       int lim = kBN;
       if (j * kBN + kBN > T) lim = T - j * kBN;
       if (causal && j == qb) lim = min(lim, r + 1);
-      if (lim < kBN) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (c * 32 + i >= lim) sr[c][i] = __float_as_uint(-INFINITY);
-      }
-      // Row max: four independent chains of 3-input max, then combine.
-      float mxc[4];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        mxc[c] = __uint_as_float(sr[c][0]);
-#pragma unroll
-        for (int i = 1; i < 31; i += 2)
-          mxc[c] = max3f(mxc[c], __uint_as_float(sr[c][i]), __uint_as_float(sr[c][i + 1]));
-        mxc[c] = fmaxf(mxc[c], __uint_as_float(sr[c][31]));
-      }
-      const float mx = fmaxf(fmaxf(mxc[0], mxc[1]), fmaxf(mxc[2], mxc[3]));
-
-      const float m_cand = mx * scale_log2;
-      const bool need = m_cand > m_ref + kRescaleThreshold;
-      float alpha = 1.f;
-      if (need) {
-        alpha = ex2_approx(m_ref - m_cand);  // 0 on the first tile
-        m_ref = m_cand;
-      }
-      const float bias = (m_ref == -INFINITY) ? 0.f : m_ref;
-      // The format of P follows the format of this key tile's V (decided by
-      // the conversion warps, long done by now).
-      const int sv = j % NSV;
-      if (!__all_sync(0xffffffffu, wait_or_abort(bars.v_conv(sv), (j / NSV) & 1, abort_flag))) {
-        ok = false;
-        break;
-      }
-      const bool wide = *reinterpret_cast<volatile int*>(&vflags[2 * NSV + sv]) != 0;
       const uint64_t c2 = f2(scale_log2, scale_log2);
-      const uint64_t nb2 = f2(-bias, -bias);
-      uint64_t sumA = f2(0.f, 0.f), sumB = f2(0.f, 0.f);
-      if (!wide) {
-        // P in fp16 (11 significant bits, p <= 2^8 with the lazy rescale).
-        // Key pair (2i, 2i+1) of chunk c goes to P column 16c + i, i.e. the
-        // first 64 columns of the S tile just read; sr[c][i] is reused to
-        // stage that pair (its S values were consumed at step i/2).
+      uint32_t sr[4][32];
+      float sum_t = 0.f;
+      // Pass 0 exponentiates against the reference of the earlier tiles, with
+      // no row max on the way. Its weights are accepted unless one of them
+      // could exceed fp16's range (the tile's sum > 2^15); then, and on the
+      // first tile, pass 1 reloads S, takes the row max and moves the
+      // reference to it first. Any common shift leaves O and LSE unchanged.
+      bool slow = (j == 0);
+      auto load_s = [&]() {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tc::ld32(tS + c * 32, sr[c]);
+        tc::wait_ld();
+        if (lim < kBN) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (c * 32 + i >= lim) sr[c][i] = __float_as_uint(-INFINITY);
+        }
+      };
+      auto move_to_row_max = [&]() {
+        // Row max: four independent chains of 3-input max, then combine.
+        float mxc[4];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
+          mxc[c] = __uint_as_float(sr[c][0]);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            float y0, y1;
-            unf2(fma2(f2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])), c2,
-                      nb2),
-                 y0, y1);
-            const float p0 = ex2_approx(y0);
-            const float p1 = ex2_approx(y1);
-            if (i & 1) sumB = add2(sumB, f2(p0, p1)); else sumA = add2(sumA, f2(p0, p1));
-            sr[c][i] = pack_f16x2(p0, p1);
+          for (int i = 1; i < 31; i += 2)
+            mxc[c] = max3f(mxc[c], __uint_as_float(sr[c][i]), __uint_as_float(sr[c][i + 1]));
+          mxc[c] = fmaxf(mxc[c], __uint_as_float(sr[c][31]));
+        }
+        const float mx = fmaxf(fmaxf(mxc[0], mxc[1]), fmaxf(mxc[2], mxc[3]));
+        const float m_new = fmaxf(m_ref, mx * scale_log2);
+        if (m_new > m_ref) {
+          const float alpha = ex2_approx(m_ref - m_new);  // 0 on the first tile
+          l *= alpha;
+          if (j > 0) pend *= alpha;
+          m_ref = m_new;
+        }
+      };
+      // !(x <= bound) also sends an inf (or NaN) sum to the slow pass.
+      auto overflow = [&]() { return __any_sync(0xffffffffu, !(sum_t <= kOverflowSum)); };
+      if (!wide) {
+#pragma unroll 1
+        for (int pass = 0; pass < 2; ++pass) {
+          load_s();
+          if (slow) move_to_row_max();
+          const float bias = (m_ref == -INFINITY) ? 0.f : m_ref;
+          const uint64_t nb2 = f2(-bias, -bias);
+          uint64_t sumA = f2(0.f, 0.f), sumB = f2(0.f, 0.f);
+          // P in fp16 (11 significant bits). Key pair (2i, 2i+1) of chunk c
+          // goes to P column 16c + i, i.e. the first 64 columns of the S tile
+          // just read; sr[c][i] is reused to stage that pair (its S values
+          // were consumed at step i/2).
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              float y0, y1;
+              unf2(fma2(f2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])), c2,
+                        nb2),
+                   y0, y1);
+              const float p0 = ex2_approx(y0);
+              const float p1 = ex2_approx(y1);
+              if (i & 1) sumB = add2(sumB, f2(p0, p1)); else sumA = add2(sumA, f2(p0, p1));
+              sr[c][i] = pack_f16x2(p0, p1);
+            }
           }
+          float sa0, sa1;
+          unf2(add2(sumA, sumB), sa0, sa1);
+          sum_t = sa0 + sa1;
+          if (slow || !overflow()) break;
+          slow = true;
         }
         uint32_t pw[32];
 #pragma unroll
@@ -490,35 +456,48 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
           tc::st32(tS + 32 * half, pw);  // P keys 64*half .. +63
         }
       } else {
-        // P = P_hi + P_lo, both bf16. P_hi is p truncated to bf16 (its upper
-        // 16 bits), P_lo = bf16(p - P_hi) (the difference is exact in fp32),
-        // so the pair carries ~16 significant bits (a single bf16 P costs up
-        // to 2^-8 relative per weight, which rows dominated by a few keys do
-        // not average away). Key pair (2i, 2i+1) of chunk c goes to P column
-        // 16c + i; P_hi fills columns 0-63 and P_lo columns 64-127. Within
-        // chunk c, sr[c][2i] is reused for the P_hi pair, sr[c][2i+1] for P_lo.
+#pragma unroll 1
+        for (int pass = 0; pass < 2; ++pass) {
+          load_s();
+          if (slow) move_to_row_max();
+          const float bias = (m_ref == -INFINITY) ? 0.f : m_ref;
+          const uint64_t nb2 = f2(-bias, -bias);
+          uint64_t sumA = f2(0.f, 0.f), sumB = f2(0.f, 0.f);
+          // P = P_hi + P_lo, both bf16. P_hi is p truncated to bf16 (its upper
+          // 16 bits), P_lo = bf16(p - P_hi) (the difference is exact in fp32),
+          // so the pair carries ~16 significant bits (a single bf16 P costs up
+          // to 2^-8 relative per weight, which rows dominated by a few keys do
+          // not average away). Within chunk c, sr[c][2i] is reused for the
+          // P_hi pair of keys (2i, 2i+1), sr[c][2i+1] for P_lo.
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < 4; ++c) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            float y0, y1;
-            unf2(fma2(f2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])), c2,
-                      nb2),
-                 y0, y1);
-            const float p0 = ex2_approx(y0);
-            const float p1 = ex2_approx(y1);
-            const uint64_t pp = f2(p0, p1);
-            if (i & 1) sumB = add2(sumB, pp); else sumA = add2(sumA, pp);
-            const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
-            uint32_t hi;
-            asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(hi) : "r"(u0), "r"(u1));
-            float d0, d1;
-            unf2(sub2(pp, f2(__uint_as_float(u0 & 0xffff0000u), __uint_as_float(u1 & 0xffff0000u))),
-                 d0, d1);
-            sr[c][2 * i] = hi;
-            sr[c][2 * i + 1] = pack_bf16x2(d0, d1);
+            for (int i = 0; i < 16; ++i) {
+              float y0, y1;
+              unf2(fma2(f2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])), c2,
+                        nb2),
+                   y0, y1);
+              const float p0 = ex2_approx(y0);
+              const float p1 = ex2_approx(y1);
+              const uint64_t pp = f2(p0, p1);
+              if (i & 1) sumB = add2(sumB, pp); else sumA = add2(sumA, pp);
+              const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
+              uint32_t hi;
+              asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(hi) : "r"(u0), "r"(u1));
+              float d0, d1;
+              unf2(sub2(pp, f2(__uint_as_float(u0 & 0xffff0000u), __uint_as_float(u1 & 0xffff0000u))),
+                   d0, d1);
+              sr[c][2 * i] = hi;
+              sr[c][2 * i + 1] = pack_bf16x2(d0, d1);
+            }
           }
+          float sa0, sa1;
+          unf2(add2(sumA, sumB), sa0, sa1);
+          sum_t = sa0 + sa1;
+          if (slow || !overflow()) break;
+          slow = true;
         }
+        // P_hi fills columns 0-63 and P_lo columns 64-127.
         uint32_t hi[32], lo[32];
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
@@ -533,16 +512,16 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
           tc::st32(tS + 64 + 32 * half, lo);  // P_lo keys 64*half .. +63
         }
       }
-      float sa0, sa1;
-      unf2(add2(sumA, sumB), sa0, sa1);
-      l = fmaf(l, alpha, sa0 + sa1);
-      if (j > 0 && __any_sync(0xffffffffu, need)) {
+      l += sum_t;
+      // O~ now holds the P V of tiles < j (complete: this tile's S was issued
+      // after them); settle what it owes before this tile's P V adds to it.
+      if (j > 0 && __any_sync(0xffffffffu, pend != 1.f)) {
+        const uint64_t a2 = f2(pend, pend);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t ov[32];
           tc::ld32(tO + c * 32, ov);
           tc::wait_ld();
-          const uint64_t a2 = f2(alpha, alpha);
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             float x0, x1;
@@ -553,6 +532,18 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
           tc::st32(tO + c * 32, ov);
         }
       }
+      pend = 1.f;
+      // Lazy reference move: once a tile's weights sum past 2^10 the
+      // reference rises by log2 of that sum, so later weights stay far from
+      // fp16's limit. l moves now; O~ owes the same factor once this tile's
+      // P V has landed in it.
+      if (sum_t > kMoveSum) {
+        const float m_new = m_ref + __log2f(sum_t);
+        const float alpha = ex2_approx(m_ref - m_new);
+        l *= alpha;
+        pend = alpha;
+        m_ref = m_new;
+      }
       tc::wait_st();
       tc::fence_before();
       mbar_arrive(bars.p_full(t));
@@ -561,7 +552,7 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
     if (ok) {
       tc::fence_after();
       const bool empty = !(l > 0.f);
-      const float inv = empty ? 0.f : 1.f / l;
+      const float inv = empty ? 0.f : pend / l;
       __nv_bfloat16* orow = o + (size_t(hq) * T + row) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
@@ -591,12 +582,46 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
   if (warp == C::MMA_WARP) tc::dealloc(tmem, C::TMEM_COLS);
 }
 
+// V (bf16 [h_kv, T, d_h]) -> fp16 copy with the same layout, and one flag per
+// (KV head, 128-key tile): 1 when the tile holds a value with |v| >= 2^16
+// (or inf / NaN), which fp16 cannot carry; such tiles are read from the bf16
+// original by the attention kernel. bf16 -> fp16 is exact for
+// 2^-14 <= |v| < 2^16 (8 significant bits fit in 11); smaller values round
+// with an absolute error below 2^-25. One CTA per tile, 16-byte accesses.
+__global__ void __launch_bounds__(256)
+    v_to_f16_kernel(const uint4* __restrict__ v, uint4* __restrict__ v16, int* __restrict__ vwide,
+                    int T, int chunks_per_row, int n_tiles) {
+  const int tile = blockIdx.x, kvh = blockIdx.y;
+  const int rows = min(kBN, T - tile * kBN);
+  const size_t base = (size_t(kvh) * T + size_t(tile) * kBN) * chunks_per_row;
+  const int n = rows * chunks_per_row;
+  uint32_t mx = 0;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const uint4 x = v[base + i];
+    uint32_t m2;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(m2) : "r"(x.x & 0x7fff7fffu), "r"(x.y & 0x7fff7fffu));
+    asm("max.u16x2 %0, %0, %1;" : "+r"(m2) : "r"(x.z & 0x7fff7fffu));
+    asm("max.u16x2 %0, %0, %1;" : "+r"(m2) : "r"(x.w & 0x7fff7fffu));
+    asm("max.u16x2 %0, %0, %1;" : "+r"(mx) : "r"(m2));
+    uint4 y;
+    y.x = pack_f16x2(bf16lo(x.x), bf16hi(x.x));
+    y.y = pack_f16x2(bf16lo(x.y), bf16hi(x.y));
+    y.z = pack_f16x2(bf16lo(x.z), bf16hi(x.z));
+    y.w = pack_f16x2(bf16lo(x.w), bf16hi(x.w));
+    v16[base + i] = y;
+  }
+  // bf16 bits 0x4780 = 2^16: the first magnitude fp16 cannot hold.
+  const int wide = __syncthreads_or((mx & 0xffffu) >= 0x4780u || (mx >> 16) >= 0x4780u);
+  if (threadIdx.x == 0) vwide[size_t(kvh) * n_tiles + tile] = wide;
+}
+
 template <int D, int NQ, int NSK, int NSV>
-cudaError_t launch(const void* q, const void* k, const void* v, void* o, float* lse, int T, int h,
-                   int h_kv, int causal, float scale, cudaStream_t stream) {
+cudaError_t launch(const void* q, const void* k, const void* v, const void* v16, const int* vwide,
+                   void* o, float* lse, int T, int h, int h_kv, int causal, float scale,
+                   cudaStream_t stream) {
   using C = PfCfg<D, NQ, NSK, NSV>;
   static_assert(C::SMEM <= 232448, "shared memory budget");
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, tv16;
   const uint32_t box[3] = {64u, 128u, 1u};
   {
     const uint64_t dims[3] = {uint64_t(D), uint64_t(T), uint64_t(h)};
@@ -614,31 +639,57 @@ cudaError_t launch(const void* q, const void* k, const void* v, void* o, float* 
     if (encode_tensor_map(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(v), dims,
                           strides, box, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
+    // Without the fp16 copy the map is a duplicate of the bf16 one, never used.
+    if (encode_tensor_map(&tv16, v16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                          3, const_cast<void*>(v16 ? v16 : v), dims, strides, box,
+                          CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
   }
   auto kern = prefill_bf16_kernel<D, NQ, NSK, NSV>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   const int n_qblk = (T + kBM - 1) / kBM;
   const dim3 grid(n_qblk, h / NQ);
-  kern<<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, static_cast<__nv_bfloat16*>(o), lse, T,
-                                               h, h_kv, causal, scale * kLog2e, n_qblk);
+  kern<<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tv16, v16 ? vwide : nullptr,
+                                               static_cast<__nv_bfloat16*>(o), lse, T, h, h_kv,
+                                               causal, scale * kLog2e, n_qblk);
   return cudaGetLastError();
 }
 
 }  // namespace
 
+PrefillLayout prefill_layout(int T, int h_kv, int d_h) {
+  PrefillLayout L;
+  L.v16_off = 0;
+  L.flags_off = align256(size_t(h_kv) * T * d_h * 2);
+  L.total = L.flags_off + align256(size_t(h_kv) * ((T + kBN - 1) / kBN) * sizeof(int));
+  return L;
+}
+
 cudaError_t launch_prefill_bf16(const void* q, const void* k, const void* v, void* o, float* lse,
                                 int T, int h, int h_kv, int d_h, int causal, float scale,
-                                cudaStream_t stream) {
+                                void* workspace, cudaStream_t stream) {
   const int g = h / h_kv;
   const bool pair = (g % 2) == 0;
+  void* v16 = nullptr;
+  int* vwide = nullptr;
+  if (workspace) {
+    const PrefillLayout L = prefill_layout(T, h_kv, d_h);
+    v16 = static_cast<uint8_t*>(workspace) + L.v16_off;
+    vwide = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + L.flags_off);
+    const int n_tiles = (T + kBN - 1) / kBN;
+    v_to_f16_kernel<<<dim3(n_tiles, h_kv), 256, 0, stream>>>(
+        static_cast<const uint4*>(v), static_cast<uint4*>(v16), vwide, T, d_h / 8, n_tiles);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   // Stage counts fill the shared memory next to the Q tiles (<= 227 KB).
   if (d_h == 128) {
-    return pair ? launch<128, 2, 2, 3>(q, k, v, o, lse, T, h, h_kv, causal, scale, stream)
-                : launch<128, 1, 3, 3>(q, k, v, o, lse, T, h, h_kv, causal, scale, stream);
+    return pair ? launch<128, 2, 2, 3>(q, k, v, v16, vwide, o, lse, T, h, h_kv, causal, scale, stream)
+                : launch<128, 1, 3, 3>(q, k, v, v16, vwide, o, lse, T, h, h_kv, causal, scale, stream);
   }
-  return pair ? launch<64, 2, 4, 4>(q, k, v, o, lse, T, h, h_kv, causal, scale, stream)
-              : launch<64, 1, 4, 4>(q, k, v, o, lse, T, h, h_kv, causal, scale, stream);
+  return pair ? launch<64, 2, 4, 4>(q, k, v, v16, vwide, o, lse, T, h, h_kv, causal, scale, stream)
+              : launch<64, 1, 4, 4>(q, k, v, v16, vwide, o, lse, T, h, h_kv, causal, scale, stream);
 }
 
 unsigned int prefill_read_and_clear_error(cudaStream_t stream, cudaError_t* st) {

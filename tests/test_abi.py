@@ -110,18 +110,24 @@ def test_invalid_arguments_rejected_before_launch(lib):
     S = attn.attn_status_string
     bad = attn.ATTN_ERR_INVALID_ARG
     # h not a multiple of h_kv
-    assert lib.attn_prefill(dummy, dummy, dummy, dummy, None, 64, 6, 4, 128, 1, 0.1, 1, None) == bad
+    assert lib.attn_prefill(dummy, dummy, dummy, dummy, None, 64, 6, 4, 128, 1, 0.1, 1, None, 0, None) == bad
     # negative T, non-positive scale, NaN scale
-    assert lib.attn_prefill(dummy, dummy, dummy, dummy, None, -1, 4, 4, 128, 1, 0.1, 1, None) == bad
-    assert lib.attn_prefill(dummy, dummy, dummy, dummy, None, 64, 4, 4, 128, 1, 0.0, 1, None) == bad
-    assert lib.attn_prefill(dummy, dummy, dummy, dummy, None, 64, 4, 4, 128, 1, float("nan"), 1, None) == bad
+    assert lib.attn_prefill(dummy, dummy, dummy, dummy, None, -1, 4, 4, 128, 1, 0.1, 1, None, 0, None) == bad
+    assert lib.attn_prefill(dummy, dummy, dummy, dummy, None, 64, 4, 4, 128, 1, 0.0, 1, None, 0, None) == bad
+    assert lib.attn_prefill(dummy, dummy, dummy, dummy, None, 64, 4, 4, 128, 1, float("nan"), 1, None, 0, None) == bad
     # misaligned pointer
-    assert lib.attn_prefill(P(258), dummy, dummy, dummy, None, 64, 4, 4, 128, 1, 0.1, 1, None) == bad
+    assert lib.attn_prefill(P(258), dummy, dummy, dummy, None, 64, 4, 4, 128, 1, 0.1, 1, None, 0, None) == bad
     # unsupported head size
-    assert lib.attn_prefill(dummy, dummy, dummy, dummy, None, 64, 4, 4, 96, 1, 0.1, 1, None) == \
+    assert lib.attn_prefill(dummy, dummy, dummy, dummy, None, 64, 4, 4, 96, 1, 0.1, 1, None, 0, None) == \
         attn.ATTN_ERR_UNSUPPORTED
     # T = 0 is a no-op
-    assert lib.attn_prefill(None, None, None, None, None, 0, 4, 4, 128, 1, 0.1, 1, None) == 0
+    assert lib.attn_prefill(None, None, None, None, None, 0, 4, 4, 128, 1, 0.1, 1, None, 0, None) == 0
+    # prefill workspace: misaligned, or smaller than attn_prefill_workspace_bytes
+    need = lib.attn_prefill_workspace_bytes(64, 4, 128, 1)
+    assert lib.attn_prefill(dummy, dummy, dummy, dummy, None, 64, 4, 4, 128, 1, 0.1, 1, P(272), need,
+                            None) == bad
+    assert lib.attn_prefill(dummy, dummy, dummy, dummy, None, 64, 4, 4, 128, 1, 0.1, 1, dummy, need - 1,
+                            None) == bad
     # decode: workspace too small, page size, group size, split count
     args = [dummy, dummy, dummy, dummy, dummy, 2, 32, 8, 128, 16, 100, 10, 16, 0.1, dummy, 16,
             dummy, None, None]
@@ -142,3 +148,16 @@ def test_invalid_arguments_rejected_before_launch(lib):
         attn.ATTN_ERR_UNSUPPORTED
     assert lib.attn_merge_states(None, None, None, None, 0, 2, 128, None, None, 1, None) == 0
     assert S(bad) == "invalid argument"
+
+
+def test_prefill_workspace_bytes(lib):
+    """fp16 copy of V (256-byte aligned) followed by one int per (KV head, 128-key tile)."""
+    assert lib.attn_prefill_workspace_bytes(8192, 8, 128, 1) == 8 * 8192 * 128 * 2 + 2048  # then 8 x 64 ints
+    assert lib.attn_prefill_workspace_bytes(333, 2, 64, 1) == 85248 + 256  # 2*333*64*2, then 6 ints
+    assert lib.attn_prefill_workspace_bytes(8192, 8, 128, 0) == 0  # fp32 SIMT path: none
+    assert lib.attn_prefill_workspace_bytes(0, 8, 128, 1) == 0
+    none = (1 << 64) - 1
+    assert lib.attn_prefill_workspace_bytes(-1, 8, 128, 1) == none
+    assert lib.attn_prefill_workspace_bytes(64, 0, 128, 1) == none
+    assert lib.attn_prefill_workspace_bytes(64, 8, 96, 1) == none
+    assert lib.attn_prefill_workspace_bytes(64, 8, 128, 7) == none

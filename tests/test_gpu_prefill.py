@@ -100,6 +100,18 @@ def test_bf16_wide_values_keep_exact_path(d):
     check_lse(lse, L_ref)
 
 
+@pytest.mark.parametrize("d,causal", [(128, True), (64, False)])
+def test_bf16_without_workspace(d, causal):
+    """No scratch: every key tile takes the exact two-term bf16 P V product."""
+    shape = W.PrefillShape("t", 8, 2, d, 333, torch.bfloat16, causal)
+    q, k, v = W.prefill_inputs(shape, 9)
+    O_ref, L_ref = oracle.attention_ref(q, k, v, shape.scale, causal)
+    o, lse = attn.attn_prefill(q.cuda(), k.cuda(), v.cuda(), causal, shape.scale, workspace=None)
+    torch.cuda.synchronize()
+    check_out(o, O_ref, torch.bfloat16)
+    check_lse(lse, L_ref)
+
+
 def test_gqa_T2048_causal_full():
     """The Llama-3-8B GQA layer at T = 2048, causal; full comparison."""
     shape = W.GQA_T2048_CAUSAL
