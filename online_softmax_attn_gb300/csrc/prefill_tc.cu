@@ -48,10 +48,10 @@ namespace {
 
 constexpr int kBM = 128;  // query rows per tile (tensor-memory lanes)
 constexpr int kBN = 128;  // keys per tile
-// A tile's weights are accepted in fp16 while their sum stays <= 2^15 (each
-// weight then fits fp16, whose largest finite value is 65504); the reference
-// moves once a tile's weights sum past 2^10.
-constexpr float kOverflowSum = 32768.0f;
+// A tile's weights are accepted in fp16 while their sum stays <= 65504, the
+// largest finite fp16 value (so every weight fits); the reference moves once
+// a tile's weights sum past 2^10.
+constexpr float kOverflowSum = 65504.0f;
 constexpr float kMoveSum = 1024.0f;
 
 template <int D, int NQ, int NSK, int NSV>
@@ -376,20 +376,15 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
       float sum_t = 0.f;
       // Pass 0 exponentiates against the reference of the earlier tiles, with
       // no row max on the way. Its weights are accepted unless one of them
-      // could exceed fp16's range (the tile's sum > 2^15); then, and on the
+      // could exceed fp16's range (the tile's sum > 65504); then, and on the
       // first tile, pass 1 reloads S, takes the row max and moves the
       // reference to it first. Any common shift leaves O and LSE unchanged.
       bool slow = (j == 0);
-      auto load_s = [&]() {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tc::ld32(tS + c * 32, sr[c]);
-        tc::wait_ld();
+      auto mask = [&](int c) {
         if (lim < kBN) {
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (c * 32 + i >= lim) sr[c][i] = __float_as_uint(-INFINITY);
+          for (int i = 0; i < 32; ++i)
+            if (c * 32 + i >= lim) sr[c][i] = __float_as_uint(-INFINITY);
         }
       };
       auto move_to_row_max = [&]() {
@@ -412,37 +407,50 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
           m_ref = m_new;
         }
       };
+      // One pass over the tile: S from tensor memory, weights against the
+      // current reference (after moving it to the row max on a slow pass),
+      // chunk by chunk through `chunk`; returns the tile's weight sum.
+      auto run_pass = [&](auto&& chunk) -> float {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tc::ld32(tS + c * 32, sr[c]);
+        tc::wait_ld();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) mask(c);
+        if (slow) move_to_row_max();
+        const float bias = (m_ref == -INFINITY) ? 0.f : m_ref;
+        const uint64_t nb2 = f2(-bias, -bias);
+        uint64_t sumA = f2(0.f, 0.f), sumB = f2(0.f, 0.f);
+        chunk(0, nb2, sumA, sumB);
+        chunk(1, nb2, sumA, sumB);
+        chunk(2, nb2, sumA, sumB);
+        chunk(3, nb2, sumA, sumB);
+        float sa0, sa1;
+        unf2(add2(sumA, sumB), sa0, sa1);
+        return sa0 + sa1;
+      };
       // !(x <= bound) also sends an inf (or NaN) sum to the slow pass.
       auto overflow = [&]() { return __any_sync(0xffffffffu, !(sum_t <= kOverflowSum)); };
       if (!wide) {
+        // P in fp16 (11 significant bits). Key pair (2i, 2i+1) of chunk c
+        // goes to P column 16c + i, i.e. the first 64 columns of the S tile
+        // just read; sr[c][i] is reused to stage that pair (its S values
+        // were consumed at step i/2).
+        auto chunk16 = [&](int c, uint64_t nb2, uint64_t& sumA, uint64_t& sumB) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            float y0, y1;
+            unf2(fma2(f2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])), c2,
+                      nb2),
+                 y0, y1);
+            const float p0 = ex2_approx(y0);
+            const float p1 = ex2_approx(y1);
+            if (i & 1) sumB = add2(sumB, f2(p0, p1)); else sumA = add2(sumA, f2(p0, p1));
+            sr[c][i] = pack_f16x2(p0, p1);
+          }
+        };
 #pragma unroll 1
         for (int pass = 0; pass < 2; ++pass) {
-          load_s();
-          if (slow) move_to_row_max();
-          const float bias = (m_ref == -INFINITY) ? 0.f : m_ref;
-          const uint64_t nb2 = f2(-bias, -bias);
-          uint64_t sumA = f2(0.f, 0.f), sumB = f2(0.f, 0.f);
-          // P in fp16 (11 significant bits). Key pair (2i, 2i+1) of chunk c
-          // goes to P column 16c + i, i.e. the first 64 columns of the S tile
-          // just read; sr[c][i] is reused to stage that pair (its S values
-          // were consumed at step i/2).
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              float y0, y1;
-              unf2(fma2(f2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])), c2,
-                        nb2),
-                   y0, y1);
-              const float p0 = ex2_approx(y0);
-              const float p1 = ex2_approx(y1);
-              if (i & 1) sumB = add2(sumB, f2(p0, p1)); else sumA = add2(sumA, f2(p0, p1));
-              sr[c][i] = pack_f16x2(p0, p1);
-            }
-          }
-          float sa0, sa1;
-          unf2(add2(sumA, sumB), sa0, sa1);
-          sum_t = sa0 + sa1;
+          sum_t = run_pass(chunk16);
           if (slow || !overflow()) break;
           slow = true;
         }
@@ -456,44 +464,36 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
           tc::st32(tS + 32 * half, pw);  // P keys 64*half .. +63
         }
       } else {
+        // P = P_hi + P_lo, both bf16. P_hi is p truncated to bf16 (its upper
+        // 16 bits), P_lo = bf16(p - P_hi) (the difference is exact in fp32),
+        // so the pair carries ~16 significant bits (a single bf16 P costs up
+        // to 2^-8 relative per weight, which rows dominated by a few keys do
+        // not average away). Within chunk c, sr[c][2i] is reused for the
+        // P_hi pair of keys (2i, 2i+1), sr[c][2i+1] for P_lo.
+        auto chunk_hl = [&](int c, uint64_t nb2, uint64_t& sumA, uint64_t& sumB) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            float y0, y1;
+            unf2(fma2(f2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])), c2,
+                      nb2),
+                 y0, y1);
+            const float p0 = ex2_approx(y0);
+            const float p1 = ex2_approx(y1);
+            const uint64_t pp = f2(p0, p1);
+            if (i & 1) sumB = add2(sumB, pp); else sumA = add2(sumA, pp);
+            const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
+            uint32_t hi;
+            asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(hi) : "r"(u0), "r"(u1));
+            float d0, d1;
+            unf2(sub2(pp, f2(__uint_as_float(u0 & 0xffff0000u), __uint_as_float(u1 & 0xffff0000u))),
+                 d0, d1);
+            sr[c][2 * i] = hi;
+            sr[c][2 * i + 1] = pack_bf16x2(d0, d1);
+          }
+        };
 #pragma unroll 1
         for (int pass = 0; pass < 2; ++pass) {
-          load_s();
-          if (slow) move_to_row_max();
-          const float bias = (m_ref == -INFINITY) ? 0.f : m_ref;
-          const uint64_t nb2 = f2(-bias, -bias);
-          uint64_t sumA = f2(0.f, 0.f), sumB = f2(0.f, 0.f);
-          // P = P_hi + P_lo, both bf16. P_hi is p truncated to bf16 (its upper
-          // 16 bits), P_lo = bf16(p - P_hi) (the difference is exact in fp32),
-          // so the pair carries ~16 significant bits (a single bf16 P costs up
-          // to 2^-8 relative per weight, which rows dominated by a few keys do
-          // not average away). Within chunk c, sr[c][2i] is reused for the
-          // P_hi pair of keys (2i, 2i+1), sr[c][2i+1] for P_lo.
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              float y0, y1;
-              unf2(fma2(f2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])), c2,
-                        nb2),
-                   y0, y1);
-              const float p0 = ex2_approx(y0);
-              const float p1 = ex2_approx(y1);
-              const uint64_t pp = f2(p0, p1);
-              if (i & 1) sumB = add2(sumB, pp); else sumA = add2(sumA, pp);
-              const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
-              uint32_t hi;
-              asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(hi) : "r"(u0), "r"(u1));
-              float d0, d1;
-              unf2(sub2(pp, f2(__uint_as_float(u0 & 0xffff0000u), __uint_as_float(u1 & 0xffff0000u))),
-                   d0, d1);
-              sr[c][2 * i] = hi;
-              sr[c][2 * i + 1] = pack_bf16x2(d0, d1);
-            }
-          }
-          float sa0, sa1;
-          unf2(add2(sumA, sumB), sa0, sa1);
-          sum_t = sa0 + sa1;
+          sum_t = run_pass(chunk_hl);
           if (slow || !overflow()) break;
           slow = true;
         }
@@ -516,20 +516,24 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
       // O~ now holds the P V of tiles < j (complete: this tile's S was issued
       // after them); settle what it owes before this tile's P V adds to it.
       if (j > 0 && __any_sync(0xffffffffu, pend != 1.f)) {
+        // All of O~ in one round trip; the S registers are free once the P
+        // stores have drained.
+        tc::wait_st();
         const uint64_t a2 = f2(pend, pend);
 #pragma unroll
+        for (int c = 0; c < D / 32; ++c) tc::ld32(tO + c * 32, sr[c]);
+        tc::wait_ld();
+#pragma unroll
         for (int c = 0; c < D / 32; ++c) {
-          uint32_t ov[32];
-          tc::ld32(tO + c * 32, ov);
-          tc::wait_ld();
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             float x0, x1;
-            unf2(mul2(f2(__uint_as_float(ov[2 * i]), __uint_as_float(ov[2 * i + 1])), a2), x0, x1);
-            ov[2 * i] = __float_as_uint(x0);
-            ov[2 * i + 1] = __float_as_uint(x1);
+            unf2(mul2(f2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])), a2),
+                 x0, x1);
+            sr[c][2 * i] = __float_as_uint(x0);
+            sr[c][2 * i + 1] = __float_as_uint(x1);
           }
-          tc::st32(tO + c * 32, ov);
+          tc::st32(tO + c * 32, sr[c]);
         }
       }
       pend = 1.f;
