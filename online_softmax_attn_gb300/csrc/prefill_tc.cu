@@ -48,11 +48,10 @@ namespace {
 
 constexpr int kBM = 128;  // query rows per tile (tensor-memory lanes)
 constexpr int kBN = 128;  // keys per tile
-// A tile's weights are accepted in fp16 while their sum stays <= 65504, the
-// largest finite fp16 value (so every weight fits); the reference moves once
-// a tile's weights sum past 2^10.
-constexpr float kOverflowSum = 65504.0f;
-constexpr float kMoveSum = 1024.0f;
+// The reference moves to the row max only when that exceeds it by more than
+// this (log2 units): weights stay at most 2^15, below fp16's largest finite
+// value (65504).
+constexpr float kRescaleBits = 15.0f;
 
 template <int D, int NQ, int NSK, int NSV>
 struct PfCfg {
@@ -353,11 +352,10 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
     const uint32_t tS = tmem + (uint32_t(wq * 32) << 16) + t * 256;
     const uint32_t tO = tS + 128;
     // m_ref: exp2-domain reference that l, O~ and this tile's P are relative
-    // to. pend: factor O~ still owes after a reference move (applied once the
-    // P V MMA of the tile that moved it has completed, or at the end).
+    // to (the row max of some tile seen so far, within 2^15 of the running
+    // max).
     float m_ref = -INFINITY;
     float l = 0.f;
-    float pend = 1.f;
     bool ok = true;
     for (int j = 0; j < nkv; ++j) {
       // The format of P follows the format of this key tile's V.
@@ -373,69 +371,73 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
       if (causal && j == qb) lim = min(lim, r + 1);
       const uint64_t c2 = f2(scale_log2, scale_log2);
       uint32_t sr[4][32];
-      float sum_t = 0.f;
-      // Pass 0 exponentiates against the reference of the earlier tiles, with
-      // no row max on the way. Its weights are accepted unless one of them
-      // could exceed fp16's range (the tile's sum > 65504); then, and on the
-      // first tile, pass 1 reloads S, takes the row max and moves the
-      // reference to it first. Any common shift leaves O and LSE unchanged.
-      bool slow = (j == 0);
-      auto mask = [&](int c) {
-        if (lim < kBN) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tc::ld32(tS + c * 32, sr[c]);
+      tc::wait_ld();
+      if (lim < kBN) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
 #pragma unroll
           for (int i = 0; i < 32; ++i)
             if (c * 32 + i >= lim) sr[c][i] = __float_as_uint(-INFINITY);
+      }
+      // Row max: per 32-column chunk a tree of 3-input maxima (11 -> 4 -> 1),
+      // then the four chunk maxima. Then the lazy reference rule: the
+      // reference moves to the row max only when that exceeds it by more than
+      // 2^15 (so every weight, at most 2^15, fits fp16); otherwise l and O~
+      // keep their scale.
+      float cm[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        auto x = [&](int i) { return __uint_as_float(sr[c][i]); };
+        float a[11];
+#pragma unroll
+        for (int i = 0; i < 10; ++i) a[i] = max3f(x(3 * i), x(3 * i + 1), x(3 * i + 2));
+        a[10] = fmaxf(x(30), x(31));
+        cm[c] = fmaxf(max3f(max3f(a[0], a[1], a[2]), max3f(a[3], a[4], a[5]), max3f(a[6], a[7], a[8])),
+                      fmaxf(a[9], a[10]));
+      }
+      const float mx = fmaxf(max3f(cm[0], cm[1], cm[2]), cm[3]);
+      const float m_cand = mx * scale_log2;
+      float alpha = 1.f;
+      if (m_cand > m_ref + kRescaleBits) {
+        alpha = ex2_approx(m_ref - m_cand);  // 0 on the first tile
+        l *= alpha;
+        m_ref = m_cand;
+      }
+      // O~ holds the P V of tiles < j (complete: this tile's S was issued
+      // after them) and is scaled by alpha before this tile's P V adds to it,
+      // 32 columns at a time between the chunks of exponentials.
+      const bool rescale = j > 0 && __any_sync(0xffffffffu, alpha != 1.f);
+      const uint64_t a2 = f2(alpha, alpha);
+      uint32_t ov[32];
+      auto o_load = [&](int c) {
+        if (rescale && c < D / 32) tc::ld32(tO + c * 32, ov);
+      };
+      auto o_store = [&](int c) {
+        if (rescale && c < D / 32) {
+          tc::wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            float x0, x1;
+            unf2(mul2(f2(__uint_as_float(ov[2 * i]), __uint_as_float(ov[2 * i + 1])), a2), x0, x1);
+            ov[2 * i] = __float_as_uint(x0);
+            ov[2 * i + 1] = __float_as_uint(x1);
+          }
+          tc::st32(tO + c * 32, ov);
         }
       };
-      auto move_to_row_max = [&]() {
-        // Row max: four independent chains of 3-input max, then combine.
-        float mxc[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          mxc[c] = __uint_as_float(sr[c][0]);
-#pragma unroll
-          for (int i = 1; i < 31; i += 2)
-            mxc[c] = max3f(mxc[c], __uint_as_float(sr[c][i]), __uint_as_float(sr[c][i + 1]));
-          mxc[c] = fmaxf(mxc[c], __uint_as_float(sr[c][31]));
-        }
-        const float mx = fmaxf(fmaxf(mxc[0], mxc[1]), fmaxf(mxc[2], mxc[3]));
-        const float m_new = fmaxf(m_ref, mx * scale_log2);
-        if (m_new > m_ref) {
-          const float alpha = ex2_approx(m_ref - m_new);  // 0 on the first tile
-          l *= alpha;
-          if (j > 0) pend *= alpha;
-          m_ref = m_new;
-        }
-      };
-      // One pass over the tile: S from tensor memory, weights against the
-      // current reference (after moving it to the row max on a slow pass),
-      // chunk by chunk through `chunk`; returns the tile's weight sum.
-      auto run_pass = [&](auto&& chunk) -> float {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tc::ld32(tS + c * 32, sr[c]);
-        tc::wait_ld();
-#pragma unroll
-        for (int c = 0; c < 4; ++c) mask(c);
-        if (slow) move_to_row_max();
-        const float bias = (m_ref == -INFINITY) ? 0.f : m_ref;
-        const uint64_t nb2 = f2(-bias, -bias);
-        uint64_t sumA = f2(0.f, 0.f), sumB = f2(0.f, 0.f);
-        chunk(0, nb2, sumA, sumB);
-        chunk(1, nb2, sumA, sumB);
-        chunk(2, nb2, sumA, sumB);
-        chunk(3, nb2, sumA, sumB);
-        float sa0, sa1;
-        unf2(add2(sumA, sumB), sa0, sa1);
-        return sa0 + sa1;
-      };
-      // !(x <= bound) also sends an inf (or NaN) sum to the slow pass.
-      auto overflow = [&]() { return __any_sync(0xffffffffu, !(sum_t <= kOverflowSum)); };
+      const float bias = (m_ref == -INFINITY) ? 0.f : m_ref;
+      const uint64_t nb2 = f2(-bias, -bias);
+      uint64_t sumA = f2(0.f, 0.f), sumB = f2(0.f, 0.f);
       if (!wide) {
         // P in fp16 (11 significant bits). Key pair (2i, 2i+1) of chunk c
         // goes to P column 16c + i, i.e. the first 64 columns of the S tile
         // just read; sr[c][i] is reused to stage that pair (its S values
         // were consumed at step i/2).
-        auto chunk16 = [&](int c, uint64_t nb2, uint64_t& sumA, uint64_t& sumB) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          o_load(c);
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             float y0, y1;
@@ -447,12 +449,7 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
             if (i & 1) sumB = add2(sumB, f2(p0, p1)); else sumA = add2(sumA, f2(p0, p1));
             sr[c][i] = pack_f16x2(p0, p1);
           }
-        };
-#pragma unroll 1
-        for (int pass = 0; pass < 2; ++pass) {
-          sum_t = run_pass(chunk16);
-          if (slow || !overflow()) break;
-          slow = true;
+          o_store(c);
         }
         uint32_t pw[32];
 #pragma unroll
@@ -470,7 +467,9 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
         // to 2^-8 relative per weight, which rows dominated by a few keys do
         // not average away). Within chunk c, sr[c][2i] is reused for the
         // P_hi pair of keys (2i, 2i+1), sr[c][2i+1] for P_lo.
-        auto chunk_hl = [&](int c, uint64_t nb2, uint64_t& sumA, uint64_t& sumB) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          o_load(c);
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             float y0, y1;
@@ -490,12 +489,7 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
             sr[c][2 * i] = hi;
             sr[c][2 * i + 1] = pack_bf16x2(d0, d1);
           }
-        };
-#pragma unroll 1
-        for (int pass = 0; pass < 2; ++pass) {
-          sum_t = run_pass(chunk_hl);
-          if (slow || !overflow()) break;
-          slow = true;
+          o_store(c);
         }
         // P_hi fills columns 0-63 and P_lo columns 64-127.
         uint32_t hi[32], lo[32];
@@ -512,42 +506,9 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
           tc::st32(tS + 64 + 32 * half, lo);  // P_lo keys 64*half .. +63
         }
       }
-      l += sum_t;
-      // O~ now holds the P V of tiles < j (complete: this tile's S was issued
-      // after them); settle what it owes before this tile's P V adds to it.
-      if (j > 0 && __any_sync(0xffffffffu, pend != 1.f)) {
-        // All of O~ in one round trip; the S registers are free once the P
-        // stores have drained.
-        tc::wait_st();
-        const uint64_t a2 = f2(pend, pend);
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) tc::ld32(tO + c * 32, sr[c]);
-        tc::wait_ld();
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            float x0, x1;
-            unf2(mul2(f2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])), a2),
-                 x0, x1);
-            sr[c][2 * i] = __float_as_uint(x0);
-            sr[c][2 * i + 1] = __float_as_uint(x1);
-          }
-          tc::st32(tO + c * 32, sr[c]);
-        }
-      }
-      pend = 1.f;
-      // Lazy reference move: once a tile's weights sum past 2^10 the
-      // reference rises by log2 of that sum, so later weights stay far from
-      // fp16's limit. l moves now; O~ owes the same factor once this tile's
-      // P V has landed in it.
-      if (sum_t > kMoveSum) {
-        const float m_new = m_ref + __log2f(sum_t);
-        const float alpha = ex2_approx(m_ref - m_new);
-        l *= alpha;
-        pend = alpha;
-        m_ref = m_new;
-      }
+      float sa0, sa1;
+      unf2(add2(sumA, sumB), sa0, sa1);
+      l += sa0 + sa1;
       tc::wait_st();
       tc::fence_before();
       mbar_arrive(bars.p_full(t));
@@ -556,7 +517,7 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
     if (ok) {
       tc::fence_after();
       const bool empty = !(l > 0.f);
-      const float inv = empty ? 0.f : pend / l;
+      const float inv = empty ? 0.f : 1.f / l;
       __nv_bfloat16* orow = o + (size_t(hq) * T + row) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {

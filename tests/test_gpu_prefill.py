@@ -112,6 +112,26 @@ def test_bf16_without_workspace(d, causal):
     check_lse(lse, L_ref)
 
 
+@pytest.mark.parametrize("causal", [True, False])
+def test_bf16_extreme_logits_take_row_max_pass(causal):
+    """Logits far outside fp32's exponent range relative to the carried
+    reference: one key 2^10 (log2 units) above the rest of its row (an inf
+    weight sum sends the tile back for its row max), and query rows whose
+    first key tile lies 2^10 below zero (a zero weight sum on the first tile)."""
+    shape = W.PrefillShape("t", 4, 2, 128, 300, torch.bfloat16, causal)
+    q, k, v = W.prefill_inputs(shape, 13)
+    ones = torch.ones(128, dtype=torch.bfloat16)
+    q[0, 270] = 8 * ones
+    k[0, 260] = 8 * ones          # q.k * scale * log2(e) ~ +1045 for (head 0, row 270)
+    q[2, 0:128] = -8 * ones
+    k[1, 0:128] = 8 * ones        # heads 2-3, first key tile ~ -1045 for rows 0-127
+    O_ref, L_ref = oracle.attention_ref(q, k, v, shape.scale, causal)
+    o, lse = run(q, k, v, causal, shape.scale)
+    check_out(o, O_ref, torch.bfloat16)
+    check_lse(lse, L_ref)
+    assert attn.attn_get_device_error() == 0
+
+
 def test_gqa_T2048_causal_full():
     """The Llama-3-8B GQA layer at T = 2048, causal; full comparison."""
     shape = W.GQA_T2048_CAUSAL
