@@ -15,17 +15,26 @@
 //     around bytes in flight: each warp owns a private ring of NST stages, and
 //     each stage receives one K page and one V page of its KV head (16 tokens x
 //     d_h bf16 each) through a 4-D TMA tensor map over the cache
-//     [num_blocks, 16, h_kv, d_h]. The page's 16 rows of 2*d_h bytes are
-//     gathered by the copy engine; the SM only waits on an mbarrier.
-//   * Arithmetic stays fp32 SIMT (no tensor cores: the contraction per page is
-//     16 x d_h x g, far too thin, and the kernel is bandwidth-bound anyway).
-//     A lane owns 8 consecutive d_h elements (one 16-byte shared-memory read
-//     per row), keeps q for all g heads in registers, and the per-token dot
-//     products are finished with a reduce-scatter across the d_h/8 lanes of a
-//     row so that each lane ends with one head's score.
+//     [num_blocks, 16, h_kv, d_h], in 64-element halves with the 128-byte
+//     swizzle (so that fragment loads hit distinct shared-memory banks). The
+//     page's 16 rows are gathered by the copy engine; the SM only waits on an
+//     mbarrier.
+//   * Per page, the two contractions are warp-level tensor-core MMAs
+//     (m16n8k16, bf16 in, fp32 accumulate) with the g query heads of the KV
+//     head as the M rows (rows g..15 are zero): S = q K^T over the page's 16
+//     keys, then O~ += P V over d_h. The S accumulator fragment of a lane is
+//     exactly the P operand fragment of the next MMA, so scores never leave
+//     registers, and the fragments of K and V come from ldmatrix (V
+//     transposed). This keeps the instruction count per page an order of
+//     magnitude below a SIMT dot product with cross-lane reductions, so a warp
+//     spends its time waiting for bytes rather than issuing.
+//   * P is the exact two-term bf16 split P_hi + P_lo (P_hi = p truncated to
+//     bf16, P_lo = bf16(p - P_hi)), two MMAs per V fragment: a single bf16 P
+//     loses up to 2^-8 relative per weight, which rows dominated by a few keys
+//     do not average away.
 //   * Softmax statistics are per page: one max and one rescale per 16 keys,
-//     in base 2 (q is pre-multiplied by scale*log2(e)); partial m is written
-//     back in natural-log units.
+//     in base 2 (scores are scaled by scale*log2(e) in fp32 after the MMA);
+//     partial m is written back in natural-log units.
 //   * Warps of a CTA take pages round-robin and merge their states through
 //     shared memory at the end, so a CTA writes one partial per head.
 //   * Launch geometry depends only on (B, h_kv, num_splits); surplus splits of
@@ -41,47 +50,49 @@ namespace {
 
 constexpr int kPage = 16;
 
-// Reduce-scatter of N per-lane partial sums across the LPT lanes of a row:
-// afterwards lane's v[0] holds the full sum for value index
-// (lane & (LPT-1)) >> log2(LPT/N).
-template <int N, int MASK>
-struct ReduceScatter {
-  static __device__ __forceinline__ void run(float* v, int lane) {
-    if constexpr (N > 1) {
-      constexpr int H = N / 2;
-      const bool up = (lane & MASK) != 0;
-#pragma unroll
-      for (int i = 0; i < H; ++i) {
-        const float send = up ? v[i] : v[i + H];
-        const float keep = up ? v[i + H] : v[i];
-        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, MASK);
-      }
-      ReduceScatter<H, MASK / 2>::run(v, lane);
-    } else if constexpr (MASK >= 1) {
-      v[0] += __shfl_xor_sync(0xffffffffu, v[0], MASK);
-      ReduceScatter<1, MASK / 2>::run(v, lane);
-    }
-  }
-};
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+// D (16x8 fp32) += A (16x16 bf16, rows 8..15 zero) * B (16x8 bf16).
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
 
 template <int D, int G, int NW, int NST>
 struct DecodeCfg {
-  static constexpr int LPT = D / 8;          // lanes per token row
-  static constexpr int TPS = 32 / LPT;       // token rows per warp step
-  static constexpr int RS = kPage / TPS;     // steps per page
-  static constexpr int PAGE_BYTES = kPage * D * 2;
-  static constexpr int STAGE_BYTES = 2 * PAGE_BYTES;  // K page + V page
+  static constexpr int HALVES = D / 64;             // 64-element (128-byte) swizzled halves
+  static constexpr int HALF_BYTES = kPage * 128;    // one half of one page: 16 rows x 128 B
+  static constexpr int PAGE_BYTES = kPage * D * 2;  // K or V page
+  static constexpr int STAGE_BYTES = 2 * PAGE_BYTES;
   static constexpr int RING_BYTES = NW * NST * STAGE_BYTES;
   static constexpr int MERGE_BYTES = NW * G * D * 4;
-  static constexpr int P_BYTES = NW * kPage * G * 4;
-  static constexpr int A_BYTES = NW * G * 4;
   static constexpr int ML_BYTES = NW * G * 2 * 4;
   static constexpr int BAR_BYTES = NW * NST * 8;
-  static constexpr int SMEM = RING_BYTES + MERGE_BYTES + P_BYTES + A_BYTES + ML_BYTES +
-                              BAR_BYTES + 1024;  // + alignment slack
-  static_assert(G <= LPT, "group size must not exceed lanes per row");
+  static constexpr int SMEM = RING_BYTES + MERGE_BYTES + ML_BYTES + BAR_BYTES + 1024;
+  static_assert(G <= 8, "the g heads of a KV head fill rows 0..7 of the MMA tile");
   static_assert(NST <= 32, "ring deeper than one block-table chunk");
+  static_assert(STAGE_BYTES % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
 };
+
+// Shared address of the 16-byte chunk `chunk` (8 elements, 0 .. D/8-1) of
+// token row `row` in a page stored as 128-byte-swizzled halves.
+__device__ __forceinline__ uint32_t page_chunk(uint32_t page, int row, int chunk) {
+  return page + (chunk >> 3) * (kPage * 128) + row * 128 + (((chunk & 7) ^ (row & 7)) << 4);
+}
 
 template <int D, int G, int NW, int NST>
 __global__ void __launch_bounds__(NW * 32, 1)
@@ -92,13 +103,32 @@ __global__ void __launch_bounds__(NW * 32, 1)
                         int num_splits, float qscale, float* __restrict__ o_part,
                         float* __restrict__ m_part, float* __restrict__ l_part) {
   using C = DecodeCfg<D, G, NW, NST>;
-  constexpr int LPT = C::LPT, TPS = C::TPS, RS = C::RS;
-  constexpr int REP = LPT / G;  // lanes holding the same head's score in a row
+  constexpr int KS = D / 16;  // k-steps of S = q K^T
+  constexpr int ND = D / 8;   // n-tiles of O~ += P V
 
   const int split = blockIdx.x;
   const int kvh = blockIdx.y;
   const int b = blockIdx.z;
-  const int h_kv = gridDim.y;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int gid = lane >> 2;  // MMA row (query head) / key / dim held by this lane
+  const int tq = lane & 3;    // column pair within the fragment
+
+  // q fragments first: they do not depend on the row length. A-operand
+  // layout of m16n8k16: a0 = (row gid, k 2tq..2tq+1), a2 = (row gid, k+8).
+  uint32_t qa0[KS], qa2[KS];
+  {
+    const __nv_bfloat16* qr = q + (size_t(b) * h + kvh * G + min(gid, G - 1)) * D + 2 * tq;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      const uint32_t x0 = __ldg(reinterpret_cast<const uint32_t*>(qr + 16 * ks));
+      const uint32_t x2 = __ldg(reinterpret_cast<const uint32_t*>(qr + 16 * ks + 8));
+      qa0[ks] = gid < G ? x0 : 0u;
+      qa2[ks] = gid < G ? x2 : 0u;
+    }
+  }
+
   const int seq_len = clamp_seq_len(seq_lens[b], max_blocks * kPage, &g_decode_err);
   int pps = 0;
   const int n_act = split_plan(seq_len, kPage, num_splits, &pps);
@@ -107,16 +137,10 @@ __global__ void __launch_bounds__(NW * 32, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint8_t* ring = smem;
-  float* merge_acc = reinterpret_cast<float*>(smem + C::RING_BYTES);         // [NW][G][D]
-  float* p_s = merge_acc + NW * G * D;                                       // [NW][16][G]
-  float* a_s = p_s + NW * kPage * G;                                         // [NW][G]
-  float* ml_s = a_s + NW * G;                                                // [NW][G][2]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(ml_s + NW * G * 2);           // [NW][NST]
+  float* merge_acc = reinterpret_cast<float*>(smem + C::RING_BYTES);  // [NW][G][D]
+  float* ml_s = merge_acc + NW * G * D;                                // [NW][G][2]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ml_s + NW * G * 2);    // [NW][NST]
 
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5;
-  const int lane = tid & 31;
   if (tid == 0) {
     prefetch_tmap(&tmap_k);
     prefetch_tmap(&tmap_v);
@@ -132,34 +156,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
   const int nloc = span > warp ? (span - warp + NW - 1) / NW : 0;
   const int32_t* bt_row = block_table + size_t(b) * max_blocks;
 
-  const int c = lane % LPT;   // d_h chunk of 8 elements
-  const int tg = lane / LPT;  // token row within a step
-  const int my_head = (lane % LPT) / REP;
-  const bool rep = (lane % REP) == 0;
-
-  // q for the g heads of this KV head, pre-scaled into the base-2 domain.
-  float qf[G][8];
-#pragma unroll
-  for (int hh = 0; hh < G; ++hh) {
-    const uint4 raw = __ldg(reinterpret_cast<const uint4*>(
-        q + (size_t(b) * h + kvh * G + hh) * D + c * 8));
-    const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      qf[hh][2 * e] = bf16lo(w4[e]) * qscale;
-      qf[hh][2 * e + 1] = bf16hi(w4[e]) * qscale;
-    }
-  }
-
-  float acc[G][8];
-#pragma unroll
-  for (int hh = 0; hh < G; ++hh)
-#pragma unroll
-    for (int e = 0; e < 8; ++e) acc[hh][e] = 0.f;
-  float m_run = -INFINITY;  // base-2 running max for head my_head
-  float l_run = 0.f;
-
-  const uint32_t ring_base = smem_u32(ring) + warp * NST * C::STAGE_BYTES;
+  const uint32_t ring_base = smem_u32(smem) + warp * NST * C::STAGE_BYTES;
   const uint32_t bar_base = smem_u32(&bars[warp * NST]);
   const uint64_t policy = policy_evict_first();
 
@@ -174,8 +171,12 @@ __global__ void __launch_bounds__(NW * 32, 1)
     if (phys < 0 || phys >= num_blocks) atomicOr(&g_decode_err, ATTN_DEVERR_BAD_PAGE);
     // An out-of-range page coordinate is filled with zeros by the copy engine.
     mbar_arrive_expect_tx(bar, C::STAGE_BYTES);
-    tma_load_4d_hint(dst, &tmap_k, bar, 0, kvh, 0, phys, policy);
-    tma_load_4d_hint(dst + C::PAGE_BYTES, &tmap_v, bar, 0, kvh, 0, phys, policy);
+#pragma unroll
+    for (int hf = 0; hf < C::HALVES; ++hf) {
+      tma_load_4d_hint(dst + hf * C::HALF_BYTES, &tmap_k, bar, hf * 64, kvh, 0, phys, policy);
+      tma_load_4d_hint(dst + C::PAGE_BYTES + hf * C::HALF_BYTES, &tmap_v, bar, hf * 64, kvh, 0,
+                       phys, policy);
+    }
   };
 
   const int npro = min(NST, nloc);
@@ -185,8 +186,23 @@ __global__ void __launch_bounds__(NW * 32, 1)
     if (lane == 0) issue(i, phys);
   }
 
-  float* p_w = p_s + warp * kPage * G;
-  float* a_w = a_s + warp * G;
+  // O~ for head gid (rows 8..15 of the tile stay zero): o[nd][0..1] are dims
+  // 8nd + 2tq, +1.
+  float o[ND][4];
+#pragma unroll
+  for (int nd = 0; nd < ND; ++nd)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) o[nd][e] = 0.f;
+  float m_run = -INFINITY;  // base-2 running max of head gid (same on the 4 lanes of a quad)
+  float l_lane = 0.f;       // this lane's share of the head's normaliser
+
+  // ldmatrix row addresses (lane -> matrix lane/8, row lane%8).
+  const int lm = lane >> 3, lr = lane & 7;
+  const int k_row = 8 * (lm >> 1) + lr;  // S: matrices (keys 0-7 | 8-15) x (chunk | chunk+1)
+  const int k_dc = lm & 1;
+  const int v_row = 8 * (lm & 1) + lr;   // P V: matrices (keys 0-7 | 8-15) x (chunk | chunk+1)
+  const int v_dc = lm >> 1;
+
   int failed_at = -1;
   for (int i = 0; i < nloc; ++i) {
     const int st = i % NST;
@@ -194,92 +210,64 @@ __global__ void __launch_bounds__(NW * 32, 1)
       failed_at = i;  // error word already set; results of this CTA are void
       break;
     }
-    const uint8_t* kp = ring + (warp * NST + st) * C::STAGE_BYTES;
-    const uint8_t* vp = kp + C::PAGE_BYTES;
+    const uint32_t kp = ring_base + st * C::STAGE_BYTES;
+    const uint32_t vp = kp + C::PAGE_BYTES;
     const int page = p_begin + warp + NW * i;
     const int valid = min(kPage, seq_len - page * kPage);
 
-    // ---- scores for this page: s[r] = head my_head, token r*TPS + tg ----
-    float s[RS];
+    // ---- S = q K^T: two 8-key n-tiles, KS k-steps ----
+    float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-    for (int r = 0; r < RS; ++r) {
-      const int t = r * TPS + tg;
-      const uint4 raw = *reinterpret_cast<const uint4*>(kp + t * D * 2 + c * 16);
-      const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
-      float kf[8];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        kf[2 * e] = bf16lo(w4[e]);
-        kf[2 * e + 1] = bf16hi(w4[e]);
-      }
-      float part[G];
-#pragma unroll
-      for (int hh = 0; hh < G; ++hh) {
-        float a0 = qf[hh][0] * kf[0];
-        float a1 = qf[hh][1] * kf[1];
-#pragma unroll
-        for (int e = 2; e < 8; e += 2) {
-          a0 = fmaf(qf[hh][e], kf[e], a0);
-          a1 = fmaf(qf[hh][e + 1], kf[e + 1], a1);
-        }
-        part[hh] = a0 + a1;
-      }
-      ReduceScatter<G, LPT / 2>::run(part, lane);
-      s[r] = (t < valid) ? part[0] : -INFINITY;
+    for (int ks = 0; ks < KS; ++ks) {
+      uint32_t b00, b01, b10, b11;
+      ldsm_x4(page_chunk(kp, k_row, 2 * ks + k_dc), b00, b01, b10, b11);
+      mma_bf16(sc[0], qa0[ks], qa2[ks], b00, b01);
+      mma_bf16(sc[1], qa0[ks], qa2[ks], b10, b11);
+    }
+    // This lane holds head gid's scores of keys 2tq, 2tq+1 (tile 0) and
+    // 8+2tq, 9+2tq (tile 1).
+    float s[4] = {sc[0][0] * qscale, sc[0][1] * qscale, sc[1][0] * qscale, sc[1][1] * qscale};
+    if (valid < kPage) {
+      if (2 * tq >= valid) s[0] = -INFINITY;
+      if (2 * tq + 1 >= valid) s[1] = -INFINITY;
+      if (8 + 2 * tq >= valid) s[2] = -INFINITY;
+      if (9 + 2 * tq >= valid) s[3] = -INFINITY;
     }
 
     // ---- online update (one rescale per page) ----
-    float mx = s[0];
-#pragma unroll
-    for (int r = 1; r < RS; ++r) mx = fmaxf(mx, s[r]);
-#pragma unroll
-    for (int m = LPT; m < 32; m <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
+    float mx = fmaxf(fmaxf(s[0], s[1]), fmaxf(s[2], s[3]));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
     const float m_new = fmaxf(m_run, mx);  // finite: every page has a valid key
     const float alpha = ex2_approx(m_run - m_new);  // 0 while m_run = -inf
-    float psum = 0.f;
-    float p[RS];
-#pragma unroll
-    for (int r = 0; r < RS; ++r) {
-      p[r] = ex2_approx(s[r] - m_new);
-      psum += p[r];
-    }
-#pragma unroll
-    for (int m = LPT; m < 32; m <<= 1) psum += __shfl_xor_sync(0xffffffffu, psum, m);
-    l_run = fmaf(l_run, alpha, psum);
     m_run = m_new;
-
-    if (rep) {
+    float p[4];
 #pragma unroll
-      for (int r = 0; r < RS; ++r) p_w[(r * TPS + tg) * G + my_head] = p[r];
-      if (tg == 0) a_w[my_head] = alpha;
+    for (int e = 0; e < 4; ++e) p[e] = ex2_approx(s[e] - m_new);
+    l_lane = fmaf(l_lane, alpha, (p[0] + p[1]) + (p[2] + p[3]));
+#pragma unroll
+    for (int nd = 0; nd < ND; ++nd) {
+      o[nd][0] *= alpha;
+      o[nd][1] *= alpha;
     }
-    __syncwarp();
+    // P as the A operand (keys 2tq.. in a0, keys 8+2tq.. in a2), two bf16 terms.
+    uint32_t ph0, ph2, pl0, pl2;
+    asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(ph0) : "r"(__float_as_uint(p[0])), "r"(__float_as_uint(p[1])));
+    asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(ph2) : "r"(__float_as_uint(p[2])), "r"(__float_as_uint(p[3])));
+    pl0 = pack_bf16x2(p[0] - __uint_as_float(__float_as_uint(p[0]) & 0xffff0000u),
+                      p[1] - __uint_as_float(__float_as_uint(p[1]) & 0xffff0000u));
+    pl2 = pack_bf16x2(p[2] - __uint_as_float(__float_as_uint(p[2]) & 0xffff0000u),
+                      p[3] - __uint_as_float(__float_as_uint(p[3]) & 0xffff0000u));
 
-    // ---- rescale and accumulate P V ----
+    // ---- O~ += P V: ND n-tiles of 8 dims, two at a time ----
 #pragma unroll
-    for (int hh = 0; hh < G; ++hh) {
-      const float a = a_w[hh];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) acc[hh][e] *= a;
-    }
-#pragma unroll
-    for (int r = 0; r < RS; ++r) {
-      const int t = r * TPS + tg;
-      const uint4 raw = *reinterpret_cast<const uint4*>(vp + t * D * 2 + c * 16);
-      const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
-      float vf[8];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        vf[2 * e] = bf16lo(w4[e]);
-        vf[2 * e + 1] = bf16hi(w4[e]);
-      }
-      float pv[G];
-#pragma unroll
-      for (int hh = 0; hh < G; ++hh) pv[hh] = p_w[t * G + hh];
-#pragma unroll
-      for (int hh = 0; hh < G; ++hh)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[hh][e] = fmaf(pv[hh], vf[e], acc[hh][e]);
+    for (int nd = 0; nd < ND; nd += 2) {
+      uint32_t b00, b01, b10, b11;
+      ldsm_x4_t(page_chunk(vp, v_row, nd + v_dc), b00, b01, b10, b11);
+      mma_bf16(o[nd], ph0, ph2, b00, b01);
+      mma_bf16(o[nd], pl0, pl2, b00, b01);
+      mma_bf16(o[nd + 1], ph0, ph2, b10, b11);
+      mma_bf16(o[nd + 1], pl0, pl2, b10, b11);
     }
     __syncwarp();
 
@@ -303,24 +291,17 @@ __global__ void __launch_bounds__(NW * 32, 1)
       (void)mbar_wait(bar_base + (j % NST) * 8, (j / NST) & 1, &g_decode_err);
   }
 
-  // ---- fold the token rows of the warp, then merge warps ----
+  // ---- head gid's normaliser over its quad, then merge the warps ----
+  l_lane += __shfl_xor_sync(0xffffffffu, l_lane, 1);
+  l_lane += __shfl_xor_sync(0xffffffffu, l_lane, 2);
+  if (gid < G) {
 #pragma unroll
-  for (int m = LPT; m < 32; m <<= 1)
-#pragma unroll
-    for (int hh = 0; hh < G; ++hh)
-#pragma unroll
-      for (int e = 0; e < 8; ++e) acc[hh][e] += __shfl_xor_sync(0xffffffffu, acc[hh][e], m);
-
-  if (tg == 0) {
-#pragma unroll
-    for (int hh = 0; hh < G; ++hh) {
-      float4* dst = reinterpret_cast<float4*>(merge_acc + (warp * G + hh) * D + c * 8);
-      dst[0] = make_float4(acc[hh][0], acc[hh][1], acc[hh][2], acc[hh][3]);
-      dst[1] = make_float4(acc[hh][4], acc[hh][5], acc[hh][6], acc[hh][7]);
-    }
-    if (rep) {
-      ml_s[(warp * G + my_head) * 2 + 0] = m_run;
-      ml_s[(warp * G + my_head) * 2 + 1] = l_run;
+    for (int nd = 0; nd < ND; ++nd)
+      *reinterpret_cast<float2*>(merge_acc + (warp * G + gid) * D + 8 * nd + 2 * tq) =
+          make_float2(o[nd][0], o[nd][1]);
+    if (tq == 0) {
+      ml_s[(warp * G + gid) * 2 + 0] = nloc > 0 ? m_run : -INFINITY;
+      ml_s[(warp * G + gid) * 2 + 1] = nloc > 0 ? l_lane : 0.f;
     }
   }
   __syncthreads();
@@ -347,7 +328,6 @@ __global__ void __launch_bounds__(NW * 32, 1)
       l_part[prow] = L;
     }
   }
-  (void)h_kv;
 }
 
 template <int D, int G, int NW, int NST>
@@ -373,7 +353,7 @@ cudaError_t launch_d(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorM
     case 1: return launch_cfg<D, 1, 8, 3>(a, tk, tv, stream);
     case 2: return launch_cfg<D, 2, 8, 3>(a, tk, tv, stream);
     case 4: return launch_cfg<D, 4, 8, 3>(a, tk, tv, stream);
-    case 8: return launch_cfg<D, 8, 8, 2>(a, tk, tv, stream);
+    case 8: return launch_cfg<D, 8, 8, 3>(a, tk, tv, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -386,12 +366,13 @@ cudaError_t launch_decode_split(const DecodeArgs& a, cudaStream_t stream) {
                             uint64_t(a.num_blocks)};
   const uint64_t strides[3] = {uint64_t(a.d_h) * 2, uint64_t(a.h_kv) * a.d_h * 2,
                                uint64_t(a.page_size) * a.h_kv * a.d_h * 2};
-  const uint32_t box[4] = {uint32_t(a.d_h), 1u, uint32_t(a.page_size), 1u};
+  // 64-element (128-byte) boxes: the widest the 128-byte swizzle allows.
+  const uint32_t box[4] = {64u, 1u, uint32_t(a.page_size), 1u};
   if (encode_tensor_map(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(a.k_cache),
-                        dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
+                        dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
   if (encode_tensor_map(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(a.v_cache),
-                        dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
+                        dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
   if (a.d_h == 128) return launch_d<128>(a, tk, tv, stream);
   return launch_d<64>(a, tk, tv, stream);
