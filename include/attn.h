@@ -132,12 +132,13 @@ int attn_decode_split_plan(int seq_len, int page_size, int num_splits, int* page
 /*
  * attn_recommended_splits -- split count for a decode batch on a GPU with
  * num_sms SMs. Follows [DEC] "The grid" (fill the first wave:
- * S* = ceil(N_SM / G_2D) with G_2D = B * h_kv) and, for ragged batches, caps
- * the largest split so that the longest row does not dominate: with the total
- * page count known, splits are also raised until the longest row's split is
- * no larger than a quarter of the mean work per CTA slot. Result in
+ * S* = ceil(N_SM / G_2D) with G_2D = B * h_kv). For a ragged batch (the
+ * longest row more than 1.25x the mean length, known from total_seq_len) the
+ * splits are raised until the longest row's split is no larger than a
+ * quarter of the mean work per CTA slot. Finally each split of the longest
+ * row keeps at least 32 pages (so a CTA's start-up is amortised). Result in
  * [1, ATTN_MAX_SPLITS]. Host-only, pure; -1 on invalid arguments.
- * total_seq_len may be 0 when unknown (then only the first-wave rule applies).
+ * total_seq_len may be 0 when unknown (then the ragged rule is skipped).
  */
 #define ATTN_MAX_SPLITS 1024
 int attn_recommended_splits(int B, int h_kv, int max_seq_len, long long total_seq_len,

@@ -75,16 +75,20 @@ int attn_recommended_splits(int B, int h_kv, int max_seq_len, long long total_se
   const long long g2d = static_cast<long long>(B) * h_kv;
   long long s = (num_sms + g2d - 1) / g2d;  // first-wave coverage
   const long long max_pages = (max_seq_len + 15) / 16;
-  if (total_seq_len > 0) {
-    // Ragged batch: keep the longest row's split below a quarter of the mean
-    // work per SM, so that the tail of the longest rows stays short.
+  // Ragged batch (the longest row well above the mean): keep the longest
+  // row's split below a quarter of the mean work per SM, so that the tail of
+  // the longest rows stays short. Rows of one length need no such rule.
+  if (total_seq_len > 0 && 4ll * max_seq_len * B > 5ll * total_seq_len) {
     const long long total_pages = ((total_seq_len + 15) / 16) * h_kv;
     const long long mean_per_sm = (total_pages + num_sms - 1) / num_sms;
     const long long target = mean_per_sm / 4 > 0 ? mean_per_sm / 4 : 1;
     const long long s_bal = (max_pages + target - 1) / target;
     if (s_bal > s) s = s_bal;
   }
-  if (max_pages > 0 && s > max_pages) s = max_pages;
+  // At least 32 pages (four per warp) per split of the longest row, so that
+  // a CTA's start-up (row length, block table, first page) is amortised.
+  const long long s_work = (max_pages + 31) / 32;
+  if (s > s_work) s = s_work;
   if (s < 1) s = 1;
   if (s > ATTN_MAX_SPLITS) s = ATTN_MAX_SPLITS;
   return static_cast<int>(s);

@@ -7,11 +7,14 @@
 // averaging tile outputs": branch around the all-empty case instead of
 // evaluating -inf - (-inf)).
 //
-// Layout: one warp per output row; lane j owns d_h/32 consecutive output
-// elements, so each split's O~ row is read as one coalesced 128-bit (d_h=128)
-// or 64-bit (d_h=64) access per lane. The split weights are computed 32 at a
-// time, one per lane, and broadcast with shuffles, so the loop over splits
-// carries no dependent global load.
+// Layout: WPR warps per output row (1 for many rows, 8 when there are too
+// few rows to fill the GPU); lane j owns d_h/32 consecutive output elements,
+// so each split's O~ row is read as one coalesced 128-bit (d_h=128) or 64-bit
+// (d_h=64) access per lane. Every warp of a row first takes the overall max M
+// over all active splits; then, per chunk of 32 splits, the weights are
+// computed one per lane and broadcast with shuffles (so the loop carries no
+// dependent global load), the warps of the row take the chunk's splits in
+// turn, and with WPR > 1 they add their sums in shared memory.
 #include "common.cuh"
 #include "internal.h"
 
@@ -19,7 +22,7 @@ namespace attn {
 
 static __device__ unsigned int g_merge_err;
 
-template <int D, bool kOutBf16>
+template <int D, bool kOutBf16, int WPR>
 __global__ void __launch_bounds__(256)
     merge_states_kernel(const float* __restrict__ o_part, const float* __restrict__ m_part,
                         const float* __restrict__ l_part, const int32_t* __restrict__ n_active,
@@ -27,20 +30,28 @@ __global__ void __launch_bounds__(256)
                         int max_len, int rows, int S, void* __restrict__ o_out, float* __restrict__ lse_out) {
   constexpr int VEC = D / 32;
   static_assert(VEC == 2 || VEC == 4, "d_h must be 64 or 128");
+  constexpr int RPC = 8 / WPR;  // rows per CTA of 8 warps
+  __shared__ float red_acc[WPR > 1 ? WPR * D : 1];
+  __shared__ float red_l[WPR];
   const int lane = threadIdx.x & 31;
-  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (row >= rows) return;
+  const int warp = threadIdx.x >> 5;
+  const int wr = warp % WPR;  // this warp's share of the row
+  const int row = blockIdx.x * RPC + warp / WPR;
+  if (WPR == 1 && row >= rows) return;
+  const bool live = row < rows;  // WPR > 1: one row per CTA, always live
 
-  int n;
-  if (n_active != nullptr) {
-    n = n_active[row];
-  } else if (seq_lens != nullptr) {
-    const int len = clamp_seq_len(seq_lens[row / heads_per_seq], max_len, &g_merge_err);
-    n = split_plan(len, page_size, S, nullptr);
-  } else {
-    n = S;
+  int n = 0;
+  if (live) {
+    if (n_active != nullptr) {
+      n = n_active[row];
+    } else if (seq_lens != nullptr) {
+      const int len = clamp_seq_len(seq_lens[row / heads_per_seq], max_len, &g_merge_err);
+      n = split_plan(len, page_size, S, nullptr);
+    } else {
+      n = S;
+    }
+    n = max(0, min(n, S));
   }
-  n = max(0, min(n, S));
 
   const float* mrow = m_part + size_t(row) * S;
   const float* lrow = l_part + size_t(row) * S;
@@ -64,11 +75,11 @@ __global__ void __launch_bounds__(256)
       if (i < n) {
         const float mi = mrow[i];
         w = (mi == -INFINITY) ? 0.f : ex2_approx(fmaf(mi, kLog2e, -Mb));
-        L = fmaf(w, lrow[i], L);
+        if (wr == 0) L = fmaf(w, lrow[i], L);
       }
       const int cnt = min(32, n - c);
-#pragma unroll 4
-      for (int j = 0; j < cnt; ++j) {
+#pragma unroll 8
+      for (int j = wr; j < cnt; j += WPR) {
         const float wj = __shfl_sync(0xffffffffu, w, j);
         const float* src = orow + size_t(c + j) * D;
         if constexpr (VEC == 4) {
@@ -86,6 +97,24 @@ __global__ void __launch_bounds__(256)
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+  }
+
+  if constexpr (WPR > 1) {
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) red_acc[wr * D + lane * VEC + e] = acc[e];
+    if (lane == 0) red_l[wr] = L;
+    __syncthreads();
+    if (wr != 0 || !live) return;
+    L = 0.f;
+#pragma unroll
+    for (int w = 0; w < WPR; ++w) L += red_l[w];
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) {
+      float a = 0.f;
+#pragma unroll
+      for (int w = 0; w < WPR; ++w) a += red_acc[w * D + lane * VEC + e];
+      acc[e] = a;
+    }
   }
 
   const bool empty = !(L > 0.f);  // also catches NaN mass
@@ -120,18 +149,21 @@ cudaError_t launch_merge(const float* o_part, const float* m_part, const float* 
                          int page_size, int max_len, int rows, int num_splits, int d_h, void* o, float* lse,
                          attn_dtype_t out_dtype, cudaStream_t stream) {
   if (rows <= 0) return cudaSuccess;
-  const int warps = 8;
-  const dim3 grid((rows + warps - 1) / warps);
-  const dim3 block(32 * warps);
+  // Few rows and many splits: spread each row's splits over 8 warps.
+  const bool wide = rows < 512 && num_splits > 4;
+  const dim3 grid(wide ? rows : (rows + 7) / 8);
+  const dim3 block(256);
   const bool bf = out_dtype == ATTN_DTYPE_BF16;
-#define ATTN_MERGE_LAUNCH(D, BF)                                                            \
-  merge_states_kernel<D, BF><<<grid, block, 0, stream>>>(o_part, m_part, l_part, n_active, \
-                                                         seq_lens, heads_per_seq, page_size, \
-                                                         max_len, rows, num_splits, o, lse)
+#define ATTN_MERGE_LAUNCH(D, BF, W)                                                              \
+  merge_states_kernel<D, BF, W><<<grid, block, 0, stream>>>(o_part, m_part, l_part, n_active,   \
+                                                            seq_lens, heads_per_seq, page_size, \
+                                                            max_len, rows, num_splits, o, lse)
   if (d_h == 128) {
-    if (bf) ATTN_MERGE_LAUNCH(128, true); else ATTN_MERGE_LAUNCH(128, false);
+    if (bf) { if (wide) ATTN_MERGE_LAUNCH(128, true, 8); else ATTN_MERGE_LAUNCH(128, true, 1); }
+    else { if (wide) ATTN_MERGE_LAUNCH(128, false, 8); else ATTN_MERGE_LAUNCH(128, false, 1); }
   } else {
-    if (bf) ATTN_MERGE_LAUNCH(64, true); else ATTN_MERGE_LAUNCH(64, false);
+    if (bf) { if (wide) ATTN_MERGE_LAUNCH(64, true, 8); else ATTN_MERGE_LAUNCH(64, true, 1); }
+    else { if (wide) ATTN_MERGE_LAUNCH(64, false, 8); else ATTN_MERGE_LAUNCH(64, false, 1); }
   }
 #undef ATTN_MERGE_LAUNCH
   return cudaGetLastError();

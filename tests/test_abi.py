@@ -161,3 +161,14 @@ def test_prefill_workspace_bytes(lib):
     assert lib.attn_prefill_workspace_bytes(64, 0, 128, 1) == none
     assert lib.attn_prefill_workspace_bytes(64, 8, 96, 1) == none
     assert lib.attn_prefill_workspace_bytes(64, 8, 128, 7) == none
+
+
+def test_recommended_splits_uniform_rows_and_minimum_work():
+    """Rows of one length take the first-wave count; no split of the longest
+    row gets fewer than 32 pages; the ragged rule needs a row well above the mean."""
+    assert attn.attn_recommended_splits(1, 8, 32768, 32768, 152) == 19   # ceil(152 / 8)
+    assert attn.attn_recommended_splits(1, 1, 32768, 32768, 152) == 64   # 2048 pages / 32
+    assert attn.attn_recommended_splits(1, 8, 256, 256, 152) == 1        # 16 pages: one split
+    assert attn.attn_recommended_splits(4, 8, 8192, 4 * 8192, 152) == 5  # uniform batch: ceil(152 / 32)
+    # ragged: one long row among short ones raises the count above the first wave
+    assert attn.attn_recommended_splits(8, 8, 16384, 16384 + 7 * 512, 152) > 3
