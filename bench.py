@@ -398,6 +398,9 @@ def run_gpu(args, world, rank, local):
                            "d2h_bytes_per_step": hdo.numel() * hdo.element_size() + hdl.numel() * hdl.element_size(),
                            "ms": avg}
 
+    # ---- pairwise (O, LSE) merge (prefix / suffix combine), outside the step ----
+    merge_pair = measure_merge_pair(dev, flush, hbm_peak, peak_kind) if args.only is None else None
+
     # ---- CPU oracle baseline (rank 0, N = 1 only) ----
     cpu = None
     dec_cpu = None
@@ -461,6 +464,7 @@ def run_gpu(args, world, rank, local):
             "e2e": dec_e2e,
             "cpu_baseline": dec_cpu,
         },
+        "merge_pair": merge_pair,
         "prefill_ms": pre_avg,
         "e2e": e2e,
         "cpu_baseline": cpu,
@@ -469,6 +473,41 @@ def run_gpu(args, world, rank, local):
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)
+
+
+def measure_merge_pair(dev, flush, hbm_peak, peak_kind, iters=20):
+    """Pairwise (O, LSE) merge of two prefill-shaped results (32 heads x 8192
+    tokens, d_h 128, bf16 in and out): the prefix / suffix combine. HBM-bound;
+    204 MB per call, L2 flushed before each call."""
+    import online_softmax_attn_gb300 as attn
+
+    rows, d = PREFILL.h * PREFILL.T, PREFILL.d_h
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    oa = torch.randn(rows, d, generator=g, device=dev).to(torch.bfloat16)
+    ob = torch.randn(rows, d, generator=g, device=dev).to(torch.bfloat16)
+    la = torch.randn(rows, generator=g, device=dev) * 20
+    lb = torch.randn(rows, generator=g, device=dev) * 20
+    o = torch.empty_like(oa)
+    lse = torch.empty_like(la)
+    for _ in range(3):
+        attn.attn_merge_lse_pair(oa, la, ob, lb, o=o, lse=lse)
+    ms = []
+    for _ in range(iters):
+        flush.fill_(1)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        attn.attn_merge_lse_pair(oa, la, ob, lb, o=o, lse=lse)
+        b.record()
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    t = statistics.median(ms)
+    nbytes = rows * (2 * d * 2 + 2 * 4 + d * 2 + 4)
+    gbs = nbytes / (t * 1e-3) / 1e9
+    return {"value": gbs, "unit": "GB/s", "ms": t, "rows": rows, "d_h": d, "bytes": nbytes,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": gbs / hbm_peak, "traffic": None, "kernel": "merge_pair_kernel",
+                         "peak_source": f"{peak_kind} copy bandwidth"}}
 
 
 def main():

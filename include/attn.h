@@ -247,6 +247,33 @@ attn_status_t attn_merge_states(const float* o_part, const float* m_part, const 
                                 void* o, float* lse, attn_dtype_t out_dtype, void* stream);
 
 /*
+ * attn_merge_lse_pair -- merge two normalised attention results over
+ * disjoint key sets, row by row. Follows [NA] "The state that gets passed
+ * around is the log-sum-exp" (the symmetric merge: M = max(lse_a, lse_b),
+ * e_x = exp(lse_x - M), o = (e_a o_a + e_b o_b) / (e_a + e_b), lse =
+ * M + ln(e_a + e_b); the weights are formed first, so o is a convex
+ * combination of o_a and o_b) and its prefix / suffix use ([NA] cascade
+ * trace). An empty side has lse = -inf and weight 0; when both are empty the
+ * row takes a branch and yields o = 0, lse = -inf ([NA] "The base case is a
+ * NaN factory"). NaN inputs propagate; +inf is not reinterpreted.
+ *
+ *   o_a, o_b     [rows, d_h]  in_dtype (bf16 or fp32), normalised outputs (read)
+ *   lse_a, lse_b [rows]       fp32, natural log (read)
+ *   o            [rows, d_h]  out_dtype (bf16 or fp32) (written); may be
+ *                o_a or o_b itself when the dtypes match (each element is read
+ *                before it is written, by the same thread)
+ *   lse          [rows]       fp32, may be NULL (written); must not overlap
+ *                lse_a or lse_b
+ * d_h must be 64 or 128. rows == 0 is a no-op. Errors: INVALID_ARG for NULL
+ * inputs (rows > 0), rows < 0, unknown dtypes, pointers not 16-byte (o_a,
+ * o_b, o) or 4-byte (lse) aligned, lse overlapping lse_a or lse_b;
+ * UNSUPPORTED for other d_h.
+ */
+attn_status_t attn_merge_lse_pair(const void* o_a, const float* lse_a, const void* o_b,
+                                  const float* lse_b, int rows, int d_h, attn_dtype_t in_dtype,
+                                  void* o, float* lse, attn_dtype_t out_dtype, void* stream);
+
+/*
  * attn_get_device_error -- synchronise `stream`, then read and clear the
  * device error word of every kernel module (ATTN_DEVERR_* bits, 0 = none)
  * into *bits. Returns ATTN_ERR_CUDA if the synchronisation fails.

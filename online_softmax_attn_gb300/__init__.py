@@ -73,6 +73,8 @@ def library() -> ctypes.CDLL:
     lib.attn_decode_paged.restype = I
     lib.attn_merge_states.argtypes = [P, P, P, P, I, I, I, P, P, I, P]
     lib.attn_merge_states.restype = I
+    lib.attn_merge_lse_pair.argtypes = [P, P, P, P, I, I, I, P, P, I, P]
+    lib.attn_merge_lse_pair.restype = I
     lib.attn_get_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint)]
     lib.attn_get_device_error.restype = I
     _lib = lib
@@ -228,6 +230,31 @@ def attn_merge_states(o_part, m_part, l_part, n_active=None, out_dtype=torch.bfl
     st = library().attn_merge_states(_ptr(o_part), _ptr(m_part), _ptr(l_part), _ptr(n_active),
                                      rows, S, d, _ptr(o), _ptr(lse), dt, _stream(stream))
     _check("attn_merge_states", st)
+    return o, lse
+
+
+def attn_merge_lse_pair(o_a, lse_a, o_b, lse_b, out_dtype=torch.bfloat16, o=None, lse=None,
+                        return_lse: bool = True, stream=None):
+    """Merge two normalised results over disjoint key sets: o_a, o_b [rows, d]
+    (bf16 or fp32, same dtype), lse_a, lse_b [rows] fp32. Returns (o [rows, d]
+    in out_dtype, lse [rows] fp32 or None). Leading dims are flattened."""
+    _need(o_a.shape == o_b.shape and o_a.dtype == o_b.dtype, "o_a and o_b must match")
+    _need(o_a.dtype in (torch.bfloat16, torch.float32), "o_a/o_b must be bf16 or fp32")
+    for t in (o_a, lse_a, o_b, lse_b):
+        _need(t.is_cuda and t.is_contiguous(), "tensors must be contiguous CUDA tensors")
+    _need(lse_a.dtype == lse_b.dtype == torch.float32, "lse must be fp32")
+    d = o_a.shape[-1]
+    rows = o_a.numel() // d
+    _need(lse_a.numel() == rows and lse_b.numel() == rows, "lse must hold one value per row")
+    if o is None:
+        o = torch.empty(o_a.shape, dtype=out_dtype, device=o_a.device)
+    if lse is None and return_lse:
+        lse = torch.empty(lse_a.shape, dtype=torch.float32, device=o_a.device)
+    dt_in = ATTN_DTYPE_BF16 if o_a.dtype == torch.bfloat16 else ATTN_DTYPE_F32
+    dt_out = ATTN_DTYPE_BF16 if o.dtype == torch.bfloat16 else ATTN_DTYPE_F32
+    st = library().attn_merge_lse_pair(_ptr(o_a), _ptr(lse_a), _ptr(o_b), _ptr(lse_b), rows, d,
+                                       dt_in, _ptr(o), _ptr(lse), dt_out, _stream(stream))
+    _check("attn_merge_lse_pair", st)
     return o, lse
 
 

@@ -205,6 +205,32 @@ attn_status_t attn_merge_states(const float* o_part, const float* m_part, const 
                                 static_cast<cudaStream_t>(stream)));
 }
 
+attn_status_t attn_merge_lse_pair(const void* o_a, const float* lse_a, const void* o_b,
+                                  const float* lse_b, int rows, int d_h, attn_dtype_t in_dtype,
+                                  void* o, float* lse, attn_dtype_t out_dtype, void* stream) {
+  if (rows < 0) return ATTN_ERR_INVALID_ARG;
+  if ((in_dtype != ATTN_DTYPE_F32 && in_dtype != ATTN_DTYPE_BF16) ||
+      (out_dtype != ATTN_DTYPE_F32 && out_dtype != ATTN_DTYPE_BF16))
+    return ATTN_ERR_INVALID_ARG;
+  if (d_h != 64 && d_h != 128) return ATTN_ERR_UNSUPPORTED;
+  if (rows == 0) return ATTN_OK;
+  if (!o_a || !lse_a || !o_b || !lse_b || !o) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(o_a, 16) || !aligned(o_b, 16) || !aligned(o, 16) || !aligned(lse_a, 4) ||
+      !aligned(lse_b, 4) || !aligned(lse, 4))
+    return ATTN_ERR_INVALID_ARG;
+  if (lse != nullptr) {
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(lse);
+    const uintptr_t hi = lo + static_cast<uintptr_t>(rows) * sizeof(float);
+    for (const float* in : {lse_a, lse_b}) {
+      const uintptr_t a = reinterpret_cast<uintptr_t>(in);
+      const uintptr_t b = a + static_cast<uintptr_t>(rows) * sizeof(float);
+      if (lo < b && a < hi) return ATTN_ERR_INVALID_ARG;
+    }
+  }
+  return from_cuda(launch_merge_pair(o_a, lse_a, o_b, lse_b, rows, d_h, in_dtype, o, lse,
+                                     out_dtype, static_cast<cudaStream_t>(stream)));
+}
+
 attn_status_t attn_get_device_error(void* stream, unsigned int* bits) {
   if (bits == nullptr) return ATTN_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

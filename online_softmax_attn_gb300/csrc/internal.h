@@ -36,6 +36,10 @@ cudaError_t launch_merge(const float* o_part, const float* m_part, const float* 
                          int page_size, int max_len, int rows, int num_splits, int d_h, void* o, float* lse,
                          attn_dtype_t out_dtype, cudaStream_t stream);
 unsigned int merge_read_and_clear_error(cudaStream_t stream, cudaError_t* st);
+// Pairwise (O, LSE) merge; arguments validated by the caller.
+cudaError_t launch_merge_pair(const void* o_a, const float* lse_a, const void* o_b,
+                              const float* lse_b, int rows, int d_h, attn_dtype_t in_dtype,
+                              void* o, float* lse, attn_dtype_t out_dtype, cudaStream_t stream);
 
 // decode.cu ----------------------------------------------------------------
 struct DecodeArgs {

@@ -169,6 +169,101 @@ cudaError_t launch_merge(const float* o_part, const float* m_part, const float* 
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// Pairwise (O, LSE) merge ("The state that gets passed around is the
+// log-sum-exp"): each thread owns 8 consecutive elements of one row (16-byte
+// bf16 or 32-byte fp32 accesses) and forms the row's two weights itself --
+// recomputing two exponentials per thread is cheaper than sharing them.
+// ---------------------------------------------------------------------------
+template <bool kBf16>
+__device__ __forceinline__ void load8(const void* base, size_t off, float (&v)[8]) {
+  if constexpr (kBf16) {
+    const uint4 x = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(base) + off));
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      v[2 * e] = bf16lo(w[e]);
+      v[2 * e + 1] = bf16hi(w[e]);
+    }
+  } else {
+    const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(base) + off);
+    const float4 a = __ldg(src), b = __ldg(src + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  }
+}
+
+template <int D, bool kInBf16, bool kOutBf16>
+__global__ void __launch_bounds__(256)
+    merge_pair_kernel(const void* __restrict__ o_a, const float* __restrict__ lse_a,
+                      const void* __restrict__ o_b, const float* __restrict__ lse_b, int rows,
+                      void* o, float* __restrict__ lse) {
+  constexpr int TPR = D / 8;  // threads per row
+  const long long total = static_cast<long long>(rows) * TPR;
+  for (long long it = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; it < total;
+       it += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int row = static_cast<int>(it / TPR);
+    const int part = static_cast<int>(it % TPR);
+    const size_t off = static_cast<size_t>(row) * D + part * 8;
+    const float la = lse_a[row], lb = lse_b[row];
+    float va[8], vb[8], r[8];
+    load8<kInBf16>(o_a, off, va);
+    load8<kInBf16>(o_b, off, vb);
+    const float M = fmaxf(la, lb);
+    float L;
+    if (M == -INFINITY) {  // both sides empty: no -inf - -inf
+#pragma unroll
+      for (int e = 0; e < 8; ++e) r[e] = 0.f;
+      L = -INFINITY;
+    } else {
+      const float ea = (la == -INFINITY) ? 0.f : expf(la - M);
+      const float eb = (lb == -INFINITY) ? 0.f : expf(lb - M);
+      const float sum = ea + eb;
+      const float wa = ea / sum, wb = eb / sum;  // weights first: a convex combination
+#pragma unroll
+      for (int e = 0; e < 8; ++e) r[e] = fmaf(wa, va[e], wb * vb[e]);
+      L = M + logf(sum);
+    }
+    if constexpr (kOutBf16) {
+      uint4 y;
+      y.x = pack_bf16x2(r[0], r[1]);
+      y.y = pack_bf16x2(r[2], r[3]);
+      y.z = pack_bf16x2(r[4], r[5]);
+      y.w = pack_bf16x2(r[6], r[7]);
+      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(o) + off) = y;
+    } else {
+      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(o) + off);
+      dst[0] = make_float4(r[0], r[1], r[2], r[3]);
+      dst[1] = make_float4(r[4], r[5], r[6], r[7]);
+    }
+    if (lse != nullptr && part == 0) lse[row] = L;
+  }
+}
+
+cudaError_t launch_merge_pair(const void* o_a, const float* lse_a, const void* o_b,
+                              const float* lse_b, int rows, int d_h, attn_dtype_t in_dtype,
+                              void* o, float* lse, attn_dtype_t out_dtype, cudaStream_t stream) {
+  if (rows <= 0) return cudaSuccess;
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    (void)cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long items = static_cast<long long>(rows) * (d_h / 8);
+  const long long blocks = (items + 255) / 256;
+  const int grid = static_cast<int>(blocks < 8ll * sms ? blocks : 8ll * sms);
+  const bool ib = in_dtype == ATTN_DTYPE_BF16, ob = out_dtype == ATTN_DTYPE_BF16;
+#define ATTN_PAIR(D, IB, OB) \
+  merge_pair_kernel<D, IB, OB><<<grid, 256, 0, stream>>>(o_a, lse_a, o_b, lse_b, rows, o, lse)
+  if (d_h == 128) {
+    if (ib) { if (ob) ATTN_PAIR(128, true, true); else ATTN_PAIR(128, true, false); }
+    else { if (ob) ATTN_PAIR(128, false, true); else ATTN_PAIR(128, false, false); }
+  } else {
+    if (ib) { if (ob) ATTN_PAIR(64, true, true); else ATTN_PAIR(64, true, false); }
+    else { if (ob) ATTN_PAIR(64, false, true); else ATTN_PAIR(64, false, false); }
+  }
+#undef ATTN_PAIR
+  return cudaGetLastError();
+}
+
 unsigned int merge_read_and_clear_error(cudaStream_t stream, cudaError_t* st) {
   unsigned int v = 0, zero = 0;
   cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_merge_err, sizeof(v), 0,

@@ -172,3 +172,26 @@ def test_recommended_splits_uniform_rows_and_minimum_work():
     assert attn.attn_recommended_splits(4, 8, 8192, 4 * 8192, 152) == 5  # uniform batch: ceil(152 / 32)
     # ragged: one long row among short ones raises the count above the first wave
     assert attn.attn_recommended_splits(8, 8, 16384, 16384 + 7 * 512, 152) > 3
+
+
+def test_merge_lse_pair_arguments(lib):
+    P = ctypes.c_void_p
+    dummy = P(256)
+    bad = attn.ATTN_ERR_INVALID_ARG
+    lib.attn_merge_lse_pair.argtypes = [P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P,
+                                        ctypes.c_int, P]
+    ok_args = [dummy, P(4096), P(512), P(8192), 4, 128, 1, P(1024), P(12288), 1, None]
+    # rows == 0 is a no-op even with NULL pointers
+    assert lib.attn_merge_lse_pair(None, None, None, None, 0, 128, 1, None, None, 1, None) == 0
+    a = list(ok_args); a[4] = -1
+    assert lib.attn_merge_lse_pair(*a) == bad
+    a = list(ok_args); a[5] = 96
+    assert lib.attn_merge_lse_pair(*a) == attn.ATTN_ERR_UNSUPPORTED
+    a = list(ok_args); a[6] = 7
+    assert lib.attn_merge_lse_pair(*a) == bad
+    a = list(ok_args); a[0] = P(264)  # o_a not 16-byte aligned
+    assert lib.attn_merge_lse_pair(*a) == bad
+    a = list(ok_args); a[2] = None
+    assert lib.attn_merge_lse_pair(*a) == bad
+    a = list(ok_args); a[8] = P(4100)  # output LSE overlaps lse_a
+    assert lib.attn_merge_lse_pair(*a) == bad
