@@ -398,6 +398,29 @@ def run_gpu(args, world, rank, local):
                            "d2h_bytes_per_step": hdo.numel() * hdo.element_size() + hdl.numel() * hdl.element_size(),
                            "ms": avg}
 
+    # ---- deterministic decode (fixed 2048-key splits) on the same batch, outside the step ----
+    det = None
+    if args.only is None:
+        pps = 128
+        det_splits = -(-table.shape[1] // pps)
+        det_ws = torch.empty(attn.attn_decode_workspace_bytes(B, DECODE.h, DECODE.d_h, det_splits),
+                             dtype=torch.uint8, device=dev)
+        for _ in range(3):
+            attn.attn_decode_paged_deterministic(dq, kc, vc, table, seq, pps, DECODE.scale,
+                                                 workspace=det_ws, o=do, lse=dlse)
+        dms = []
+        for _ in range(20):
+            a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a_.record(stream)
+            attn.attn_decode_paged_deterministic(dq, kc, vc, table, seq, pps, DECODE.scale,
+                                                 workspace=det_ws, o=do, lse=dlse)
+            b_.record(stream)
+            b_.synchronize()
+            dms.append(a_.elapsed_time(b_))
+        dt = statistics.median(dms)
+        det = {"value": db / (dt * 1e-3) / 1e9, "unit": "GB/s", "ms": dt, "pages_per_split": pps,
+               "num_splits": det_splits, "frac_of_hbm": db / (dt * 1e-3) / 1e9 / hbm_peak}
+
     # ---- pairwise (O, LSE) merge (prefix / suffix combine), outside the step ----
     merge_pair = measure_merge_pair(dev, flush, hbm_peak, peak_kind) if args.only is None else None
 
@@ -463,6 +486,7 @@ def run_gpu(args, world, rank, local):
                          "peak_source": f"{peak_kind} copy bandwidth"},
             "e2e": dec_e2e,
             "cpu_baseline": dec_cpu,
+            "deterministic": det,
         },
         "merge_pair": merge_pair,
         "prefill_ms": pre_avg,

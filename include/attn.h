@@ -193,6 +193,33 @@ attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* 
                                 void* o, float* lse, void* stream);
 
 /*
+ * attn_decode_paged_deterministic -- attn_decode_paged with splits of a fixed
+ * length, so that a row's result depends on the row alone. Follows [DEC]
+ * "Split-K breaks bitwise reproducibility" (the split count, and with it the
+ * order of the fp32 merge, otherwise follows the batch) and its fixed-tile
+ * remedy: every split of a row covers pages_per_split pages (the last one the
+ * rest), a row of n pages uses ceil(n / pages_per_split) splits, and the
+ * partials are merged in split order. The output of a row is then
+ * bit-identical whatever the other rows, the batch size or num_splits are.
+ * The trade: a short row uses few splits, so a small batch may leave SMs idle.
+ *
+ * Arguments, layouts, workspace (attn_decode_workspace_bytes for num_splits)
+ * and errors are those of attn_decode_paged, plus:
+ *   pages_per_split >= 1: pages (of page_size keys) per split;
+ *   num_splits: the grid's split count; must satisfy
+ *     num_splits * pages_per_split >= max_blocks_per_seq (INVALID_ARG
+ *     otherwise), so that every row's splits fit.
+ */
+attn_status_t attn_decode_paged_deterministic(const void* q, const void* k_cache,
+                                              const void* v_cache, const int32_t* block_table,
+                                              const int32_t* seq_lens, int B, int h, int h_kv,
+                                              int d_h, int page_size, int num_blocks,
+                                              int max_blocks_per_seq, int num_splits,
+                                              int pages_per_split, float scale, void* workspace,
+                                              size_t workspace_bytes, void* o, float* lse,
+                                              void* stream);
+
+/*
  * attn_decode_paged_static -- attn_decode_paged without a workspace argument
  * and without any allocation. The pages have no counterpart of this entry
  * point; it exists for callers that cannot obtain device memory at the call

@@ -71,6 +71,9 @@ def library() -> ctypes.CDLL:
     lib.attn_decode_workspace_bytes.restype = S
     lib.attn_decode_paged.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, F, P, S, P, P, P]
     lib.attn_decode_paged.restype = I
+    lib.attn_decode_paged_deterministic.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, P, S, P,
+                                                     P, P]
+    lib.attn_decode_paged_deterministic.restype = I
     lib.attn_merge_states.argtypes = [P, P, P, P, I, I, I, P, P, I, P]
     lib.attn_merge_states.restype = I
     lib.attn_merge_lse_pair.argtypes = [P, P, P, P, I, I, I, P, P, I, P]
@@ -206,6 +209,43 @@ def attn_decode_paged(q, k_cache, v_cache, block_table, seq_lens, num_splits: in
         page, nb, block_table.shape[1], int(num_splits), scale, _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(o), _ptr(lse), _stream(stream))
     _check("attn_decode_paged", st)
+    return o, lse
+
+
+def attn_decode_paged_deterministic(q, k_cache, v_cache, block_table, seq_lens, pages_per_split: int,
+                                    scale: float | None = None, num_splits: int | None = None,
+                                    workspace=None, o=None, lse=None, return_lse: bool = True,
+                                    stream=None):
+    """attn_decode_paged with fixed-length splits (pages_per_split pages each):
+    each row's result is independent of the rest of the batch. num_splits
+    defaults to the smallest grid that covers the block table."""
+    for t in (q, k_cache, v_cache, block_table, seq_lens):
+        _need(t.is_cuda and t.is_contiguous(), "decode tensors must be contiguous CUDA tensors")
+    _need(q.dtype == k_cache.dtype == v_cache.dtype == torch.bfloat16, "q and caches must be bf16")
+    _need(block_table.dtype == torch.int32 and seq_lens.dtype == torch.int32,
+          "block_table and seq_lens must be int32")
+    _need(pages_per_split >= 1, "pages_per_split must be >= 1")
+    B, h, d = q.shape
+    nb, page, h_kv, d2 = k_cache.shape
+    _need(d2 == d and v_cache.shape == k_cache.shape, "cache shape mismatch")
+    _need(block_table.dim() == 2 and block_table.shape[0] == B and seq_lens.shape == (B,),
+          "block_table [B,max_blocks] and seq_lens [B] expected")
+    max_blocks = block_table.shape[1]
+    if num_splits is None:
+        num_splits = -(-max_blocks // pages_per_split)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    need = attn_decode_workspace_bytes(B, h, d, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, h), dtype=torch.float32, device=q.device)
+    st = library().attn_decode_paged_deterministic(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens), B, h, h_kv, d,
+        page, nb, max_blocks, int(num_splits), int(pages_per_split), scale, _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(o), _ptr(lse), _stream(stream))
+    _check("attn_decode_paged_deterministic", st)
     return o, lse
 
 

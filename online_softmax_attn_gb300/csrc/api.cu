@@ -135,10 +135,13 @@ attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o,
   return from_cuda(e);
 }
 
-attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* v_cache,
+namespace {
+// Shared by attn_decode_paged (fixed_pps = 0: pages per split from
+// num_splits) and attn_decode_paged_deterministic (fixed_pps > 0).
+attn_status_t decode_paged_impl(const void* q, const void* k_cache, const void* v_cache,
                                 const int32_t* block_table, const int32_t* seq_lens, int B, int h,
                                 int h_kv, int d_h, int page_size, int num_blocks,
-                                int max_blocks_per_seq, int num_splits, float scale,
+                                int max_blocks_per_seq, int num_splits, int fixed_pps, float scale,
                                 void* workspace, size_t workspace_bytes, void* o, float* lse,
                                 void* stream) {
   if (B < 0 || h < 1 || h_kv < 1 || h % h_kv != 0 || num_blocks < 1 || max_blocks_per_seq < 1 ||
@@ -177,6 +180,7 @@ attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* 
   a.max_blocks_per_seq = max_blocks_per_seq;
   a.num_splits = num_splits;
   a.scale = scale;
+  a.fixed_pps = fixed_pps;
   a.o_part = reinterpret_cast<float*>(ws + L.o_off);
   a.m_part = reinterpret_cast<float*>(ws + L.m_off);
   a.l_part = reinterpret_cast<float*>(ws + L.l_off);
@@ -185,8 +189,37 @@ attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* 
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
   e = launch_merge(a.o_part, a.m_part, a.l_part, nullptr, seq_lens, h, page_size,
                    max_blocks_per_seq * page_size, static_cast<int>(rows), num_splits, d_h, o, lse,
-                   ATTN_DTYPE_BF16, s);
+                   ATTN_DTYPE_BF16, s, fixed_pps);
   return from_cuda(e);
+}
+}  // namespace
+
+attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* v_cache,
+                                const int32_t* block_table, const int32_t* seq_lens, int B, int h,
+                                int h_kv, int d_h, int page_size, int num_blocks,
+                                int max_blocks_per_seq, int num_splits, float scale,
+                                void* workspace, size_t workspace_bytes, void* o, float* lse,
+                                void* stream) {
+  return decode_paged_impl(q, k_cache, v_cache, block_table, seq_lens, B, h, h_kv, d_h, page_size,
+                           num_blocks, max_blocks_per_seq, num_splits, 0, scale, workspace,
+                           workspace_bytes, o, lse, stream);
+}
+
+attn_status_t attn_decode_paged_deterministic(const void* q, const void* k_cache,
+                                              const void* v_cache, const int32_t* block_table,
+                                              const int32_t* seq_lens, int B, int h, int h_kv,
+                                              int d_h, int page_size, int num_blocks,
+                                              int max_blocks_per_seq, int num_splits,
+                                              int pages_per_split, float scale, void* workspace,
+                                              size_t workspace_bytes, void* o, float* lse,
+                                              void* stream) {
+  if (pages_per_split < 1 || max_blocks_per_seq < 1) return ATTN_ERR_INVALID_ARG;
+  // The grid must hold every split of the longest possible row.
+  if (static_cast<long long>(num_splits) * pages_per_split < max_blocks_per_seq)
+    return ATTN_ERR_INVALID_ARG;
+  return decode_paged_impl(q, k_cache, v_cache, block_table, seq_lens, B, h, h_kv, d_h, page_size,
+                           num_blocks, max_blocks_per_seq, num_splits, pages_per_split, scale,
+                           workspace, workspace_bytes, o, lse, stream);
 }
 
 attn_status_t attn_merge_states(const float* o_part, const float* m_part, const float* l_part,

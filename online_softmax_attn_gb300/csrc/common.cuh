@@ -26,16 +26,25 @@ constexpr float kLn2 = 0.6931471805599453f;
 // ---------------------------------------------------------------------------
 // Split plan, shared by the decode producer, its reduce and the host.
 // ---------------------------------------------------------------------------
-__host__ __device__ __forceinline__ int split_plan(int seq_len, int page_size, int num_splits,
-                                                   int* pages_per_split) {
+// fixed_pps > 0: every split covers fixed_pps pages (the last one the rest),
+// so a row's split boundaries depend on its own length only; the caller
+// guarantees num_splits >= ceil(n_pages / fixed_pps).
+__host__ __device__ __forceinline__ int split_plan_fixed(int seq_len, int page_size,
+                                                         int num_splits, int fixed_pps,
+                                                         int* pages_per_split) {
   const int n_pages = (seq_len + page_size - 1) / page_size;
   if (n_pages <= 0) {
     if (pages_per_split) *pages_per_split = 0;
     return 0;
   }
-  const int pps = (n_pages + num_splits - 1) / num_splits;
+  const int pps = fixed_pps > 0 ? fixed_pps : (n_pages + num_splits - 1) / num_splits;
   if (pages_per_split) *pages_per_split = pps;
   return (n_pages + pps - 1) / pps;
+}
+
+__host__ __device__ __forceinline__ int split_plan(int seq_len, int page_size, int num_splits,
+                                                   int* pages_per_split) {
+  return split_plan_fixed(seq_len, page_size, num_splits, 0, pages_per_split);
 }
 
 // Row length as the decode kernels use it: clamped into [0, max_blocks*page].

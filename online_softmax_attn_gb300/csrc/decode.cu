@@ -100,7 +100,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
                         const __grid_constant__ CUtensorMap tmap_v,
                         const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ block_table,
                         const int32_t* __restrict__ seq_lens, int h, int max_blocks, int num_blocks,
-                        int num_splits, float qscale, float* __restrict__ o_part,
+                        int num_splits, int fixed_pps, float qscale, float* __restrict__ o_part,
                         float* __restrict__ m_part, float* __restrict__ l_part) {
   using C = DecodeCfg<D, G, NW, NST>;
   constexpr int KS = D / 16;  // k-steps of S = q K^T
@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
 
   const int seq_len = clamp_seq_len(seq_lens[b], max_blocks * kPage, &g_decode_err);
   int pps = 0;
-  const int n_act = split_plan(seq_len, kPage, num_splits, &pps);
+  const int n_act = split_plan_fixed(seq_len, kPage, num_splits, fixed_pps, &pps);
   if (split >= n_act) return;  // surplus split of a short (or empty) row
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -341,7 +341,8 @@ cudaError_t launch_cfg(const DecodeArgs& a, const CUtensorMap& tk, const CUtenso
   const float qscale = a.scale * kLog2e;
   kern<<<grid, NW * 32, C::SMEM, stream>>>(
       tk, tv, static_cast<const __nv_bfloat16*>(a.q), a.block_table, a.seq_lens, a.h,
-      a.max_blocks_per_seq, a.num_blocks, a.num_splits, qscale, a.o_part, a.m_part, a.l_part);
+      a.max_blocks_per_seq, a.num_blocks, a.num_splits, a.fixed_pps, qscale, a.o_part, a.m_part,
+      a.l_part);
   return cudaGetLastError();
 }
 

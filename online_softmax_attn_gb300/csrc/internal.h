@@ -31,10 +31,11 @@ inline PartialLayout partial_layout(long long rows, int num_splits, int d_h) {
 // n_active == nullptr and seq_lens == nullptr: all splits active.
 // seq_lens != nullptr: n_active(row) = split_plan(seq_lens[row / heads_per_seq]),
 // with the length clamped into [0, max_len] exactly as the decode kernel does.
+// fixed_pps as in split_plan_fixed (0: pages per split from num_splits).
 cudaError_t launch_merge(const float* o_part, const float* m_part, const float* l_part,
                          const int32_t* n_active, const int32_t* seq_lens, int heads_per_seq,
                          int page_size, int max_len, int rows, int num_splits, int d_h, void* o, float* lse,
-                         attn_dtype_t out_dtype, cudaStream_t stream);
+                         attn_dtype_t out_dtype, cudaStream_t stream, int fixed_pps = 0);
 unsigned int merge_read_and_clear_error(cudaStream_t stream, cudaError_t* st);
 // Pairwise (O, LSE) merge; arguments validated by the caller.
 cudaError_t launch_merge_pair(const void* o_a, const float* lse_a, const void* o_b,
@@ -53,6 +54,7 @@ struct DecodeArgs {
   float* o_part;
   float* m_part;
   float* l_part;
+  int fixed_pps = 0;  // > 0: fixed pages per split (split_plan_fixed)
 };
 cudaError_t launch_decode_split(const DecodeArgs& a, cudaStream_t stream);
 unsigned int decode_read_and_clear_error(cudaStream_t stream, cudaError_t* st);

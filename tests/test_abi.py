@@ -195,3 +195,19 @@ def test_merge_lse_pair_arguments(lib):
     assert lib.attn_merge_lse_pair(*a) == bad
     a = list(ok_args); a[8] = P(4100)  # output LSE overlaps lse_a
     assert lib.attn_merge_lse_pair(*a) == bad
+
+
+def test_decode_deterministic_arguments(lib):
+    P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    lib.attn_decode_paged_deterministic.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, P,
+                                                    ctypes.c_size_t, P, P, P]
+    d = P(256)
+    bad = attn.ATTN_ERR_INVALID_ARG
+    base = [d, d, d, d, d, 2, 32, 8, 128, 16, 100, 64, 4, 16, 0.1, d, 1 << 30, d, None, None]
+    # 4 splits x 16 pages cover a 64-page table; arguments otherwise valid up to the launch
+    a = list(base); a[13] = 0                   # pages_per_split < 1
+    assert lib.attn_decode_paged_deterministic(*a) == bad
+    a = list(base); a[12] = 3                   # 3 x 16 < 64 pages: a row would not fit
+    assert lib.attn_decode_paged_deterministic(*a) == bad
+    a = list(base); a[5] = 0                    # B = 0 is a no-op
+    assert lib.attn_decode_paged_deterministic(*a) == 0
