@@ -421,6 +421,30 @@ def run_gpu(args, world, rank, local):
         det = {"value": db / (dt * 1e-3) / 1e9, "unit": "GB/s", "ms": dt, "pages_per_split": pps,
                "num_splits": det_splits, "frac_of_hbm": db / (dt * 1e-3) / 1e9 / hbm_peak}
 
+    # ---- adaptive decode (split count planned on the device, grid of 32), outside the step ----
+    adaptive = None
+    if args.only is None:
+        amax = 32
+        ad_ws = torch.empty(attn.attn_decode_adaptive_workspace_bytes(B, DECODE.h, DECODE.d_h, amax),
+                            dtype=torch.uint8, device=dev)
+        for _ in range(3):
+            attn.attn_decode_paged_adaptive(dq, kc, vc, table, seq, amax, DECODE.scale,
+                                            workspace=ad_ws, o=do, lse=dlse)
+        ams = []
+        for _ in range(20):
+            a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a_.record(stream)
+            attn.attn_decode_paged_adaptive(dq, kc, vc, table, seq, amax, DECODE.scale,
+                                            workspace=ad_ws, o=do, lse=dlse)
+            b_.record(stream)
+            b_.synchronize()
+            ams.append(a_.elapsed_time(b_))
+        at = statistics.median(ams)
+        off = attn.attn_decode_workspace_bytes(B, DECODE.h, DECODE.d_h, amax)
+        adaptive = {"value": db / (at * 1e-3) / 1e9, "unit": "GB/s", "ms": at, "max_splits": amax,
+                    "device_pages_per_split": int(ad_ws[off:off + 4].view(torch.int32).item()),
+                    "frac_of_hbm": db / (at * 1e-3) / 1e9 / hbm_peak}
+
     # ---- pairwise (O, LSE) merge (prefix / suffix combine), outside the step ----
     merge_pair = measure_merge_pair(dev, flush, hbm_peak, peak_kind) if args.only is None else None
 
@@ -487,6 +511,7 @@ def run_gpu(args, world, rank, local):
             "e2e": dec_e2e,
             "cpu_baseline": dec_cpu,
             "deterministic": det,
+            "adaptive": adaptive,
         },
         "merge_pair": merge_pair,
         "prefill_ms": pre_avg,

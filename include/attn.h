@@ -193,6 +193,33 @@ attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* 
                                 void* o, float* lse, void* stream);
 
 /*
+ * attn_decode_paged_adaptive -- attn_decode_paged with the split count chosen
+ * on the device, for CUDA-graph capture. Follows [DEC] "SGLang: a split count
+ * computed per sequence, on device" and "CUDA graphs need the split count
+ * pinned": the launch geometry is fixed by max_splits (a grid of
+ * max_splits x h_kv x B; CTAs past a row's splits return at once), while a
+ * one-CTA plan kernel reads the batch's seq_lens, applies the rule of
+ * attn_recommended_splits (with the GPU's SM count) capped at max_splits, and
+ * turns it into pages per split of the longest row. Every row is cut into
+ * splits of that many pages; the split kernel and the merge read the same
+ * device value, so they agree on each row's active splits. A graph captured
+ * once stays valid for any seq_lens with the same B and max_blocks_per_seq.
+ *
+ * Arguments, layouts and errors are those of attn_decode_paged with
+ * num_splits replaced by max_splits (1 .. ATTN_MAX_SPLITS), plus:
+ *   workspace: attn_decode_adaptive_workspace_bytes(B, h, d_h, max_splits)
+ *     bytes; its last 256 bytes begin with the plan (int32 pages per split)
+ *     written by the call.
+ */
+size_t attn_decode_adaptive_workspace_bytes(int B, int h, int d_h, int max_splits);
+attn_status_t attn_decode_paged_adaptive(const void* q, const void* k_cache, const void* v_cache,
+                                         const int32_t* block_table, const int32_t* seq_lens,
+                                         int B, int h, int h_kv, int d_h, int page_size,
+                                         int num_blocks, int max_blocks_per_seq, int max_splits,
+                                         float scale, void* workspace, size_t workspace_bytes,
+                                         void* o, float* lse, void* stream);
+
+/*
  * attn_decode_paged_deterministic -- attn_decode_paged with splits of a fixed
  * length, so that a row's result depends on the row alone. Follows [DEC]
  * "Split-K breaks bitwise reproducibility" (the split count, and with it the

@@ -71,6 +71,10 @@ def library() -> ctypes.CDLL:
     lib.attn_decode_workspace_bytes.restype = S
     lib.attn_decode_paged.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, F, P, S, P, P, P]
     lib.attn_decode_paged.restype = I
+    lib.attn_decode_adaptive_workspace_bytes.argtypes = [I, I, I, I]
+    lib.attn_decode_adaptive_workspace_bytes.restype = S
+    lib.attn_decode_paged_adaptive.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, F, P, S, P, P, P]
+    lib.attn_decode_paged_adaptive.restype = I
     lib.attn_decode_paged_deterministic.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, P, S, P,
                                                      P, P]
     lib.attn_decode_paged_deterministic.restype = I
@@ -209,6 +213,42 @@ def attn_decode_paged(q, k_cache, v_cache, block_table, seq_lens, num_splits: in
         page, nb, block_table.shape[1], int(num_splits), scale, _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(o), _ptr(lse), _stream(stream))
     _check("attn_decode_paged", st)
+    return o, lse
+
+
+def attn_decode_adaptive_workspace_bytes(B: int, h: int, d_h: int, max_splits: int) -> int:
+    """Partials for max_splits plus 256 bytes for the on-device plan."""
+    return library().attn_decode_adaptive_workspace_bytes(B, h, d_h, max_splits)
+
+
+def attn_decode_paged_adaptive(q, k_cache, v_cache, block_table, seq_lens, max_splits: int,
+                               scale: float | None = None, workspace=None, o=None, lse=None,
+                               return_lse: bool = True, stream=None):
+    """Paged decode whose split count is planned on the device from seq_lens
+    (launch geometry fixed by max_splits: capturable in a CUDA graph)."""
+    for t in (q, k_cache, v_cache, block_table, seq_lens):
+        _need(t.is_cuda and t.is_contiguous(), "decode tensors must be contiguous CUDA tensors")
+    _need(q.dtype == k_cache.dtype == v_cache.dtype == torch.bfloat16, "q and caches must be bf16")
+    _need(block_table.dtype == torch.int32 and seq_lens.dtype == torch.int32,
+          "block_table and seq_lens must be int32")
+    B, h, d = q.shape
+    nb, page, h_kv, d2 = k_cache.shape
+    _need(d2 == d and v_cache.shape == k_cache.shape, "cache shape mismatch")
+    _need(block_table.dim() == 2 and block_table.shape[0] == B and seq_lens.shape == (B,),
+          "block_table [B,max_blocks] and seq_lens [B] expected")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    need = attn_decode_adaptive_workspace_bytes(B, h, d, max_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, h), dtype=torch.float32, device=q.device)
+    st = library().attn_decode_paged_adaptive(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens), B, h, h_kv, d,
+        page, nb, block_table.shape[1], int(max_splits), scale, _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(o), _ptr(lse), _stream(stream))
+    _check("attn_decode_paged_adaptive", st)
     return o, lse
 
 

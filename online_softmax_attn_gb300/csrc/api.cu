@@ -72,26 +72,7 @@ int attn_decode_split_plan(int seq_len, int page_size, int num_splits, int* page
 int attn_recommended_splits(int B, int h_kv, int max_seq_len, long long total_seq_len,
                             int num_sms) {
   if (B < 1 || h_kv < 1 || max_seq_len < 0 || total_seq_len < 0 || num_sms < 1) return -1;
-  const long long g2d = static_cast<long long>(B) * h_kv;
-  long long s = (num_sms + g2d - 1) / g2d;  // first-wave coverage
-  const long long max_pages = (max_seq_len + 15) / 16;
-  // Ragged batch (the longest row well above the mean): keep the longest
-  // row's split below a quarter of the mean work per SM, so that the tail of
-  // the longest rows stays short. Rows of one length need no such rule.
-  if (total_seq_len > 0 && 4ll * max_seq_len * B > 5ll * total_seq_len) {
-    const long long total_pages = ((total_seq_len + 15) / 16) * h_kv;
-    const long long mean_per_sm = (total_pages + num_sms - 1) / num_sms;
-    const long long target = mean_per_sm / 4 > 0 ? mean_per_sm / 4 : 1;
-    const long long s_bal = (max_pages + target - 1) / target;
-    if (s_bal > s) s = s_bal;
-  }
-  // At least 32 pages (four per warp) per split of the longest row, so that
-  // a CTA's start-up (row length, block table, first page) is amortised.
-  const long long s_work = (max_pages + 31) / 32;
-  if (s > s_work) s = s_work;
-  if (s < 1) s = 1;
-  if (s > ATTN_MAX_SPLITS) s = ATTN_MAX_SPLITS;
-  return static_cast<int>(s);
+  return splits_rule(B, h_kv, max_seq_len, total_seq_len, num_sms, ATTN_MAX_SPLITS);
 }
 
 size_t attn_decode_workspace_bytes(int B, int h, int d_h, int num_splits) {
@@ -137,13 +118,15 @@ attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o,
 
 namespace {
 // Shared by attn_decode_paged (fixed_pps = 0: pages per split from
-// num_splits) and attn_decode_paged_deterministic (fixed_pps > 0).
+// num_splits), attn_decode_paged_deterministic (fixed_pps > 0) and
+// attn_decode_paged_adaptive (adaptive: pages per split planned on the device,
+// kept in the 256 bytes after the partials).
 attn_status_t decode_paged_impl(const void* q, const void* k_cache, const void* v_cache,
                                 const int32_t* block_table, const int32_t* seq_lens, int B, int h,
                                 int h_kv, int d_h, int page_size, int num_blocks,
                                 int max_blocks_per_seq, int num_splits, int fixed_pps, float scale,
                                 void* workspace, size_t workspace_bytes, void* o, float* lse,
-                                void* stream) {
+                                void* stream, bool adaptive = false) {
   if (B < 0 || h < 1 || h_kv < 1 || h % h_kv != 0 || num_blocks < 1 || max_blocks_per_seq < 1 ||
       num_splits < 1 || num_splits > ATTN_MAX_SPLITS || !std::isfinite(scale) || !(scale > 0.f))
     return ATTN_ERR_INVALID_ARG;
@@ -162,7 +145,7 @@ attn_status_t decode_paged_impl(const void* q, const void* k_cache, const void* 
     return ATTN_ERR_INVALID_ARG;
   const long long rows = static_cast<long long>(B) * h;
   const PartialLayout L = partial_layout(rows, num_splits, d_h);
-  if (workspace_bytes < L.total) return ATTN_ERR_INVALID_ARG;
+  if (workspace_bytes < L.total + (adaptive ? 256u : 0u)) return ATTN_ERR_INVALID_ARG;
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   DecodeArgs a;
@@ -181,15 +164,27 @@ attn_status_t decode_paged_impl(const void* q, const void* k_cache, const void* 
   a.num_splits = num_splits;
   a.scale = scale;
   a.fixed_pps = fixed_pps;
+  int* pps_dev = adaptive ? reinterpret_cast<int*>(ws + L.total) : nullptr;
+  a.pps_dev = pps_dev;
   a.o_part = reinterpret_cast<float*>(ws + L.o_off);
   a.m_part = reinterpret_cast<float*>(ws + L.m_off);
   a.l_part = reinterpret_cast<float*>(ws + L.l_off);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_decode_split(a, s);
+  cudaError_t e = cudaSuccess;
+  if (adaptive) {
+    int dev = 0, sms = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+      e = launch_decode_plan(seq_lens, B, h_kv, max_blocks_per_seq * page_size, sms, num_splits,
+                             pps_dev, s);
+    if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  }
+  e = launch_decode_split(a, s);
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
   e = launch_merge(a.o_part, a.m_part, a.l_part, nullptr, seq_lens, h, page_size,
                    max_blocks_per_seq * page_size, static_cast<int>(rows), num_splits, d_h, o, lse,
-                   ATTN_DTYPE_BF16, s, fixed_pps);
+                   ATTN_DTYPE_BF16, s, fixed_pps, pps_dev);
   return from_cuda(e);
 }
 }  // namespace
@@ -203,6 +198,22 @@ attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* 
   return decode_paged_impl(q, k_cache, v_cache, block_table, seq_lens, B, h, h_kv, d_h, page_size,
                            num_blocks, max_blocks_per_seq, num_splits, 0, scale, workspace,
                            workspace_bytes, o, lse, stream);
+}
+
+size_t attn_decode_adaptive_workspace_bytes(int B, int h, int d_h, int max_splits) {
+  if (B < 0 || h < 1 || d_h < 1 || max_splits < 1) return 0;
+  return partial_layout(static_cast<long long>(B) * h, max_splits, d_h).total + 256;
+}
+
+attn_status_t attn_decode_paged_adaptive(const void* q, const void* k_cache, const void* v_cache,
+                                         const int32_t* block_table, const int32_t* seq_lens,
+                                         int B, int h, int h_kv, int d_h, int page_size,
+                                         int num_blocks, int max_blocks_per_seq, int max_splits,
+                                         float scale, void* workspace, size_t workspace_bytes,
+                                         void* o, float* lse, void* stream) {
+  return decode_paged_impl(q, k_cache, v_cache, block_table, seq_lens, B, h, h_kv, d_h, page_size,
+                           num_blocks, max_blocks_per_seq, max_splits, 0, scale, workspace,
+                           workspace_bytes, o, lse, stream, true);
 }
 
 attn_status_t attn_decode_paged_deterministic(const void* q, const void* k_cache,

@@ -47,6 +47,32 @@ __host__ __device__ __forceinline__ int split_plan(int seq_len, int page_size, i
   return split_plan_fixed(seq_len, page_size, num_splits, 0, pages_per_split);
 }
 
+// Split count for a decode batch ([DEC] "The grid": fill the first wave,
+// S* = ceil(N_SM / (B h_kv))). A ragged batch (longest row > 1.25x the mean,
+// known from total_len > 0) is raised until the longest row's split is at
+// most a quarter of the mean work per SM; every split of the longest row then
+// keeps at least 32 pages. Result in [1, max_splits]. The host recommendation
+// and the on-device plan of the adaptive decode use this same function.
+__host__ __device__ __forceinline__ int splits_rule(long long B, long long h_kv, long long max_len,
+                                                    long long total_len, long long num_sms,
+                                                    long long max_splits) {
+  const long long g2d = B * h_kv;
+  long long s = (num_sms + g2d - 1) / g2d;  // first-wave coverage
+  const long long max_pages = (max_len + 15) / 16;
+  if (total_len > 0 && 4ll * max_len * B > 5ll * total_len) {
+    const long long total_pages = ((total_len + 15) / 16) * h_kv;
+    const long long mean_per_sm = (total_pages + num_sms - 1) / num_sms;
+    const long long target = mean_per_sm / 4 > 0 ? mean_per_sm / 4 : 1;
+    const long long s_bal = (max_pages + target - 1) / target;
+    if (s_bal > s) s = s_bal;
+  }
+  const long long s_work = (max_pages + 31) / 32;
+  if (s > s_work) s = s_work;
+  if (s < 1) s = 1;
+  if (s > max_splits) s = max_splits;
+  return static_cast<int>(s);
+}
+
 // Row length as the decode kernels use it: clamped into [0, max_blocks*page].
 __device__ __forceinline__ int clamp_seq_len(int seq_len, int max_len, unsigned int* err) {
   if (seq_len < 0 || seq_len > max_len) {

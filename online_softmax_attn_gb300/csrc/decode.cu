@@ -100,7 +100,8 @@ __global__ void __launch_bounds__(NW * 32, 1)
                         const __grid_constant__ CUtensorMap tmap_v,
                         const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ block_table,
                         const int32_t* __restrict__ seq_lens, int h, int max_blocks, int num_blocks,
-                        int num_splits, int fixed_pps, float qscale, float* __restrict__ o_part,
+                        int num_splits, int fixed_pps, const int* __restrict__ pps_dev,
+                        float qscale, float* __restrict__ o_part,
                         float* __restrict__ m_part, float* __restrict__ l_part) {
   using C = DecodeCfg<D, G, NW, NST>;
   constexpr int KS = D / 16;  // k-steps of S = q K^T
@@ -131,7 +132,8 @@ __global__ void __launch_bounds__(NW * 32, 1)
 
   const int seq_len = clamp_seq_len(seq_lens[b], max_blocks * kPage, &g_decode_err);
   int pps = 0;
-  const int n_act = split_plan_fixed(seq_len, kPage, num_splits, fixed_pps, &pps);
+  const int n_act =
+      split_plan_fixed(seq_len, kPage, num_splits, pps_dev ? *pps_dev : fixed_pps, &pps);
   if (split >= n_act) return;  // surplus split of a short (or empty) row
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -341,8 +343,8 @@ cudaError_t launch_cfg(const DecodeArgs& a, const CUtensorMap& tk, const CUtenso
   const float qscale = a.scale * kLog2e;
   kern<<<grid, NW * 32, C::SMEM, stream>>>(
       tk, tv, static_cast<const __nv_bfloat16*>(a.q), a.block_table, a.seq_lens, a.h,
-      a.max_blocks_per_seq, a.num_blocks, a.num_splits, a.fixed_pps, qscale, a.o_part, a.m_part,
-      a.l_part);
+      a.max_blocks_per_seq, a.num_blocks, a.num_splits, a.fixed_pps, a.pps_dev, qscale, a.o_part,
+      a.m_part, a.l_part);
   return cudaGetLastError();
 }
 
@@ -359,7 +361,47 @@ cudaError_t launch_d(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorM
   }
 }
 
+// On-device split plan of the adaptive decode: the batch's longest and total
+// (clamped) length, splits_rule, then pages per split of the longest row. The
+// split kernel and the merge read the result, so the launch geometry (a grid
+// of max_splits) never depends on the lengths.
+__global__ void __launch_bounds__(256)
+    decode_plan_kernel(const int32_t* __restrict__ seq_lens, int B, int h_kv, int max_len,
+                       int num_sms, int max_splits, int* __restrict__ pps_out) {
+  __shared__ long long s_tot[256];
+  __shared__ int s_max[256];
+  long long tot = 0;
+  int mx = 0;
+  for (int b = threadIdx.x; b < B; b += blockDim.x) {
+    const int len = clamp_seq_len(seq_lens[b], max_len, &g_decode_err);
+    tot += len;
+    mx = max(mx, len);
+  }
+  s_tot[threadIdx.x] = tot;
+  s_max[threadIdx.x] = mx;
+  __syncthreads();
+  for (int off = blockDim.x / 2; off > 0; off >>= 1) {
+    if (threadIdx.x < off) {
+      s_tot[threadIdx.x] += s_tot[threadIdx.x + off];
+      s_max[threadIdx.x] = max(s_max[threadIdx.x], s_max[threadIdx.x + off]);
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    const int s = splits_rule(B, h_kv, s_max[0], s_tot[0], num_sms, max_splits);
+    const int max_pages = (s_max[0] + kPage - 1) / kPage;
+    *pps_out = max(1, (max_pages + s - 1) / s);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_decode_plan(const int32_t* seq_lens, int B, int h_kv, int max_len,
+                               int num_sms, int max_splits, int* pps_out, cudaStream_t stream) {
+  decode_plan_kernel<<<1, 256, 0, stream>>>(seq_lens, B, h_kv, max_len, num_sms, max_splits,
+                                            pps_out);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_decode_split(const DecodeArgs& a, cudaStream_t stream) {
   CUtensorMap tk, tv;

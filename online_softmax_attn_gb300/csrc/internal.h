@@ -35,7 +35,8 @@ inline PartialLayout partial_layout(long long rows, int num_splits, int d_h) {
 cudaError_t launch_merge(const float* o_part, const float* m_part, const float* l_part,
                          const int32_t* n_active, const int32_t* seq_lens, int heads_per_seq,
                          int page_size, int max_len, int rows, int num_splits, int d_h, void* o, float* lse,
-                         attn_dtype_t out_dtype, cudaStream_t stream, int fixed_pps = 0);
+                         attn_dtype_t out_dtype, cudaStream_t stream, int fixed_pps = 0,
+                         const int* pps_dev = nullptr);
 unsigned int merge_read_and_clear_error(cudaStream_t stream, cudaError_t* st);
 // Pairwise (O, LSE) merge; arguments validated by the caller.
 cudaError_t launch_merge_pair(const void* o_a, const float* lse_a, const void* o_b,
@@ -55,7 +56,12 @@ struct DecodeArgs {
   float* m_part;
   float* l_part;
   int fixed_pps = 0;  // > 0: fixed pages per split (split_plan_fixed)
+  const int* pps_dev = nullptr;  // non-null: pages per split read from device memory
 };
+// One CTA: the batch's split count by splits_rule, as pages per split of the
+// longest row, written to *pps_out (adaptive decode).
+cudaError_t launch_decode_plan(const int32_t* seq_lens, int B, int h_kv, int max_len,
+                               int num_sms, int max_splits, int* pps_out, cudaStream_t stream);
 cudaError_t launch_decode_split(const DecodeArgs& a, cudaStream_t stream);
 unsigned int decode_read_and_clear_error(cudaStream_t stream, cudaError_t* st);
 

@@ -28,7 +28,7 @@ __global__ void __launch_bounds__(256)
                         const float* __restrict__ l_part, const int32_t* __restrict__ n_active,
                         const int32_t* __restrict__ seq_lens, int heads_per_seq, int page_size,
                         int max_len, int rows, int S, void* __restrict__ o_out, float* __restrict__ lse_out,
-                        int fixed_pps) {
+                        int fixed_pps, const int* __restrict__ pps_dev) {
   constexpr int VEC = D / 32;
   static_assert(VEC == 2 || VEC == 4, "d_h must be 64 or 128");
   constexpr int RPC = 8 / WPR;  // rows per CTA of 8 warps
@@ -47,7 +47,7 @@ __global__ void __launch_bounds__(256)
       n = n_active[row];
     } else if (seq_lens != nullptr) {
       const int len = clamp_seq_len(seq_lens[row / heads_per_seq], max_len, &g_merge_err);
-      n = split_plan_fixed(len, page_size, S, fixed_pps, nullptr);
+      n = split_plan_fixed(len, page_size, S, pps_dev ? *pps_dev : fixed_pps, nullptr);
     } else {
       n = S;
     }
@@ -148,7 +148,8 @@ __global__ void __launch_bounds__(256)
 cudaError_t launch_merge(const float* o_part, const float* m_part, const float* l_part,
                          const int32_t* n_active, const int32_t* seq_lens, int heads_per_seq,
                          int page_size, int max_len, int rows, int num_splits, int d_h, void* o, float* lse,
-                         attn_dtype_t out_dtype, cudaStream_t stream, int fixed_pps) {
+                         attn_dtype_t out_dtype, cudaStream_t stream, int fixed_pps,
+                         const int* pps_dev) {
   if (rows <= 0) return cudaSuccess;
   // Few rows and many splits: spread each row's splits over 8 warps.
   const bool wide = rows < 512 && num_splits > 4;
@@ -159,7 +160,7 @@ cudaError_t launch_merge(const float* o_part, const float* m_part, const float* 
   merge_states_kernel<D, BF, W><<<grid, block, 0, stream>>>(o_part, m_part, l_part, n_active,   \
                                                             seq_lens, heads_per_seq, page_size, \
                                                             max_len, rows, num_splits, o, lse, \
-                                                            fixed_pps)
+                                                            fixed_pps, pps_dev)
   if (d_h == 128) {
     if (bf) { if (wide) ATTN_MERGE_LAUNCH(128, true, 8); else ATTN_MERGE_LAUNCH(128, true, 1); }
     else { if (wide) ATTN_MERGE_LAUNCH(128, false, 8); else ATTN_MERGE_LAUNCH(128, false, 1); }

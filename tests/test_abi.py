@@ -211,3 +211,15 @@ def test_decode_deterministic_arguments(lib):
     assert lib.attn_decode_paged_deterministic(*a) == bad
     a = list(base); a[5] = 0                    # B = 0 is a no-op
     assert lib.attn_decode_paged_deterministic(*a) == 0
+
+
+def test_decode_adaptive_workspace(lib):
+    """The adaptive decode needs the partials for max_splits plus 256 bytes."""
+    need = attn.attn_decode_workspace_bytes(3, 32, 128, 16)
+    assert attn.attn_decode_adaptive_workspace_bytes(3, 32, 128, 16) == need + 256
+    P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    lib.attn_decode_paged_adaptive.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, F, P,
+                                               ctypes.c_size_t, P, P, P]
+    d = P(256)
+    assert lib.attn_decode_paged_adaptive(d, d, d, d, d, 3, 32, 8, 128, 16, 100, 64, 16, 0.1, d, need,
+                                          d, None, None) == attn.ATTN_ERR_INVALID_ARG
