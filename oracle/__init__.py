@@ -17,6 +17,8 @@ Contents (each function cites the passage it follows):
 * ``online_softmax_attention`` - the streaming recurrence over key blocks.
 * ``merge_partials_ref``   - the N-way reduce of split partial states.
 * ``merge_lse_pair_ref``   - the symmetric (O, LSE) merge of two results.
+* ``prefill_paged_ref``    - variable-length query rows over a paged cache
+                             (queries are a row's last key positions).
 """
 from .attention import (  # noqa: F401
     EMPTY_M,
@@ -30,5 +32,6 @@ from .attention import (  # noqa: F401
     merge_partials_ref,
     merge_states,
     online_softmax_attention,
+    prefill_paged_ref,
     to_f64,
 )

@@ -16,8 +16,9 @@ Readings taken where the pages are silent:
   * A row with no allowed key has output 0 and LSE = -inf ([MRG], last
     paragraph, which offers zero output as the extension; [DEC] reduce step
     returns 0 when the exp-sum is 0).
-  * Causal masking is for equal query and key lengths: key j is allowed for
-    query i iff j <= i.
+  * Causal masking for equal query and key lengths: key j is allowed for
+    query i iff j <= i. For a paged row with fewer queries than keys, the
+    queries are the last key positions (bottom-right alignment).
   * Inputs are upcast to float64 exactly as stored (bf16 / fp32 values).
 """
 from __future__ import annotations
@@ -168,6 +169,72 @@ def decode_paged_ref(q, k_cache, v_cache, block_table, seq_lens, scale: float, r
         o, lse = attention_ref(q64[b][:, None, :], K, V, scale, causal=False)
         O[b] = o[:, 0]
         LSE[b] = lse[:, 0]
+    return O, LSE
+
+
+def _gather_row(k_cache, v_cache, table_row, s: int):
+    """Keys 0 .. s-1 of one row through its page table, as [h_kv, s, d] float64."""
+    page = k_cache.shape[1]
+    pos = np.arange(s)
+    phys = np.asarray(table_row)[pos // page].astype(np.int64)
+    slot = pos % page
+    if hasattr(k_cache, "detach"):
+        import torch  # the caches may be CPU torch tensors (bf16)
+
+        ip, isl = torch.from_numpy(phys), torch.from_numpy(slot)
+        return (to_f64(k_cache[ip, isl]).transpose(1, 0, 2), to_f64(v_cache[ip, isl]).transpose(1, 0, 2))
+    return (to_f64(k_cache[phys, slot]).transpose(1, 0, 2), to_f64(v_cache[phys, slot]).transpose(1, 0, 2))
+
+
+def prefill_paged_ref(q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens, scale: float,
+                      causal: bool = True, tokens=None):
+    """Variable-length query rows over a paged KV cache (chunked prefill).
+
+    Row b owns query tokens cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 of the packed
+    q [total_q, h, d_h] and keys 0 .. seq_lens[b]-1 of the cache, gathered as in
+    ``decode_paged_ref`` ([DEC] paged addressing). Reading for unequal lengths:
+    the row's q_len queries are its last q_len key positions, so query i sits
+    at position seq_len - q_len + i and, with ``causal``, sees keys up to and
+    including that position (without it, all seq_len keys). Each allowed set
+    then goes through the definition (materialised safe softmax, per head with
+    the GQA broadcast of ``attention_ref``).
+
+    Returns O [total_q, h, d_h] and LSE [total_q, h] (float64). With ``tokens``
+    only those query tokens are evaluated (the others stay 0 / -inf).
+    """
+    q64 = to_f64(q)
+    table = np.asarray(block_table.cpu() if hasattr(block_table, "cpu") else block_table)
+    cu = np.asarray(cu_seqlens_q.cpu() if hasattr(cu_seqlens_q, "cpu") else cu_seqlens_q).tolist()
+    lens = np.asarray(seq_lens.cpu() if hasattr(seq_lens, "cpu") else seq_lens).tolist()
+    total_q, h, _ = q64.shape
+    h_kv = k_cache.shape[2]
+    d = v_cache.shape[3]
+    g = h // h_kv
+    O = np.zeros((total_q, h, d), dtype=np.float64)
+    LSE = np.full((total_q, h), EMPTY_M, dtype=np.float64)
+    want = None if tokens is None else set(int(t) for t in tokens)
+    for b in range(len(lens)):
+        t0, t1, s = int(cu[b]), int(cu[b + 1]), int(lens[b])
+        q_len = t1 - t0
+        if q_len == 0:
+            continue
+        if s < q_len:
+            raise ValueError("a row needs at least as many keys as queries")
+        sel = [i for i in range(q_len) if want is None or t0 + i in want]
+        if not sel:
+            continue
+        K, V = _gather_row(k_cache, v_cache, table[b], s)
+        pos = s - q_len + np.asarray(sel)  # key position of each selected query
+        if causal:
+            allowed = np.arange(s)[None, :] <= pos[:, None]
+        else:
+            allowed = np.ones((len(sel), s), dtype=bool)
+        for hq in range(h):
+            kvh = hq // g
+            S = scale * (q64[t0 + np.asarray(sel), hq] @ K[kvh].T)
+            o, lse = _softmax_rows_times_v(S, allowed, V[kvh])
+            O[t0 + np.asarray(sel), hq] = o
+            LSE[t0 + np.asarray(sel), hq] = lse
     return O, LSE
 
 

@@ -365,6 +365,69 @@ def pin_merge_lse_pair(A):
     assert np.allclose(Lm, L[:, 0], rtol=1e-12, atol=1e-12)
 
 
+def pin_paged_prefill(A):
+    """Variable-length paged rows: a row whose queries cover all its keys is
+    the square causal definition on the gathered keys; a one-query row is the
+    paged decode; tiny rows equal pure-Python loops with the queries at the
+    row's last key positions."""
+    rng = np.random.default_rng(21)
+    page, h, h_kv, d = 16, 4, 2, 3
+    q_lens = [5, 1, 3, 20]
+    s_lens = [5, 37, 18, 20]
+    need = [(s + page - 1) // page for s in s_lens]
+    nblk = sum(need) + 1
+    perm = rng.permutation(nblk)
+    table = -np.ones((len(s_lens), max(need)), dtype=np.int32)
+    off = 0
+    for b, n in enumerate(need):
+        table[b, :n] = perm[off:off + n]
+        off += n
+    cu = np.concatenate([[0], np.cumsum(q_lens)])
+    q = rng.normal(size=(int(cu[-1]), h, d))
+    kc = rng.normal(size=(nblk, page, h_kv, d))
+    vc = rng.normal(size=(nblk, page, h_kv, d))
+    scale = 0.45
+    O, L = A.prefill_paged_ref(q, kc, vc, table, cu, s_lens, scale, causal=True)
+
+    def gather(b):
+        s = s_lens[b]
+        phys = [int(table[b][p // page]) for p in range(s)]
+        K = np.stack([kc[phys[p], p % page] for p in range(s)], axis=1)  # [h_kv, s, d]
+        V = np.stack([vc[phys[p], p % page] for p in range(s)], axis=1)
+        return K, V
+
+    # row 0 and row 3: queries cover every key -> square causal attention
+    for b in (0, 3):
+        K, V = gather(b)
+        Oq, Lq = A.attention_ref(q[cu[b]:cu[b + 1]].transpose(1, 0, 2), K, V, scale, causal=True)
+        assert np.allclose(O[cu[b]:cu[b + 1]], Oq.transpose(1, 0, 2), atol=1e-12)
+        assert np.allclose(L[cu[b]:cu[b + 1]], Lq.T, atol=1e-12)
+    # row 1: one query -> the paged decode of that row over all 37 keys
+    Od, Ld = A.decode_paged_ref(q[cu[1]:cu[2]], kc, vc, table[1:2], [s_lens[1]], scale)
+    assert np.allclose(O[cu[1]], Od[0], atol=1e-12) and np.allclose(L[cu[1]], Ld[0], atol=1e-12)
+    # row 2: brute force, 3 queries at key positions 15, 16, 17 of 18
+    b, s, ql = 2, s_lens[2], q_lens[2]
+    for i in range(ql):
+        posi = s - ql + i
+        for hq in range(h):
+            kv = hq // (h // h_kv)
+            xs, vs = [], []
+            for p_ in range(posi + 1):
+                phys = int(table[b][p_ // page])
+                xs.append(scale * sum(q[cu[b] + i, hq, c] * kc[phys, p_ % page, kv, c] for c in range(d)))
+                vs.append(vc[phys, p_ % page, kv])
+            mx = max(xs)
+            es = [math.exp(x - mx) for x in xs]
+            tot = sum(es)
+            ob = [sum(es[t] * vs[t][c] for t in range(len(xs))) / tot for c in range(d)]
+            assert np.allclose(O[cu[b] + i, hq], ob, atol=1e-12)
+            assert abs(L[cu[b] + i, hq] - (mx + math.log(tot))) < 1e-12
+    # without the mask every query of a row sees all of its keys
+    On, Ln = A.prefill_paged_ref(q, kc, vc, table, cu, s_lens, scale, causal=False)
+    Od, Ld = A.decode_paged_ref(q[cu[2]:cu[2] + 1], kc, vc, table[2:3], [s_lens[2]], scale)
+    assert np.allclose(On[cu[2]], Od[0], atol=1e-12) and np.allclose(Ln[cu[2]], Ld[0], atol=1e-12)
+
+
 ALL_PINS = [
     pin_worked_example,
     pin_max_jump_rescale,
@@ -377,4 +440,5 @@ ALL_PINS = [
     pin_library_sdpa,
     pin_merge_partials,
     pin_merge_lse_pair,
+    pin_paged_prefill,
 ]

@@ -128,6 +128,36 @@ def _decode_slot_swapped(q, k_cache, v_cache, block_table, seq_lens, scale):
     return O, L
 
 
+def _paged_variant(top_left=False, ignore_mask=False):
+    """prefill_paged_ref with the queries aligned to the first key positions,
+    or with the causal mask ignored."""
+    def prefill_paged_ref(q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens, scale,
+                          causal=True, tokens=None):
+        q64 = A.to_f64(q)
+        table = np.asarray(block_table)
+        cu = list(np.asarray(cu_seqlens_q))
+        lens = list(np.asarray(seq_lens))
+        total_q, h, _ = q64.shape
+        h_kv = k_cache.shape[2]
+        g = h // h_kv
+        O = np.zeros((total_q, h, v_cache.shape[3]))
+        L = np.full((total_q, h), -np.inf)
+        for b in range(len(lens)):
+            t0, t1, s_ = int(cu[b]), int(cu[b + 1]), int(lens[b])
+            ql = t1 - t0
+            if ql == 0:
+                continue
+            K, V = A._gather_row(k_cache, v_cache, table[b], s_)
+            pos = np.arange(ql) if top_left else s_ - ql + np.arange(ql)
+            allowed = (np.arange(s_)[None, :] <= pos[:, None]) if (causal and not ignore_mask) \
+                else np.ones((ql, s_), bool)
+            for hq in range(h):
+                S = scale * (q64[t0:t1, hq] @ K[hq // g].T)
+                O[t0:t1, hq], L[t0:t1, hq] = A._softmax_rows_times_v(S, allowed, V[hq // g])
+        return O, L
+    return prefill_paged_ref
+
+
 MUTANTS = {
     # name: (attribute patches, pin expected to fail)
     "accumulator_not_rescaled": ({"online_softmax_attention": _online_variant(rescale_acc=False)},
@@ -149,6 +179,10 @@ MUTANTS = {
                                     pins.pin_merge_partials),
     "pair_merge_unweighted": ({"merge_lse_pair_ref": _merge_pair_unweighted}, pins.pin_merge_lse_pair),
     "page_and_slot_swapped": ({"decode_paged_ref": _decode_slot_swapped}, pins.pin_brute_force_decode),
+    "paged_queries_top_left": ({"prefill_paged_ref": _paged_variant(top_left=True)},
+                               pins.pin_paged_prefill),
+    "paged_mask_ignored": ({"prefill_paged_ref": _paged_variant(ignore_mask=True)},
+                           pins.pin_paged_prefill),
 }
 
 
