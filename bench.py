@@ -447,6 +447,7 @@ def run_gpu(args, world, rank, local):
 
     # ---- pairwise (O, LSE) merge (prefix / suffix combine), outside the step ----
     merge_pair = measure_merge_pair(dev, flush, hbm_peak, peak_kind) if args.only is None else None
+    prefill_paged = measure_prefill_paged(dev, flush, tc_peak, peak_kind) if args.only is None else None
 
     # ---- CPU oracle baseline (rank 0, N = 1 only) ----
     cpu = None
@@ -514,6 +515,7 @@ def run_gpu(args, world, rank, local):
             "adaptive": adaptive,
         },
         "merge_pair": merge_pair,
+        "prefill_paged": prefill_paged,
         "prefill_ms": pre_avg,
         "e2e": e2e,
         "cpu_baseline": cpu,
@@ -522,6 +524,49 @@ def run_gpu(args, world, rank, local):
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)
+
+
+def measure_prefill_paged(dev, flush, tc_peak, peak_kind, iters=10):
+    """Chunked prefill over a paged cache: 8 rows, each with its last 1024
+    positions as new queries over an 8192-key context (h=32, h_kv=8, d_h=128,
+    Q and K x3 as in the main prefill workload). TFLOP/s of allowed pairs,
+    L2 flushed before each call."""
+    import online_softmax_attn_gb300 as attn
+
+    B, qn, ctx = 8, 1024, PREFILL.T
+    h, h_kv, d = PREFILL.h, PREFILL.h_kv, PREFILL.d_h
+    table, nblk = W.paged_layout([ctx] * B, seed=11)
+    q = W.normal((B * qn, h, d), 31, torch.bfloat16, dev, PREFILL.qk_mult)
+    kc = W.normal((nblk, W.PAGE_SIZE, h_kv, d), 32, torch.bfloat16, dev, PREFILL.qk_mult)
+    vc = W.normal((nblk, W.PAGE_SIZE, h_kv, d), 33, torch.bfloat16, dev)
+    cu = torch.arange(0, (B + 1) * qn, qn, dtype=torch.int32, device=dev)
+    seq = torch.full((B,), ctx, dtype=torch.int32, device=dev)
+    table = table.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((B * qn, h), dtype=torch.float32, device=dev)
+    ws = torch.empty(256 + 4 * (B + 1), dtype=torch.uint8, device=dev)
+    call = lambda: attn.attn_prefill_paged(q, kc, vc, table, cu, seq, qn, True, PREFILL.scale,
+                                           workspace=ws, o=o, lse=lse)
+    for _ in range(3):
+        call()
+    ms = []
+    for _ in range(iters):
+        flush.fill_(1)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        call()
+        b.record()
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    t = statistics.median(ms)
+    pairs = B * sum(ctx - qn + i + 1 for i in range(qn))
+    flops = 4.0 * h * d * pairs
+    tf = flops / (t * 1e-3) / 1e12
+    return {"value": tf, "unit": "TFLOP/s", "ms": t, "rows": B, "queries_per_row": qn, "context": ctx,
+            "flops": flops,
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": tc_peak, "unit": "TFLOP/s",
+                         "frac": tf / tc_peak, "traffic": None, "kernel": "prefill_bf16_kernel (paged)",
+                         "peak_source": f"{peak_kind} bf16 burst"}}
 
 
 def measure_merge_pair(dev, flush, hbm_peak, peak_kind, iters=20):

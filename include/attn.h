@@ -117,6 +117,54 @@ attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o,
                            void* stream);
 
 /*
+ * attn_prefill_paged -- exact attention for a batch of variable-length query
+ * rows over a paged KV cache (chunked prefill, and mixed batches of prefill
+ * and decode rows). Row b has the q_len_b = cu_seqlens_q[b+1] - cu_seqlens_q[b]
+ * query tokens cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 of q, and keys
+ * 0 .. seq_lens[b]-1 in the cache through block_table row b ([DEC] paged
+ * addressing); its queries are its last q_len_b key positions, so with causal
+ * query i sees keys up to seq_lens[b] - q_len_b + i (bottom-right alignment;
+ * the pages leave unequal lengths open and this is the chunked-prefill
+ * reading); without causal it sees all seq_lens[b] keys. Method as
+ * attn_prefill ([NA] (3), "Extending the recurrence to the output"), on the
+ * tcgen05 kernel with key tiles gathered page by page; P V uses the exact
+ * two-term bf16 P (the cache stays bf16).
+ *
+ *   q            [total_q, h, d_h] bf16, rows packed back to back    (read)
+ *   k_cache,
+ *   v_cache      [num_blocks, page_size, h_kv, d_h] bf16                (read)
+ *   block_table  [B, max_blocks_per_seq] int32                          (read)
+ *   cu_seqlens_q [B + 1] int32, cu_seqlens_q[0] = 0, non-decreasing,
+ *                cu_seqlens_q[B] = total_q                              (read)
+ *   seq_lens     [B] int32, q_len_b <= seq_lens[b] <= max_blocks_per_seq *
+ *                page_size                                              (read)
+ *   max_q_len    host bound on every q_len_b (sizes the grid)
+ *   workspace    attn_prefill_paged_workspace_bytes(B) bytes, 256-byte
+ *                aligned (per-row tile offsets), overwritten by the call
+ *   o            [total_q, h, d_h] bf16                                 (written)
+ *   lse          [total_q, h] fp32, natural log, may be NULL             (written)
+ * All tensor arguments are device pointers. Device-side problems set bits in
+ * the error word instead of faulting: a block-table entry outside the cache
+ * (ATTN_DEVERR_BAD_PAGE; that page reads as zeros), seq_lens outside
+ * [q_len_b, max_blocks_per_seq * page_size] or q_len_b outside
+ * [0, max_q_len] (ATTN_DEVERR_BAD_SEQ_LEN; the length is clamped, or the
+ * row is skipped and its outputs are not written).
+ * Errors: INVALID_ARG for NULL or misaligned pointers (16 bytes for q, the
+ * caches and o; 4 for the int32 arrays and lse), B < 0, total_q < 0,
+ * max_q_len < 1 with total_q > 0, h < 1, h > 65535, h % h_kv != 0,
+ * num_blocks < 1, max_blocks_per_seq < 1, scale not finite and > 0, a small
+ * workspace; UNSUPPORTED for d_h other than 64 / 128 or page_size != 16.
+ * B == 0 or total_q == 0 is a no-op.
+ */
+size_t attn_prefill_paged_workspace_bytes(int B);
+attn_status_t attn_prefill_paged(const void* q, const void* k_cache, const void* v_cache,
+                                 const int32_t* block_table, const int32_t* cu_seqlens_q,
+                                 const int32_t* seq_lens, int B, int total_q, int h, int h_kv,
+                                 int d_h, int page_size, int num_blocks, int max_blocks_per_seq,
+                                 int max_q_len, int causal, float scale, void* workspace,
+                                 size_t workspace_bytes, void* o, float* lse, void* stream);
+
+/*
  * attn_decode_split_plan -- how one row's keys are cut into splits.
  * Follows [DEC] "Segment length, and the early exit": a row of seq_len keys
  * has n_pages = ceil(seq_len / page_size) pages; with at most num_splits

@@ -63,6 +63,10 @@ def library() -> ctypes.CDLL:
     lib.attn_prefill_workspace_bytes.restype = S
     lib.attn_prefill.argtypes = [P, P, P, P, P, I, I, I, I, I, F, I, P, S, P]
     lib.attn_prefill.restype = I
+    lib.attn_prefill_paged_workspace_bytes.argtypes = [I]
+    lib.attn_prefill_paged_workspace_bytes.restype = S
+    lib.attn_prefill_paged.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, F, P, S, P, P, P]
+    lib.attn_prefill_paged.restype = I
     lib.attn_decode_split_plan.argtypes = [I, I, I, ctypes.POINTER(I)]
     lib.attn_decode_split_plan.restype = I
     lib.attn_recommended_splits.argtypes = [I, I, I, Z, I]
@@ -156,6 +160,42 @@ def attn_prefill(q, k, v, causal: bool, scale: float | None = None, o=None, lse=
                                 int(bool(causal)), scale, dt, _ptr(workspace), ws_bytes,
                                 _stream(stream))
     _check("attn_prefill", st)
+    return o, lse
+
+
+def attn_prefill_paged(q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens, max_q_len: int,
+                       causal: bool = True, scale: float | None = None, workspace=None, o=None,
+                       lse=None, return_lse: bool = True, stream=None):
+    """Variable-length query rows over a paged cache. q [total_q, h, d] bf16
+    (rows packed back to back), caches [num_blocks, 16, h_kv, d] bf16,
+    block_table [B, max_blocks] int32, cu_seqlens_q [B+1] int32, seq_lens [B]
+    int32 (all CUDA). Row b's queries are its last q_len_b key positions.
+    Returns (o [total_q, h, d] bf16, lse [total_q, h] fp32 or None)."""
+    for t in (q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens):
+        _need(t.is_cuda and t.is_contiguous(), "tensors must be contiguous CUDA tensors")
+    _need(q.dtype == k_cache.dtype == v_cache.dtype == torch.bfloat16, "q and caches must be bf16")
+    _need(block_table.dtype == cu_seqlens_q.dtype == seq_lens.dtype == torch.int32,
+          "block_table, cu_seqlens_q and seq_lens must be int32")
+    total_q, h, d = q.shape
+    nb, page, h_kv, d2 = k_cache.shape
+    _need(d2 == d and v_cache.shape == k_cache.shape, "cache shape mismatch")
+    B = seq_lens.shape[0]
+    _need(cu_seqlens_q.shape == (B + 1,) and block_table.dim() == 2 and block_table.shape[0] == B,
+          "cu_seqlens_q [B+1], block_table [B, max_blocks] and seq_lens [B] expected")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if workspace is None:
+        workspace = torch.empty(max(library().attn_prefill_paged_workspace_bytes(B), 256),
+                                dtype=torch.uint8, device=q.device)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((total_q, h), dtype=torch.float32, device=q.device)
+    st = library().attn_prefill_paged(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(cu_seqlens_q), _ptr(seq_lens),
+        B, total_q, h, h_kv, d, page, nb, block_table.shape[1], int(max_q_len), int(bool(causal)),
+        scale, _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(o), _ptr(lse),
+        _stream(stream))
+    _check("attn_prefill_paged", st)
     return o, lse
 
 

@@ -189,6 +189,55 @@ attn_status_t decode_paged_impl(const void* q, const void* k_cache, const void* 
 }
 }  // namespace
 
+size_t attn_prefill_paged_workspace_bytes(int B) {
+  if (B < 0) return 0;
+  return align256(size_t(B + 1) * sizeof(int32_t));
+}
+
+attn_status_t attn_prefill_paged(const void* q, const void* k_cache, const void* v_cache,
+                                 const int32_t* block_table, const int32_t* cu_seqlens_q,
+                                 const int32_t* seq_lens, int B, int total_q, int h, int h_kv,
+                                 int d_h, int page_size, int num_blocks, int max_blocks_per_seq,
+                                 int max_q_len, int causal, float scale, void* workspace,
+                                 size_t workspace_bytes, void* o, float* lse, void* stream) {
+  if (B < 0 || total_q < 0 || h < 1 || h > 65535 || h_kv < 1 || h % h_kv != 0 ||
+      num_blocks < 1 || max_blocks_per_seq < 1 || !std::isfinite(scale) || !(scale > 0.f))
+    return ATTN_ERR_INVALID_ARG;
+  if ((d_h != 64 && d_h != 128) || page_size != 16) return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(max_blocks_per_seq) * page_size > (1ll << 30))
+    return ATTN_ERR_INVALID_ARG;
+  if (B == 0 || total_q == 0) return ATTN_OK;
+  if (max_q_len < 1) return ATTN_ERR_INVALID_ARG;
+  if (!q || !k_cache || !v_cache || !block_table || !cu_seqlens_q || !seq_lens || !workspace || !o)
+    return ATTN_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(o, 16) ||
+      !aligned(block_table, 4) || !aligned(cu_seqlens_q, 4) || !aligned(seq_lens, 4) ||
+      !aligned(lse, 4) || !aligned(workspace, 256))
+    return ATTN_ERR_INVALID_ARG;
+  if (workspace_bytes < attn_prefill_paged_workspace_bytes(B)) return ATTN_ERR_INVALID_ARG;
+  PagedPrefill a;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_table = block_table;
+  a.cu_q = cu_seqlens_q;
+  a.seq_lens = seq_lens;
+  a.tile_off = static_cast<int32_t*>(workspace);
+  a.B = B;
+  a.total_q = total_q;
+  a.h = h;
+  a.h_kv = h_kv;
+  a.d_h = d_h;
+  a.num_blocks = num_blocks;
+  a.max_blocks = max_blocks_per_seq;
+  a.max_q_len = max_q_len;
+  a.causal = causal != 0;
+  a.scale = scale;
+  a.o = o;
+  a.lse = lse;
+  return from_cuda(launch_prefill_paged(a, static_cast<cudaStream_t>(stream)));
+}
+
 attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* v_cache,
                                 const int32_t* block_table, const int32_t* seq_lens, int B, int h,
                                 int h_kv, int d_h, int page_size, int num_blocks,

@@ -81,6 +81,21 @@ PrefillLayout prefill_layout(int T, int h_kv, int d_h);
 cudaError_t launch_prefill_bf16(const void* q, const void* k, const void* v, void* o, float* lse,
                                 int T, int h, int h_kv, int d_h, int causal, float scale,
                                 void* workspace, cudaStream_t stream);
+// Paged, variable-length prefill (arguments validated by the caller).
+struct PagedPrefill {
+  const void* q;            // [total_q, h, d_h] bf16
+  const void* k_cache;      // [num_blocks, 16, h_kv, d_h] bf16
+  const void* v_cache;
+  const int32_t* block_table;  // [B, max_blocks]
+  const int32_t* cu_q;         // [B + 1]
+  const int32_t* seq_lens;     // [B]
+  int32_t* tile_off;           // [B + 1] workspace
+  int B, total_q, h, h_kv, d_h, num_blocks, max_blocks, max_q_len, causal;
+  float scale;
+  void* o;                     // [total_q, h, d_h] bf16
+  float* lse;                  // [total_q, h] or nullptr
+};
+cudaError_t launch_prefill_paged(const PagedPrefill& a, cudaStream_t stream);
 unsigned int prefill_read_and_clear_error(cudaStream_t stream, cudaError_t* st);
 
 // tensor maps ---------------------------------------------------------------

@@ -163,14 +163,27 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
   }
 }
 
-template <int D, int NQ, int NSK, int NSV>
+// Paged, variable-length rows (PAGED kernels): queries are packed token-major
+// [total_q, h, d_h]; row b's queries are tokens cu_q[b] .. cu_q[b+1]-1 and
+// sit at the last q_len positions of its seq_lens[b] keys, which live in the
+// paged cache [num_blocks, 16, h_kv, d_h] through block_table row b.
+// tile_off[b] is row b's first 128-query tile (tile_off[B]: all tiles).
+struct PagedArgs {
+  const int32_t* block_table;
+  const int32_t* cu_q;
+  const int32_t* seq_lens;
+  const int32_t* tile_off;
+  int B, max_blocks, num_blocks;
+};
+
+template <int D, int NQ, int NSK, int NSV, bool PAGED>
 __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
     prefill_bf16_kernel(const __grid_constant__ CUtensorMap tmap_q,
                         const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v,
                         const __grid_constant__ CUtensorMap tmap_v16,
                         const int* __restrict__ vwide, __nv_bfloat16* __restrict__ o, float* __restrict__ lse, int T, int h,
-                        int h_kv, int causal, float scale_log2, int n_qblk) {
+                        int h_kv, int causal, float scale_log2, int n_qblk, const PagedArgs pa) {
   using C = PfCfg<D, NQ, NSK, NSV>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -182,11 +195,38 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int qb = causal ? (n_qblk - 1 - int(blockIdx.x)) : int(blockIdx.x);
   const int hq0 = blockIdx.y * NQ;
   const int kvh = hq0 / (h / h_kv);
-  const int n_kv_all = (T + kBN - 1) / kBN;
-  const int nkv = causal ? min(qb + 1, n_kv_all) : n_kv_all;
+  int qb, nkv, n_kv_all;
+  // Paged rows: the row, its first query token, query count and key count.
+  int pb = 0, q_tok0 = 0, q_len = 0, ctx = 0, n_pages = 0;
+  if constexpr (PAGED) {
+    const int tile = int(blockIdx.x);
+    if (tile >= pa.tile_off[pa.B]) return;  // surplus CTA of the fixed grid
+    int lo = 0, hi = pa.B - 1;              // last row whose first tile <= tile
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (pa.tile_off[mid] <= tile) lo = mid; else hi = mid - 1;
+    }
+    pb = lo;
+    qb = pa.tile_off[pb + 1] - 1 - tile;  // longest tile of the row first
+    q_tok0 = pa.cu_q[pb];
+    q_len = pa.cu_q[pb + 1] - q_tok0;
+    ctx = pa.seq_lens[pb];
+    if (ctx < q_len || ctx > pa.max_blocks * 16) {
+      if (threadIdx.x == 0) atomicOr(&g_prefill_err, ATTN_DEVERR_BAD_SEQ_LEN);
+      ctx = ctx < q_len ? q_len : pa.max_blocks * 16;
+    }
+    n_pages = (ctx + 15) / 16;
+    const int q_hi = min(qb * kBM + kBM, q_len);  // end of this tile's queries
+    const int key_end = causal ? ctx - q_len + q_hi : ctx;
+    nkv = (key_end + kBN - 1) / kBN;
+    n_kv_all = nkv;
+  } else {
+    qb = causal ? (n_qblk - 1 - int(blockIdx.x)) : int(blockIdx.x);
+    n_kv_all = (T + kBN - 1) / kBN;
+    nkv = causal ? min(qb + 1, n_kv_all) : n_kv_all;
+  }
   // Per key tile of this KV head: nonzero -> V stays bf16 (exact P_hi + P_lo
   // product); zero -> V is read from its fp16 copy (fp16 P). No flags: all
   // tiles bf16.
@@ -222,26 +262,60 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
       if (tile_wide) prefetch_tmap(&tmap_v16);
       mbar_arrive_expect_tx(bars.q_full(), NQ * C::QTILE);
       for (int t = 0; t < NQ; ++t)
-        for (int s = 0; s < C::SUBS; ++s)
-          tma_load_3d(sbase + C::Q_OFF + t * C::QTILE + s * C::SUB_BYTES, &tmap_q, bars.q_full(),
-                      s * 64, qb * kBM, hq0 + t);
+        for (int s = 0; s < C::SUBS; ++s) {
+          if constexpr (PAGED)
+            tma_load_3d(sbase + C::Q_OFF + t * C::QTILE + s * C::SUB_BYTES, &tmap_q, bars.q_full(),
+                        s * 64, hq0 + t, q_tok0 + qb * kBM);
+          else
+            tma_load_3d(sbase + C::Q_OFF + t * C::QTILE + s * C::SUB_BYTES, &tmap_q, bars.q_full(),
+                        s * 64, qb * kBM, hq0 + t);
+        }
+      // Paged rows: the 8 pages of key tile j (a page past the row's end, or
+      // an invalid entry, is read at coordinate -1 and arrives as zeros).
+      int pg[8];
+      auto fetch_pages = [&](int j) {
+        if constexpr (PAGED) {
+#pragma unroll
+          for (int p = 0; p < 8; ++p) {
+            const int page = j * 8 + p;
+            int phys = -1;
+            if (page < n_pages) {
+              phys = pa.block_table[size_t(pb) * pa.max_blocks + page];
+              if (phys < 0 || phys >= pa.num_blocks) {
+                atomicOr(&g_prefill_err, ATTN_DEVERR_BAD_PAGE);
+                phys = -1;
+              }
+            }
+            pg[p] = phys;
+          }
+        }
+      };
+      auto load_tile = [&](uint32_t dst, const CUtensorMap* map, uint32_t bar, int j) {
+        if constexpr (PAGED) {
+#pragma unroll
+          for (int s = 0; s < C::SUBS; ++s)
+#pragma unroll
+            for (int p = 0; p < 8; ++p)
+              tma_load_4d(dst + s * C::SUB_BYTES + p * 16 * 128, map, bar, s * 64, kvh, 0, pg[p]);
+        } else {
+          for (int s = 0; s < C::SUBS; ++s)
+            tma_load_3d(dst + s * C::SUB_BYTES, map, bar, s * 64, j * kBN, kvh);
+        }
+      };
       // K and V have rings of their own: a K stage frees as soon as the last
       // head's S MMA on it completes, a V stage after the last P V MMA.
       int k_issued = 0, v_issued = 0;
       for (int j = 0; j < nkv; ++j) {
         const int sk = j % NSK, sv = j % NSV;
+        fetch_pages(j);
         if (j >= NSK && !wait_or_abort(bars.k_empty(sk), ((j / NSK) - 1) & 1, abort_flag)) break;
         mbar_arrive_expect_tx(bars.k_full(sk), C::KTILE);
-        for (int s = 0; s < C::SUBS; ++s)
-          tma_load_3d(sbase + C::K_OFF + sk * C::KTILE + s * C::SUB_BYTES, &tmap_k,
-                      bars.k_full(sk), s * 64, j * kBN, kvh);
+        load_tile(sbase + C::K_OFF + sk * C::KTILE, &tmap_k, bars.k_full(sk), j);
         k_issued = j + 1;
         if (j >= NSV && !wait_or_abort(bars.v_empty(sv), ((j / NSV) - 1) & 1, abort_flag)) break;
         mbar_arrive_expect_tx(bars.v_full(sv), C::KTILE);
         const CUtensorMap* vmap = is_wide(j) ? &tmap_v : &tmap_v16;
-        for (int s = 0; s < C::SUBS; ++s)
-          tma_load_3d(sbase + C::V_OFF + sv * C::KTILE + s * C::SUB_BYTES, vmap,
-                      bars.v_full(sv), s * 64, j * kBN, kvh);
+        load_tile(sbase + C::V_OFF + sv * C::KTILE, vmap, bars.v_full(sv), j);
         v_issued = j + 1;
       }
       if (*abort_flag) {
@@ -347,8 +421,12 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
     const int t = warp >> 2;
     const int wq = warp & 3;
     const int r = wq * 32 + lane;
-    const int row = qb * kBM + r;
+    const int row = qb * kBM + r;  // query index within the row (paged) or the sequence
     const int hq = hq0 + t;
+    // Paged rows: keys [0, key_end) are visible to this query (none for the
+    // padding rows of a row's last tile).
+    const bool row_valid = PAGED ? row < q_len : row < T;
+    const int key_end = !PAGED ? 0 : (!row_valid ? 0 : (causal ? ctx - q_len + row + 1 : ctx));
     const uint32_t tS = tmem + (uint32_t(wq * 32) << 16) + t * 256;
     const uint32_t tO = tS + 128;
     // m_ref: exp2-domain reference that l, O~ and this tile's P are relative
@@ -367,8 +445,12 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
       }
       tc::fence_after();
       int lim = kBN;
-      if (j * kBN + kBN > T) lim = T - j * kBN;
-      if (causal && j == qb) lim = min(lim, r + 1);
+      if constexpr (PAGED) {
+        lim = min(kBN, key_end - j * kBN);
+      } else {
+        if (j * kBN + kBN > T) lim = T - j * kBN;
+        if (causal && j == qb) lim = min(lim, r + 1);
+      }
       const uint64_t c2 = f2(scale_log2, scale_log2);
       uint32_t sr[4][32];
 #pragma unroll
@@ -518,13 +600,14 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
       tc::fence_after();
       const bool empty = !(l > 0.f);
       const float inv = empty ? 0.f : 1.f / l;
-      __nv_bfloat16* orow = o + (size_t(hq) * T + row) * D;
+      const size_t orow_idx = PAGED ? size_t(q_tok0 + row) * h + hq : size_t(hq) * T + row;
+      __nv_bfloat16* orow = o + orow_idx * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t ov[32];
         tc::ld32(tO + c * 32, ov);
         tc::wait_ld();
-        if (row < T) {
+        if (row_valid) {
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             uint4 pk;
@@ -536,8 +619,8 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
           }
         }
       }
-      if (row < T && lse != nullptr)
-        lse[size_t(hq) * T + row] = empty ? -INFINITY : (m_ref + log2f(l)) * kLn2;
+      if (row_valid && lse != nullptr)
+        lse[orow_idx] = empty ? -INFINITY : (m_ref + log2f(l)) * kLn2;
     }
   }
 
@@ -610,14 +693,79 @@ cudaError_t launch(const void* q, const void* k, const void* v, const void* v16,
                           CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  auto kern = prefill_bf16_kernel<D, NQ, NSK, NSV>;
+  auto kern = prefill_bf16_kernel<D, NQ, NSK, NSV, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   const int n_qblk = (T + kBM - 1) / kBM;
   const dim3 grid(n_qblk, h / NQ);
   kern<<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tv16, v16 ? vwide : nullptr,
                                                static_cast<__nv_bfloat16*>(o), lse, T, h, h_kv,
-                                               causal, scale * kLog2e, n_qblk);
+                                               causal, scale * kLog2e, n_qblk, PagedArgs{});
+  return cudaGetLastError();
+}
+
+// Row b's query tiles: tile_off[b+1] = tile_off[b] + ceil(q_len_b / 128). A
+// query count below 0 or above max_q_len (the grid's bound) is an error:
+// that row gets no tiles and its outputs are not written.
+__global__ void paged_tiles_kernel(const int32_t* __restrict__ cu_q, int B, int max_q_len,
+                                   int32_t* __restrict__ tile_off) {
+  if (threadIdx.x != 0) return;
+  int acc = 0;
+  tile_off[0] = 0;
+  for (int b = 0; b < B; ++b) {
+    int n = cu_q[b + 1] - cu_q[b];
+    if (n < 0 || n > max_q_len) {
+      atomicOr(&g_prefill_err, ATTN_DEVERR_BAD_SEQ_LEN);
+      n = 0;
+    }
+    acc += (n + kBM - 1) / kBM;
+    tile_off[b + 1] = acc;
+  }
+}
+
+template <int D, int NQ, int NSK, int NSV>
+cudaError_t launch_paged(const PagedPrefill& a, cudaStream_t stream) {
+  using C = PfCfg<D, NQ, NSK, NSV>;
+  CUtensorMap tq, tk, tv;
+  {
+    // Q and O token-major [total_q, h, d_h]: a 128-token box of one head.
+    const uint64_t dims[3] = {uint64_t(D), uint64_t(a.h), uint64_t(a.total_q)};
+    const uint64_t strides[2] = {uint64_t(D) * 2, uint64_t(a.h) * D * 2};
+    const uint32_t box[3] = {64u, 1u, 128u};
+    if (encode_tensor_map(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.q), dims,
+                          strides, box, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    // Cache [num_blocks, 16, h_kv, d_h]: one page of one KV head per box.
+    const uint64_t dims[4] = {uint64_t(D), uint64_t(a.h_kv), 16u, uint64_t(a.num_blocks)};
+    const uint64_t strides[3] = {uint64_t(D) * 2, uint64_t(a.h_kv) * D * 2,
+                                 uint64_t(16) * a.h_kv * D * 2};
+    const uint32_t box[4] = {64u, 1u, 16u, 1u};
+    if (encode_tensor_map(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(a.k_cache),
+                          dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+    if (encode_tensor_map(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(a.v_cache),
+                          dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  paged_tiles_kernel<<<1, 32, 0, stream>>>(a.cu_q, a.B, a.max_q_len, a.tile_off);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  auto kern = prefill_bf16_kernel<D, NQ, NSK, NSV, true>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  // At most one partial tile per row beyond ceil(total_q / 128), and no row
+  // has more than ceil(max_q_len / 128) tiles.
+  const long long by_total = (static_cast<long long>(a.total_q) + kBM - 1) / kBM + a.B;
+  const long long by_row = static_cast<long long>(a.B) * ((a.max_q_len + kBM - 1) / kBM);
+  const long long tiles = by_total < by_row ? by_total : by_row;
+  if (tiles <= 0) return cudaSuccess;
+  const dim3 grid(static_cast<unsigned>(tiles), a.h / NQ);
+  PagedArgs pa{a.block_table, a.cu_q, a.seq_lens, a.tile_off, a.B, a.max_blocks, a.num_blocks};
+  kern<<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tv, nullptr,
+                                               static_cast<__nv_bfloat16*>(a.o), a.lse, 0, a.h,
+                                               a.h_kv, a.causal, a.scale * kLog2e, 0, pa);
   return cudaGetLastError();
 }
 
@@ -655,6 +803,13 @@ cudaError_t launch_prefill_bf16(const void* q, const void* k, const void* v, voi
   }
   return pair ? launch<64, 2, 4, 4>(q, k, v, v16, vwide, o, lse, T, h, h_kv, causal, scale, stream)
               : launch<64, 1, 4, 4>(q, k, v, v16, vwide, o, lse, T, h, h_kv, causal, scale, stream);
+}
+
+cudaError_t launch_prefill_paged(const PagedPrefill& a, cudaStream_t stream) {
+  const bool pair = ((a.h / a.h_kv) % 2) == 0;
+  if (a.d_h == 128)
+    return pair ? launch_paged<128, 2, 2, 3>(a, stream) : launch_paged<128, 1, 3, 3>(a, stream);
+  return pair ? launch_paged<64, 2, 4, 4>(a, stream) : launch_paged<64, 1, 4, 4>(a, stream);
 }
 
 unsigned int prefill_read_and_clear_error(cudaStream_t stream, cudaError_t* st) {
