@@ -48,7 +48,10 @@ KERNEL_FILES = {
 }
 NCU_TRAFFIC = {
     # kind: (dram read + write bytes per launch, sha256[:16] of the kernel's files)
-    "prefill": (131.63e6, "3fcea0a47caa1b48"),  # profiles/prefill_bf16_T8192_causal.md
+    "prefill": (131.79e6, "4a27b205c4361958"),  # profiles/prefill_bf16_T8192_causal.md
+    # decode: 16-row capture (303.9 MB for 299.5 MB algorithmic) scaled by KV bytes to the
+    # 66-row batch (profiles/decode_split_paged_B16.md)
+    "decode": (2.1514e9, "2dcc49156d4ec784"),
 }
 
 
@@ -400,7 +403,7 @@ def run_gpu(args, world, rank, local):
 
     # ---- deterministic decode (fixed 2048-key splits) on the same batch, outside the step ----
     det = None
-    if args.only is None:
+    if args.only is None and not args.no_extras:
         pps = 128
         det_splits = -(-table.shape[1] // pps)
         det_ws = torch.empty(attn.attn_decode_workspace_bytes(B, DECODE.h, DECODE.d_h, det_splits),
@@ -423,7 +426,7 @@ def run_gpu(args, world, rank, local):
 
     # ---- adaptive decode (split count planned on the device, grid of 32), outside the step ----
     adaptive = None
-    if args.only is None:
+    if args.only is None and not args.no_extras:
         amax = 32
         ad_ws = torch.empty(attn.attn_decode_adaptive_workspace_bytes(B, DECODE.h, DECODE.d_h, amax),
                             dtype=torch.uint8, device=dev)
@@ -446,8 +449,9 @@ def run_gpu(args, world, rank, local):
                     "frac_of_hbm": db / (at * 1e-3) / 1e9 / hbm_peak}
 
     # ---- pairwise (O, LSE) merge (prefix / suffix combine), outside the step ----
-    merge_pair = measure_merge_pair(dev, flush, hbm_peak, peak_kind) if args.only is None else None
-    prefill_paged = measure_prefill_paged(dev, flush, tc_peak, peak_kind) if args.only is None else None
+    extras = args.only is None and not args.no_extras
+    merge_pair = measure_merge_pair(dev, flush, hbm_peak, peak_kind) if extras else None
+    prefill_paged = measure_prefill_paged(dev, flush, tc_peak, peak_kind) if extras else None
 
     # ---- CPU oracle baseline (rank 0, N = 1 only) ----
     cpu = None
@@ -613,6 +617,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=16.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the measurements outside the step (deterministic / adaptive decode, "
+                         "pair merge, paged prefill), e.g. for a launch list of the step alone")
     ap.add_argument("--only", choices=["prefill", "decode"], default=None,
                     help="run one half of the step (profiler captures; not a bench line)")
     ap.add_argument("--decode-rows", type=int, default=0,
