@@ -10,11 +10,11 @@
 // any common shift is legal ("The state that gets passed around is the
 // log-sum-exp") licenses the reference used here: l, O~ and each tile's
 // weights P share one exp2-domain reference m_ref, which need not be the row
-// max. A tile is exponentiated against the reference of the tiles before it
-// (no row max on the common path); only the first tile, or one whose weights
-// would leave fp16's range, takes its row max first. The reference rises by
-// log2 of a tile's weight sum once that sum passes 2^10, so O~ is rescaled
-// rarely; O = O~ / l and LSE are independent of the reference.
+// max. Every tile takes its row max; the reference moves only when that max
+// passes it by more than 15 (weights then still fit fp16), and it moves to 8
+// above the max, so O~ is rescaled rarely; the rescale runs after P is
+// stored, in the registers S held. O = O~ / l and LSE are independent of the
+// reference.
 //
 // GB300 design (one CTA per (KV head, 128-query block, pair of query heads)):
 //   * softmax warpgroups (warps 0-3, 4-7), one per query head; thread = row
@@ -48,10 +48,16 @@ namespace {
 
 constexpr int kBM = 128;  // query rows per tile (tensor-memory lanes)
 constexpr int kBN = 128;  // keys per tile
-// The reference moves to the row max only when that exceeds it by more than
-// this (log2 units): weights stay at most 2^15, below fp16's largest finite
-// value (65504).
+// The reference moves only when the row max exceeds it by more than this (log2
+// units): weights stay at most 2^15, below fp16's largest finite value (65504).
 constexpr float kRescaleBits = 15.0f;
+// When it moves, the reference goes this far above the row max, so the max
+// may grow by kRescaleBits + kRefHeadroom before the next move (on logits with
+// a standard deviation of 9 that cuts the 32-row warps that move per tile from
+// about 23% to 6%). Weights under 2^-14 are then fp16 subnormals: absolute
+// error at most 2^-25 against a row sum of at least 2^-kRefHeadroom, i.e. at
+// most 2^-17 of the sum per key.
+constexpr float kRefHeadroom = 8.0f;
 
 template <int D, int NQ, int NSK, int NSV>
 struct PfCfg {
@@ -465,9 +471,9 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
       }
       // Row max: per 32-column chunk a tree of 3-input maxima (11 -> 4 -> 1),
       // then the four chunk maxima. Then the lazy reference rule: the
-      // reference moves to the row max only when that exceeds it by more than
-      // 2^15 (so every weight, at most 2^15, fits fp16); otherwise l and O~
-      // keep their scale.
+      // reference moves (to kRefHeadroom above the row max) only when the row
+      // max exceeds it by more than kRescaleBits, so every weight stays at
+      // most 2^15 and fits fp16; otherwise l and O~ keep their scale.
       float cm[4];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -483,32 +489,16 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
       const float m_cand = mx * scale_log2;
       float alpha = 1.f;
       if (m_cand > m_ref + kRescaleBits) {
-        alpha = ex2_approx(m_ref - m_cand);  // 0 on the first tile
+        const float m_new = m_cand + kRefHeadroom;
+        alpha = ex2_approx(m_ref - m_new);  // 0 on the first tile
         l *= alpha;
-        m_ref = m_cand;
+        m_ref = m_new;
       }
       // O~ holds the P V of tiles < j (complete: this tile's S was issued
-      // after them) and is scaled by alpha before this tile's P V adds to it,
-      // 32 columns at a time between the chunks of exponentials.
+      // after them) and is scaled by alpha before this tile's P V adds to it.
+      // That happens after P is stored, in the registers S occupied, so that
+      // the exponent loop carries no extra live state for it.
       const bool rescale = j > 0 && __any_sync(0xffffffffu, alpha != 1.f);
-      const uint64_t a2 = f2(alpha, alpha);
-      uint32_t ov[32];
-      auto o_load = [&](int c) {
-        if (rescale && c < D / 32) tc::ld32(tO + c * 32, ov);
-      };
-      auto o_store = [&](int c) {
-        if (rescale && c < D / 32) {
-          tc::wait_ld();
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            float x0, x1;
-            unf2(mul2(f2(__uint_as_float(ov[2 * i]), __uint_as_float(ov[2 * i + 1])), a2), x0, x1);
-            ov[2 * i] = __float_as_uint(x0);
-            ov[2 * i + 1] = __float_as_uint(x1);
-          }
-          tc::st32(tO + c * 32, ov);
-        }
-      };
       const float bias = (m_ref == -INFINITY) ? 0.f : m_ref;
       const uint64_t nb2 = f2(-bias, -bias);
       uint64_t sumA = f2(0.f, 0.f), sumB = f2(0.f, 0.f);
@@ -519,7 +509,6 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
         // were consumed at step i/2).
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          o_load(c);
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             float y0, y1;
@@ -531,7 +520,6 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
             if (i & 1) sumB = add2(sumB, f2(p0, p1)); else sumA = add2(sumA, f2(p0, p1));
             sr[c][i] = pack_f16x2(p0, p1);
           }
-          o_store(c);
         }
         uint32_t pw[32];
 #pragma unroll
@@ -551,7 +539,6 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
         // P_hi pair of keys (2i, 2i+1), sr[c][2i+1] for P_lo.
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          o_load(c);
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             float y0, y1;
@@ -571,7 +558,6 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
             sr[c][2 * i] = hi;
             sr[c][2 * i + 1] = pack_bf16x2(d0, d1);
           }
-          o_store(c);
         }
         // P_hi fills columns 0-63 and P_lo columns 64-127.
         uint32_t hi[32], lo[32];
@@ -586,6 +572,26 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
             }
           tc::st32(tS + 32 * half, hi);       // P_hi keys 64*half .. +63
           tc::st32(tS + 64 + 32 * half, lo);  // P_lo keys 64*half .. +63
+        }
+      }
+      if (rescale) {
+        // sr is free once P is stored (tcgen05.st reads its registers at
+        // issue): all of O~ at once, one load latency.
+        const uint64_t a2 = f2(alpha, alpha);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) tc::ld32(tO + c * 32, sr[c]);
+        tc::wait_ld();
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            float x0, x1;
+            unf2(mul2(f2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])), a2),
+                 x0, x1);
+            sr[c][2 * i] = __float_as_uint(x0);
+            sr[c][2 * i + 1] = __float_as_uint(x1);
+          }
+          tc::st32(tO + c * 32, sr[c]);
         }
       }
       float sa0, sa1;
