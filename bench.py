@@ -534,7 +534,7 @@ def measure_prefill_paged(dev, flush, tc_peak, peak_kind, iters=10):
     """Chunked prefill over a paged cache: 8 rows, each with its last 1024
     positions as new queries over an 8192-key context (h=32, h_kv=8, d_h=128,
     Q and K x3 as in the main prefill workload). TFLOP/s of allowed pairs,
-    L2 flushed before each call."""
+    L2 flushed before each call; the time includes the fp16 V copy."""
     import online_softmax_attn_gb300 as attn
 
     B, qn, ctx = 8, 1024, PREFILL.T
@@ -548,7 +548,10 @@ def measure_prefill_paged(dev, flush, tc_peak, peak_kind, iters=10):
     table = table.to(dev)
     o = torch.empty_like(q)
     lse = torch.empty((B * qn, h), dtype=torch.float32, device=dev)
-    ws = torch.empty(256 + 4 * (B + 1), dtype=torch.uint8, device=dev)
+    # The workspace with room for the fp16 V copy (the pre-pass that fills it
+    # runs inside every timed call).
+    ws = torch.empty(attn.attn_prefill_paged_workspace_bytes(B, table.shape[1], h_kv, d, v16=True),
+                     dtype=torch.uint8, device=dev)
     call = lambda: attn.attn_prefill_paged(q, kc, vc, table, cu, seq, qn, True, PREFILL.scale,
                                            workspace=ws, o=o, lse=lse)
     for _ in range(3):

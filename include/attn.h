@@ -127,8 +127,13 @@ attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o,
  * the pages leave unequal lengths open and this is the chunked-prefill
  * reading); without causal it sees all seq_lens[b] keys. Method as
  * attn_prefill ([NA] (3), "Extending the recurrence to the output"), on the
- * tcgen05 kernel with key tiles gathered page by page; P V uses the exact
- * two-term bf16 P (the cache stays bf16).
+ * tcgen05 kernel with key tiles gathered page by page. P V runs in one of two
+ * forms, as in attn_prefill: with the small workspace every V tile stays
+ * bf16 and takes the exact two-term bf16 P; with the larger one
+ * (attn_prefill_paged_v16_workspace_bytes) a pre-pass copies the pages each
+ * row uses into an fp16 buffer in the workspace, row by row, and a 128-key
+ * tile that converts exactly takes an fp16 P against it (one MMA instead of
+ * two); a tile holding |v| >= 2^16, inf or NaN keeps the bf16 path.
  *
  *   q            [total_q, h, d_h] bf16, rows packed back to back    (read)
  *   k_cache,
@@ -139,16 +144,21 @@ attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o,
  *   seq_lens     [B] int32, q_len_b <= seq_lens[b] <= max_blocks_per_seq *
  *                page_size                                              (read)
  *   max_q_len    host bound on every q_len_b (sizes the grid)
- *   workspace    attn_prefill_paged_workspace_bytes(B) bytes, 256-byte
- *                aligned (per-row tile offsets), overwritten by the call
+ *   workspace    at least attn_prefill_paged_workspace_bytes(B) bytes
+ *                (per-row tile offsets); with at least
+ *                attn_prefill_paged_v16_workspace_bytes(B,
+ *                max_blocks_per_seq, h_kv, d_h) bytes (when that is nonzero)
+ *                the fp16 V form is used. 256-byte aligned, device memory,
+ *                overwritten by the call
  *   o            [total_q, h, d_h] bf16                                 (written)
  *   lse          [total_q, h] fp32, natural log, may be NULL             (written)
  * All tensor arguments are device pointers. Device-side problems set bits in
  * the error word instead of faulting: a block-table entry outside the cache
  * (ATTN_DEVERR_BAD_PAGE; that page reads as zeros), seq_lens outside
  * [q_len_b, max_blocks_per_seq * page_size] or q_len_b outside
- * [0, max_q_len] (ATTN_DEVERR_BAD_SEQ_LEN; the length is clamped, or the
- * row is skipped and its outputs are not written).
+ * [0, min(max_q_len, max_blocks_per_seq * page_size)]
+ * (ATTN_DEVERR_BAD_SEQ_LEN; the length is clamped, or the row is skipped and
+ * its outputs are not written).
  * Errors: INVALID_ARG for NULL or misaligned pointers (16 bytes for q, the
  * caches and o; 4 for the int32 arrays and lse), B < 0, total_q < 0,
  * max_q_len < 1 with total_q > 0, h < 1, h > 65535, h % h_kv != 0,
@@ -157,6 +167,18 @@ attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o,
  * B == 0 or total_q == 0 is a no-op.
  */
 size_t attn_prefill_paged_workspace_bytes(int B);
+/*
+ * attn_prefill_paged_v16_workspace_bytes -- workspace bytes for the fp16 V
+ * form of attn_prefill_paged: the tile offsets (256-byte aligned), then
+ * int32 V-format flags [B, h_kv, ceil(max_blocks_per_seq / 8)] (256-byte
+ * aligned), then the fp16 copy [B, ceil(max_blocks_per_seq / 8) * 128,
+ * h_kv, d_h] (row b's key t at token b * ceil(max_blocks_per_seq / 8) * 128
+ * + t). Host-only, pure. Returns 0 for invalid arguments (B < 0,
+ * max_blocks_per_seq outside [1, 2^26], h_kv outside [1, 65535], d_h other
+ * than 64 / 128) and when B * ceil(max_blocks_per_seq / 8) * 128 >= 2^31 (the
+ * copy's token index must fit int32); the small workspace then still works.
+ */
+size_t attn_prefill_paged_v16_workspace_bytes(int B, int max_blocks_per_seq, int h_kv, int d_h);
 attn_status_t attn_prefill_paged(const void* q, const void* k_cache, const void* v_cache,
                                  const int32_t* block_table, const int32_t* cu_seqlens_q,
                                  const int32_t* seq_lens, int B, int total_q, int h, int h_kv,

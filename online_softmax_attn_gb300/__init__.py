@@ -65,6 +65,8 @@ def library() -> ctypes.CDLL:
     lib.attn_prefill.restype = I
     lib.attn_prefill_paged_workspace_bytes.argtypes = [I]
     lib.attn_prefill_paged_workspace_bytes.restype = S
+    lib.attn_prefill_paged_v16_workspace_bytes.argtypes = [I, I, I, I]
+    lib.attn_prefill_paged_v16_workspace_bytes.restype = S
     lib.attn_prefill_paged.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, F, P, S, P, P, P]
     lib.attn_prefill_paged.restype = I
     lib.attn_decode_split_plan.argtypes = [I, I, I, ctypes.POINTER(I)]
@@ -163,13 +165,25 @@ def attn_prefill(q, k, v, causal: bool, scale: float | None = None, o=None, lse=
     return o, lse
 
 
+def attn_prefill_paged_workspace_bytes(B: int, max_blocks: int = 0, h_kv: int = 0, d_h: int = 0,
+                                       v16: bool = False) -> int:
+    """Workspace bytes of attn_prefill_paged: the small form (tile offsets),
+    or with ``v16`` the form that also holds the fp16 V copy (0 if that copy
+    cannot be used for these sizes)."""
+    if v16:
+        return int(library().attn_prefill_paged_v16_workspace_bytes(B, max_blocks, h_kv, d_h))
+    return int(library().attn_prefill_paged_workspace_bytes(B))
+
+
 def attn_prefill_paged(q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens, max_q_len: int,
-                       causal: bool = True, scale: float | None = None, workspace=None, o=None,
+                       causal: bool = True, scale: float | None = None, workspace="auto", o=None,
                        lse=None, return_lse: bool = True, stream=None):
     """Variable-length query rows over a paged cache. q [total_q, h, d] bf16
     (rows packed back to back), caches [num_blocks, 16, h_kv, d] bf16,
     block_table [B, max_blocks] int32, cu_seqlens_q [B+1] int32, seq_lens [B]
     int32 (all CUDA). Row b's queries are its last q_len_b key positions.
+    ``workspace``: "auto" allocates the fp16-V form when it is available,
+    None the small form (all V tiles bf16), or a caller's uint8 CUDA tensor.
     Returns (o [total_q, h, d] bf16, lse [total_q, h] fp32 or None)."""
     for t in (q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens):
         _need(t.is_cuda and t.is_contiguous(), "tensors must be contiguous CUDA tensors")
@@ -183,8 +197,14 @@ def attn_prefill_paged(q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens,
     _need(cu_seqlens_q.shape == (B + 1,) and block_table.dim() == 2 and block_table.shape[0] == B,
           "cu_seqlens_q [B+1], block_table [B, max_blocks] and seq_lens [B] expected")
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    if workspace is None:
-        workspace = torch.empty(max(library().attn_prefill_paged_workspace_bytes(B), 256),
+    if isinstance(workspace, str):
+        _need(workspace == "auto", 'workspace must be "auto", None or a tensor')
+        n = attn_prefill_paged_workspace_bytes(B, block_table.shape[1], h_kv, d, v16=True)
+        if n == 0:
+            n = attn_prefill_paged_workspace_bytes(B)
+        workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=q.device)
+    elif workspace is None:
+        workspace = torch.empty(max(attn_prefill_paged_workspace_bytes(B), 256),
                                 dtype=torch.uint8, device=q.device)
     if o is None:
         o = torch.empty_like(q)

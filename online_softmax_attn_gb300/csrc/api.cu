@@ -194,6 +194,33 @@ size_t attn_prefill_paged_workspace_bytes(int B) {
   return align256(size_t(B + 1) * sizeof(int32_t));
 }
 
+namespace {
+// Layout of the larger paged-prefill workspace: tile offsets, then the V
+// format flags [B, h_kv, max_tiles] int32, then the fp16 V copy
+// [B, max_tiles * 128, h_kv, d_h]. Zero when the copy cannot be addressed
+// (its token count must stay below 2^31) or the arguments are invalid.
+struct PagedV16Layout {
+  size_t flags_off = 0, v16_off = 0, total = 0;
+};
+PagedV16Layout paged_v16_layout(int B, int max_blocks_per_seq, int h_kv, int d_h) {
+  PagedV16Layout L;
+  if (B < 0 || max_blocks_per_seq < 1 || max_blocks_per_seq > (1 << 26) || h_kv < 1 ||
+      h_kv > 65535 || (d_h != 64 && d_h != 128))
+    return L;
+  const long long max_tiles = (max_blocks_per_seq + 7) / 8;
+  const long long tokens = static_cast<long long>(B) * max_tiles * 128;
+  if (tokens >= (1ll << 31)) return L;
+  L.flags_off = attn_prefill_paged_workspace_bytes(B);
+  L.v16_off = L.flags_off + align256(size_t(B) * h_kv * max_tiles * sizeof(int32_t));
+  L.total = L.v16_off + size_t(tokens) * h_kv * d_h * 2;
+  return L;
+}
+}  // namespace
+
+size_t attn_prefill_paged_v16_workspace_bytes(int B, int max_blocks_per_seq, int h_kv, int d_h) {
+  return paged_v16_layout(B, max_blocks_per_seq, h_kv, d_h).total;
+}
+
 attn_status_t attn_prefill_paged(const void* q, const void* k_cache, const void* v_cache,
                                  const int32_t* block_table, const int32_t* cu_seqlens_q,
                                  const int32_t* seq_lens, int B, int total_q, int h, int h_kv,
@@ -223,6 +250,13 @@ attn_status_t attn_prefill_paged(const void* q, const void* k_cache, const void*
   a.cu_q = cu_seqlens_q;
   a.seq_lens = seq_lens;
   a.tile_off = static_cast<int32_t*>(workspace);
+  a.v16 = nullptr;
+  a.vwide = nullptr;
+  const PagedV16Layout L = paged_v16_layout(B, max_blocks_per_seq, h_kv, d_h);
+  if (L.total != 0 && workspace_bytes >= L.total) {
+    a.v16 = static_cast<uint8_t*>(workspace) + L.v16_off;
+    a.vwide = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + L.flags_off);
+  }
   a.B = B;
   a.total_q = total_q;
   a.h = h;

@@ -90,6 +90,8 @@ struct PagedPrefill {
   const int32_t* cu_q;         // [B + 1]
   const int32_t* seq_lens;     // [B]
   int32_t* tile_off;           // [B + 1] workspace
+  void* v16;                   // fp16 V copy [B, max_tiles * 128, h_kv, d_h] or nullptr
+  int32_t* vwide;              // [B, h_kv, max_tiles] V-format flags (with v16)
   int B, total_q, h, h_kv, d_h, num_blocks, max_blocks, max_q_len, causal;
   float scale;
   void* o;                     // [total_q, h, d_h] bf16

@@ -180,6 +180,7 @@ struct PagedArgs {
   const int32_t* seq_lens;
   const int32_t* tile_off;
   int B, max_blocks, num_blocks;
+  int max_tiles;  // 128-key tiles per row in the fp16 V copy: ceil(max_blocks / 8)
 };
 
 template <int D, int NQ, int NSK, int NSV, bool PAGED>
@@ -235,8 +236,10 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
   }
   // Per key tile of this KV head: nonzero -> V stays bf16 (exact P_hi + P_lo
   // product); zero -> V is read from its fp16 copy (fp16 P). No flags: all
-  // tiles bf16.
-  const int* tile_wide = vwide ? vwide + size_t(kvh) * n_kv_all : nullptr;
+  // tiles bf16. Paged rows: flags [B, h_kv, max_tiles].
+  const int* tile_wide =
+      !vwide ? nullptr
+             : vwide + (PAGED ? (size_t(pb) * h_kv + kvh) * pa.max_tiles : size_t(kvh) * n_kv_all);
   auto is_wide = [&](int j) { return tile_wide ? (__ldg(tile_wide + j) != 0) : true; };
 
   if (threadIdx.x == 0) {
@@ -320,8 +323,18 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
         k_issued = j + 1;
         if (j >= NSV && !wait_or_abort(bars.v_empty(sv), ((j / NSV) - 1) & 1, abort_flag)) break;
         mbar_arrive_expect_tx(bars.v_full(sv), C::KTILE);
-        const CUtensorMap* vmap = is_wide(j) ? &tmap_v : &tmap_v16;
-        load_tile(sbase + C::V_OFF + sv * C::KTILE, vmap, bars.v_full(sv), j);
+        const bool v_wide = is_wide(j);
+        if (PAGED && !v_wide) {
+          // The row's fp16 copy is token-contiguous: one 128-token box per
+          // 64-element column block instead of one box per page.
+          const int tok = pb * pa.max_tiles * kBN + j * kBN;
+          for (int s = 0; s < C::SUBS; ++s)
+            tma_load_3d(sbase + C::V_OFF + sv * C::KTILE + s * C::SUB_BYTES, &tmap_v16,
+                        bars.v_full(sv), s * 64, kvh, tok);
+        } else {
+          load_tile(sbase + C::V_OFF + sv * C::KTILE, v_wide ? &tmap_v : &tmap_v16, bars.v_full(sv),
+                    j);
+        }
         v_issued = j + 1;
       }
       if (*abort_flag) {
@@ -669,6 +682,55 @@ __global__ void __launch_bounds__(256)
   if (threadIdx.x == 0) vwide[size_t(kvh) * n_tiles + tile] = wide;
 }
 
+// Paged V -> fp16 copy of the pages each row uses, token-contiguous per row:
+// [B, max_tiles * 128, h_kv, d_h] (row b's key t at token b * max_tiles * 128
+// + t), and flags [B, h_kv, max_tiles] with v_to_f16_kernel's meaning. Pages
+// from the row's last page to the end of its last 128-key tile, and
+// block-table entries outside the cache, are written as zeros: what the
+// bf16 path reads for them. Rows the attention kernel skips (query count
+// above the row's capacity) are left alone. The key count is clamped as the
+// attention kernel clamps it. One CTA per (tile, row, KV head).
+__global__ void __launch_bounds__(256)
+    paged_v_to_f16_kernel(const uint4* __restrict__ vc, const int32_t* __restrict__ block_table,
+                          const int32_t* __restrict__ cu_q, const int32_t* __restrict__ seq_lens,
+                          int max_blocks, int num_blocks, int h_kv, int chunks_per_row,
+                          int max_tiles, uint4* __restrict__ v16, int* __restrict__ vwide) {
+  const int jt = blockIdx.x, b = blockIdx.y, kvh = blockIdx.z;
+  const int cap = max_blocks * 16;
+  const int q_len = cu_q[b + 1] - cu_q[b];
+  if (q_len < 0 || q_len > cap) return;
+  int ctx = seq_lens[b];
+  if (ctx < q_len || ctx > cap) ctx = ctx < q_len ? q_len : cap;
+  const int n_pages = (ctx + 15) / 16;
+  if (jt * 8 >= n_pages) return;
+  const int n = kBN * chunks_per_row;
+  uint32_t mx = 0;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const int tok = i / chunks_per_row, c = i - tok * chunks_per_row;
+    const int page = jt * 8 + (tok >> 4), slot = tok & 15;
+    int phys = -1;
+    if (page < n_pages) {
+      phys = __ldg(block_table + size_t(b) * max_blocks + page);
+      if (phys >= num_blocks) phys = -1;
+    }
+    uint4 x = make_uint4(0u, 0u, 0u, 0u);
+    if (phys >= 0) x = vc[((size_t(phys) * 16 + slot) * h_kv + kvh) * chunks_per_row + c];
+    uint32_t m2;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(m2) : "r"(x.x & 0x7fff7fffu), "r"(x.y & 0x7fff7fffu));
+    asm("max.u16x2 %0, %0, %1;" : "+r"(m2) : "r"(x.z & 0x7fff7fffu));
+    asm("max.u16x2 %0, %0, %1;" : "+r"(m2) : "r"(x.w & 0x7fff7fffu));
+    asm("max.u16x2 %0, %0, %1;" : "+r"(mx) : "r"(m2));
+    uint4 y;
+    y.x = pack_f16x2(bf16lo(x.x), bf16hi(x.x));
+    y.y = pack_f16x2(bf16lo(x.y), bf16hi(x.y));
+    y.z = pack_f16x2(bf16lo(x.z), bf16hi(x.z));
+    y.w = pack_f16x2(bf16lo(x.w), bf16hi(x.w));
+    v16[((size_t(b) * max_tiles * kBN + size_t(jt) * kBN + tok) * h_kv + kvh) * chunks_per_row + c] = y;
+  }
+  const int wide = __syncthreads_or((mx & 0xffffu) >= 0x4780u || (mx >> 16) >= 0x4780u);
+  if (threadIdx.x == 0) vwide[(size_t(b) * h_kv + kvh) * max_tiles + jt] = wide;
+}
+
 template <int D, int NQ, int NSK, int NSV>
 cudaError_t launch(const void* q, const void* k, const void* v, const void* v16, const int* vwide,
                    void* o, float* lse, int T, int h, int h_kv, int causal, float scale,
@@ -714,13 +776,13 @@ cudaError_t launch(const void* q, const void* k, const void* v, const void* v16,
 // query count below 0 or above max_q_len (the grid's bound) is an error:
 // that row gets no tiles and its outputs are not written.
 __global__ void paged_tiles_kernel(const int32_t* __restrict__ cu_q, int B, int max_q_len,
-                                   int32_t* __restrict__ tile_off) {
+                                   int max_blocks, int32_t* __restrict__ tile_off) {
   if (threadIdx.x != 0) return;
   int acc = 0;
   tile_off[0] = 0;
   for (int b = 0; b < B; ++b) {
     int n = cu_q[b + 1] - cu_q[b];
-    if (n < 0 || n > max_q_len) {
+    if (n < 0 || n > max_q_len || n > max_blocks * 16) {
       atomicOr(&g_prefill_err, ATTN_DEVERR_BAD_SEQ_LEN);
       n = 0;
     }
@@ -755,7 +817,24 @@ cudaError_t launch_paged(const PagedPrefill& a, cudaStream_t stream) {
                           dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  paged_tiles_kernel<<<1, 32, 0, stream>>>(a.cu_q, a.B, a.max_q_len, a.tile_off);
+  const int max_tiles = (a.max_blocks + 7) / 8;
+  CUtensorMap tv16 = tv;
+  if (a.v16 != nullptr) {
+    // fp16 copy [B * max_tiles * 128 tokens, h_kv, d_h]: a 128-token box of one head.
+    const uint64_t dims[3] = {uint64_t(D), uint64_t(a.h_kv),
+                              uint64_t(a.B) * uint64_t(max_tiles) * kBN};
+    const uint64_t strides[2] = {uint64_t(D) * 2, uint64_t(a.h_kv) * D * 2};
+    const uint32_t box[3] = {64u, 1u, 128u};
+    if (encode_tensor_map(&tv16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, a.v16, dims, strides, box,
+                          CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+    paged_v_to_f16_kernel<<<dim3(max_tiles, a.B, a.h_kv), 256, 0, stream>>>(
+        static_cast<const uint4*>(a.v_cache), a.block_table, a.cu_q, a.seq_lens, a.max_blocks,
+        a.num_blocks, a.h_kv, D / 8, max_tiles, static_cast<uint4*>(a.v16), a.vwide);
+    const cudaError_t e0 = cudaGetLastError();
+    if (e0 != cudaSuccess) return e0;
+  }
+  paged_tiles_kernel<<<1, 32, 0, stream>>>(a.cu_q, a.B, a.max_q_len, a.max_blocks, a.tile_off);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   auto kern = prefill_bf16_kernel<D, NQ, NSK, NSV, true>;
@@ -768,8 +847,9 @@ cudaError_t launch_paged(const PagedPrefill& a, cudaStream_t stream) {
   const long long tiles = by_total < by_row ? by_total : by_row;
   if (tiles <= 0) return cudaSuccess;
   const dim3 grid(static_cast<unsigned>(tiles), a.h / NQ);
-  PagedArgs pa{a.block_table, a.cu_q, a.seq_lens, a.tile_off, a.B, a.max_blocks, a.num_blocks};
-  kern<<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tv, nullptr,
+  PagedArgs pa{a.block_table, a.cu_q,      a.seq_lens,   a.tile_off,
+               a.B,           a.max_blocks, a.num_blocks, max_tiles};
+  kern<<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tv16, a.v16 ? a.vwide : nullptr,
                                                static_cast<__nv_bfloat16*>(a.o), a.lse, 0, a.h,
                                                a.h_kv, a.causal, a.scale * kLog2e, 0, pa);
   return cudaGetLastError();

@@ -150,6 +150,23 @@ def test_invalid_arguments_rejected_before_launch(lib):
     assert S(bad) == "invalid argument"
 
 
+def test_prefill_paged_v16_workspace_bytes(lib):
+    """Tile offsets, then flags [B, h_kv, ceil(max_blocks/8)] int32, then the fp16 V copy
+    [B, ceil(max_blocks/8) * 128, h_kv, d_h], each region 256-byte aligned."""
+    lib.attn_prefill_paged_v16_workspace_bytes.argtypes = [ctypes.c_int] * 4
+    lib.attn_prefill_paged_v16_workspace_bytes.restype = ctypes.c_size_t
+    f = lib.attn_prefill_paged_v16_workspace_bytes
+    assert f(8, 512, 8, 128) == 256 + 16384 + 8 * 64 * 128 * 8 * 128 * 2
+    # 3 rows, 19 pages -> 3 tiles per row: offsets 256, flags 3*2*3*4=72 -> 256, copy 3*384*2*64*2
+    assert f(3, 19, 2, 64) == 256 + 256 + 3 * 384 * 2 * 64 * 2
+    assert f(0, 19, 2, 64) == 256 + 0 + 0
+    for bad in [(-1, 19, 2, 64), (3, 0, 2, 64), (3, 19, 0, 64), (3, 19, 2, 96), (3, 1 << 27, 2, 64)]:
+        assert f(*bad) == 0, bad
+    # the copy's token index must fit int32: 2^13 rows x 2^11 tiles x 128 = 2^31
+    assert f(1 << 13, 1 << 14, 1, 64) == 0
+    assert f((1 << 13) - 1, 1 << 14, 1, 64) != 0
+
+
 def test_prefill_workspace_bytes(lib):
     """fp16 copy of V (256-byte aligned) followed by one int per (KV head, 128-key tile)."""
     assert lib.attn_prefill_workspace_bytes(8192, 8, 128, 1) == 8 * 8192 * 128 * 2 + 2048  # then 8 x 64 ints

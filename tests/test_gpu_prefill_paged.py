@@ -35,12 +35,13 @@ MIXED = ([1, 128, 200, 77, 5, 300, 1, 129],
 
 @pytest.mark.parametrize("h,h_kv,d", [(8, 2, 128), (6, 2, 128), (4, 2, 64)])
 @pytest.mark.parametrize("causal", [True, False])
-def test_mixed_batch_matches_oracle(h, h_kv, d, causal):
+@pytest.mark.parametrize("workspace", ["auto", None], ids=["fp16V", "bf16V"])
+def test_mixed_batch_matches_oracle(h, h_kv, d, causal, workspace):
     q_lens, ctx = MIXED
     q, kc, vc, table, cu, seq = paged_batch(q_lens, ctx, h, h_kv, d, 3)
     scale = 1.0 / d ** 0.5
     o, lse = attn.attn_prefill_paged(q.cuda(), kc.cuda(), vc.cuda(), table.cuda(), cu.cuda(), seq.cuda(),
-                                     max(q_lens), causal, scale)
+                                     max(q_lens), causal, scale, workspace=workspace)
     torch.cuda.synchronize()
     assert attn.attn_get_device_error() == 0
     O_ref, L_ref = oracle.prefill_paged_ref(q, kc, vc, table, cu, seq, scale, causal)
@@ -84,3 +85,88 @@ def test_bad_page_sets_error_without_fault():
     torch.cuda.synchronize()
     assert attn.attn_get_device_error() & 0x2  # page index outside the cache
     assert attn.attn_get_device_error() == 0  # read clears
+
+
+def v16_layout(B, max_blocks, h_kv, d):
+    tiles = (max_blocks + 7) // 8
+    flags_off = attn.attn_prefill_paged_workspace_bytes(B)
+    v16_off = flags_off + -(-(B * h_kv * tiles * 4) // 256) * 256
+    return tiles, flags_off, v16_off
+
+
+def test_fp16_copy_layout_and_flags():
+    """The workspace's fp16 copy holds each row's keys token-contiguously
+    (row b's key t at token b * tiles * 128 + t), zeros from the row's last page
+    to the end of its last 128-key tile, and a zero flag for tiles fp16 holds."""
+    h, h_kv, d = 4, 2, 64
+    q_lens, ctx = [5, 40, 1], [300, 40, 129]
+    q, kc, vc, table, cu, seq = paged_batch(q_lens, ctx, h, h_kv, d, 6)
+    B, mb = len(ctx), table.shape[1]
+    n = attn.attn_prefill_paged_workspace_bytes(B, mb, h_kv, d, v16=True)
+    ws = torch.full((n,), 0x7f, dtype=torch.uint8, device="cuda")  # fp16 NaN pattern if left unwritten
+    attn.attn_prefill_paged(q.cuda(), kc.cuda(), vc.cuda(), table.cuda(), cu.cuda(), seq.cuda(),
+                            max(q_lens), True, 1.0 / d ** 0.5, workspace=ws)
+    torch.cuda.synchronize()
+    assert attn.attn_get_device_error() == 0
+    tiles, flags_off, v16_off = v16_layout(B, mb, h_kv, d)
+    flags = ws[flags_off:flags_off + B * h_kv * tiles * 4].view(torch.int32).view(B, h_kv, tiles).cpu()
+    v16 = ws[v16_off:].view(torch.float16).view(B, tiles * 128, h_kv, d).cpu()
+    for b in range(B):
+        pages = -(-ctx[b] // 16)
+        used_tiles = -(-pages // 8)
+        assert (flags[b, :, :used_tiles] == 0).all()
+        keys = torch.stack([vc[table[b, t // 16], t % 16] for t in range(pages * 16)])
+        assert torch.equal(v16[b, :pages * 16], keys.to(torch.float16))
+        assert (v16[b, pages * 16:used_tiles * 128] == 0).all()
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_wide_v_tiles_match_oracle(causal):
+    """Pages holding values fp16 cannot carry (|v| >= 2^16) flag their 128-key
+    tile, which then takes the bf16 P_hi + P_lo path; the other tiles of the
+    same rows take fp16 P. Outputs match the oracle either way."""
+    h, h_kv, d = 8, 2, 128
+    q_lens, ctx = [200, 64, 1], [1000, 600, 300]
+    q, kc, vc, table, cu, seq = paged_batch(q_lens, ctx, h, h_kv, d, 7)
+    vc = vc.clone()
+    vc[table[0, 3], 5, 1, 7] = 3.0e5      # row 0, tile 0, head 1
+    vc[table[1, 20], 0, 0, 100] = -7.0e4  # row 1, tile 2, head 0
+    vc[table[2, 9], 2, 1, 0] = 65280.0    # largest bf16 below 2^16, fits fp16: tile stays fp16
+    B, mb = len(ctx), table.shape[1]
+    n = attn.attn_prefill_paged_workspace_bytes(B, mb, h_kv, d, v16=True)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    scale = 1.0 / d ** 0.5
+    o, lse = attn.attn_prefill_paged(q.cuda(), kc.cuda(), vc.cuda(), table.cuda(), cu.cuda(), seq.cuda(),
+                                     max(q_lens), causal, scale, workspace=ws)
+    torch.cuda.synchronize()
+    assert attn.attn_get_device_error() == 0
+    tiles, flags_off, _ = v16_layout(B, mb, h_kv, d)
+    flags = ws[flags_off:flags_off + B * h_kv * tiles * 4].view(torch.int32).view(B, h_kv, tiles).cpu()
+    wide = {(b, k, t) for b in range(B) for k in range(h_kv) for t in range(-(-ctx[b] // 128))
+            if flags[b, k, t] != 0}
+    assert wide == {(0, 1, 0), (1, 0, 2)}
+    O_ref, L_ref = oracle.prefill_paged_ref(q, kc, vc, table, cu, seq, scale, causal)
+    check_out(o, O_ref, torch.bfloat16)
+    check_lse(lse, L_ref)
+
+
+@pytest.mark.parametrize("workspace", ["auto", None], ids=["fp16V", "bf16V"])
+def test_row_beyond_capacity_is_skipped(workspace):
+    """A row with more queries than its block-table row can hold keys is
+    skipped (outputs untouched) and flagged; the other rows are exact."""
+    h, h_kv, d = 4, 2, 64
+    q, kc, vc, table, cu, seq = paged_batch([40, 3, 1], [300, 20, 300], h, h_kv, d, 8)
+    cap = table.shape[1] * 16                      # 19 pages -> 304 keys
+    q_lens = [40, 3, cap + 6]
+    cu = torch.zeros(4, dtype=torch.int32)
+    cu[1:] = torch.cumsum(torch.tensor(q_lens, dtype=torch.int32), 0)
+    q = W.normal((int(cu[-1]), h, d), 81, torch.bfloat16)
+    scale = 1.0 / d ** 0.5
+    o = torch.full((int(cu[-1]), h, d), 7.0, dtype=torch.bfloat16, device="cuda")
+    attn.attn_prefill_paged(q.cuda(), kc.cuda(), vc.cuda(), table.cuda(), cu.cuda(), seq.cuda(),
+                            max(q_lens), True, scale, workspace=workspace, o=o)
+    torch.cuda.synchronize()
+    assert attn.attn_get_device_error() & 0x8  # ATTN_DEVERR_BAD_SEQ_LEN
+    assert (o[int(cu[2]):] == 7.0).all()
+    O_ref, _ = oracle.prefill_paged_ref(q[:int(cu[2])], kc, vc, table[:2], cu[:3], seq[:2], scale, True)
+    check_out(o[:int(cu[2])], O_ref, torch.bfloat16)
