@@ -46,9 +46,11 @@ KERNEL_FILES = {
                 "online_softmax_attn_gb300/csrc/common.cuh"],
     "decode": ["online_softmax_attn_gb300/csrc/decode.cu", "online_softmax_attn_gb300/csrc/common.cuh"],
 }
+KERNEL_FILES["prefill_paged"] = KERNEL_FILES["prefill"]
 NCU_TRAFFIC = {
     # kind: (dram read + write bytes per launch, sha256[:16] of the kernel's files)
-    "prefill": (131.43e6, "91ebea244e40db53"),  # profiles/prefill_bf16_T8192_causal.md
+    "prefill": (131.51e6, "7dfaa9e0f1bc11f3"),  # profiles/prefill_bf16_T8192_causal.md
+    "prefill_paged": (437.82e6, "7dfaa9e0f1bc11f3"),  # profiles/prefill_paged_B8_q1024_ctx8192.md
     # decode: 16-row capture (303.9 MB for 299.5 MB algorithmic) scaled by KV bytes to the
     # 66-row batch (profiles/decode_split_paged_B16.md)
     "decode": (2.1514e9, "2dcc49156d4ec784"),
@@ -274,6 +276,13 @@ def run_gpu(args, world, rank, local):
     torch.cuda.set_device(dev)
     hbm_peak, tc_peak, peak_kind = peaks()
     stream = torch.cuda.current_stream()
+    if args.only == "prefill_paged":
+        # The paged chunked-prefill measurement alone (profiler captures).
+        flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+        res = measure_prefill_paged(dev, flush, tc_peak, peak_kind, iters=max(1, args.steps))
+        if rank == 0:
+            print(json.dumps({"only": "prefill_paged", "prefill_paged": res}), flush=True)
+        return
 
     # ---- inputs, resident in HBM before the timed region ----
     q, k, v = W.prefill_inputs(PREFILL, seed=rank, device=dev)
@@ -572,7 +581,8 @@ def measure_prefill_paged(dev, flush, tc_peak, peak_kind, iters=10):
     return {"value": tf, "unit": "TFLOP/s", "ms": t, "rows": B, "queries_per_row": qn, "context": ctx,
             "flops": flops,
             "roofline": {"bound": "tensor", "achieved": tf, "peak": tc_peak, "unit": "TFLOP/s",
-                         "frac": tf / tc_peak, "traffic": None, "kernel": "prefill_bf16_kernel (paged)",
+                         "frac": tf / tc_peak, "traffic": traffic_for("prefill_paged"),
+                         "kernel": "prefill_bf16_kernel (paged)",
                          "peak_source": f"{peak_kind} bf16 burst"}}
 
 
@@ -623,8 +633,9 @@ def main():
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the measurements outside the step (deterministic / adaptive decode, "
                          "pair merge, paged prefill), e.g. for a launch list of the step alone")
-    ap.add_argument("--only", choices=["prefill", "decode"], default=None,
-                    help="run one half of the step (profiler captures; not a bench line)")
+    ap.add_argument("--only", choices=["prefill", "decode", "prefill_paged"], default=None,
+                    help="run one half of the step, or the paged prefill measurement alone "
+                         "(profiler captures; not a bench line)")
     ap.add_argument("--decode-rows", type=int, default=0,
                     help="truncate the decode batch (profiler captures; not a bench line)")
     args = ap.parse_args()
