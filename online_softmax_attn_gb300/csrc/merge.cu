@@ -8,13 +8,17 @@
 // evaluating -inf - (-inf)).
 //
 // Layout: WPR warps per output row (1 for many rows, 8 when there are too
-// few rows to fill the GPU); lane j owns d_h/32 consecutive output elements,
+// few rows to fill the GPU, and always 8 for fixed-size splits); lane j owns d_h/32 consecutive output elements,
 // so each split's O~ row is read as one coalesced 128-bit (d_h=128) or 64-bit
-// (d_h=64) access per lane. Every warp of a row first takes the overall max M
-// over all active splits; then, per chunk of 32 splits, the weights are
-// computed one per lane and broadcast with shuffles (so the loop carries no
-// dependent global load), the warps of the row take the chunk's splits in
-// turn, and with WPR > 1 they add their sums in shared memory.
+// (d_h=64) access per lane. Warp w of a row takes splits w, w + WPR, ... in
+// batches of 4 whose m, l and O~ loads are issued together; the first batch
+// is issued beside the load that gives the active-split count (it stays
+// inside the partial buffers, which hold all S splits, and a split found
+// inactive is skipped, never multiplied by zero), so a row costs one memory
+// round trip rather than three (count, then every m for the max, then O~).
+// Each warp keeps a running (max, l, O~) over its splits -- the same merge,
+// taken in a different order -- and with WPR > 1 the warps' states combine in
+// shared memory.
 #include "common.cuh"
 #include "internal.h"
 
@@ -32,14 +36,40 @@ __global__ void __launch_bounds__(256)
   constexpr int VEC = D / 32;
   static_assert(VEC == 2 || VEC == 4, "d_h must be 64 or 128");
   constexpr int RPC = 8 / WPR;  // rows per CTA of 8 warps
+  constexpr int U = 4;          // splits per warp whose loads are in flight together
   __shared__ float red_acc[WPR > 1 ? WPR * D : 1];
-  __shared__ float red_l[WPR];
+  __shared__ float red_m[WPR], red_l[WPR];
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int wr = warp % WPR;  // this warp's share of the row
   const int row = blockIdx.x * RPC + warp / WPR;
   if (WPR == 1 && row >= rows) return;
   const bool live = row < rows;  // WPR > 1: one row per CTA, always live
+
+  const float* mrow = m_part + size_t(row) * S;
+  const float* lrow = l_part + size_t(row) * S;
+  const float* orow = o_part + size_t(row) * S * D + lane * VEC;
+  float mi[U], li[U], oi[U][VEC];
+  auto load_batch = [&](int base, int lim) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = base + u * WPR;
+      if (i < lim) {
+        mi[u] = mrow[i];
+        li[u] = lrow[i];
+        const float* src = orow + size_t(i) * D;
+        if constexpr (VEC == 4) {
+          const float4 t = __ldg(reinterpret_cast<const float4*>(src));
+          oi[u][0] = t.x; oi[u][1] = t.y; oi[u][2] = t.z; oi[u][3] = t.w;
+        } else {
+          const float2 t = __ldg(reinterpret_cast<const float2*>(src));
+          oi[u][0] = t.x; oi[u][1] = t.y;
+        }
+      }
+    }
+  };
+  // First batch: in flight beside the active-split count.
+  if (live) load_batch(wr, S);
 
   int n = 0;
   if (live) {
@@ -54,71 +84,68 @@ __global__ void __launch_bounds__(256)
     n = max(0, min(n, S));
   }
 
-  const float* mrow = m_part + size_t(row) * S;
-  const float* lrow = l_part + size_t(row) * S;
-  const float* orow = o_part + size_t(row) * S * D + lane * VEC;
-
-  // Overall max over the active splits.
-  float M = -INFINITY;
-  for (int i = lane; i < n; i += 32) M = fmaxf(M, mrow[i]);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-
-  float acc[VEC];
+  // Running state over this warp's splits, exp2 domain for the max.
+  float Mw = -INFINITY, Lw = 0.f, acc[VEC];
 #pragma unroll
   for (int e = 0; e < VEC; ++e) acc[e] = 0.f;
-  float L = 0.f;
-  if (M != -INFINITY) {  // at least one non-empty split; no -inf - -inf below
-    const float Mb = M * kLog2e;
-    for (int c = 0; c < n; c += 32) {
-      const int i = c + lane;
-      float w = 0.f;
-      if (i < n) {
-        const float mi = mrow[i];
-        w = (mi == -INFINITY) ? 0.f : ex2_approx(fmaf(mi, kLog2e, -Mb));
-        if (wr == 0) L = fmaf(w, lrow[i], L);
-      }
-      const int cnt = min(32, n - c);
-#pragma unroll 8
-      for (int j = wr; j < cnt; j += WPR) {
-        const float wj = __shfl_sync(0xffffffffu, w, j);
-        const float* src = orow + size_t(c + j) * D;
-        if constexpr (VEC == 4) {
-          const float4 t = __ldg(reinterpret_cast<const float4*>(src));
-          acc[0] = fmaf(wj, t.x, acc[0]);
-          acc[1] = fmaf(wj, t.y, acc[1]);
-          acc[2] = fmaf(wj, t.z, acc[2]);
-          acc[3] = fmaf(wj, t.w, acc[3]);
-        } else {
-          const float2 t = __ldg(reinterpret_cast<const float2*>(src));
-          acc[0] = fmaf(wj, t.x, acc[0]);
-          acc[1] = fmaf(wj, t.y, acc[1]);
-        }
+  auto merge_batch = [&](int base) {
+    float bm = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (base + u * WPR < n) bm = fmaxf(bm, mi[u] * kLog2e);
+    if (bm == -INFINITY) return;  // no active split with keys in this batch
+    const float Mn = fmaxf(Mw, bm);
+    const float sc = (Mw == -INFINITY) ? 0.f : ex2_approx(Mw - Mn);
+    Lw *= sc;
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) acc[e] *= sc;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (base + u * WPR < n && mi[u] != -INFINITY) {
+        const float w = ex2_approx(fmaf(mi[u], kLog2e, -Mn));
+        Lw = fmaf(w, li[u], Lw);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) acc[e] = fmaf(w, oi[u][e], acc[e]);
       }
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+    Mw = Mn;
+  };
+  if (live) {
+    merge_batch(wr);
+    for (int base = wr + U * WPR; base < n; base += U * WPR) {
+      load_batch(base, n);
+      merge_batch(base);
+    }
   }
 
+  float M = Mw, L = Lw;
   if constexpr (WPR > 1) {
 #pragma unroll
     for (int e = 0; e < VEC; ++e) red_acc[wr * D + lane * VEC + e] = acc[e];
-    if (lane == 0) red_l[wr] = L;
+    if (lane == 0) {
+      red_m[wr] = Mw;
+      red_l[wr] = Lw;
+    }
     __syncthreads();
     if (wr != 0 || !live) return;
+    M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < WPR; ++w) M = fmaxf(M, red_m[w]);
     L = 0.f;
 #pragma unroll
-    for (int w = 0; w < WPR; ++w) L += red_l[w];
+    for (int e = 0; e < VEC; ++e) acc[e] = 0.f;
+    if (M != -INFINITY) {
 #pragma unroll
-    for (int e = 0; e < VEC; ++e) {
-      float a = 0.f;
+      for (int w = 0; w < WPR; ++w) {
+        const float f = (red_m[w] == -INFINITY) ? 0.f : ex2_approx(red_m[w] - M);
+        L = fmaf(f, red_l[w], L);
 #pragma unroll
-      for (int w = 0; w < WPR; ++w) a += red_acc[w * D + lane * VEC + e];
-      acc[e] = a;
+        for (int e = 0; e < VEC; ++e) acc[e] = fmaf(f, red_acc[w * D + lane * VEC + e], acc[e]);
+      }
     }
   }
 
-  const bool empty = !(L > 0.f);  // also catches NaN mass
+  const bool empty = !(L > 0.f);  // also catches NaN mass and rows with no active split
   const float inv = empty ? 0.f : 1.f / L;
 #pragma unroll
   for (int e = 0; e < VEC; ++e) acc[e] = empty ? 0.f : acc[e] * inv;
@@ -142,7 +169,8 @@ __global__ void __launch_bounds__(256)
       *reinterpret_cast<float2*>(dst) = make_float2(acc[0], acc[1]);
     }
   }
-  if (lse_out != nullptr && lane == 0) lse_out[row] = empty ? -INFINITY : M + logf(L);
+  // M is in exp2 units here; the partials' m and the LSE are natural-log.
+  if (lse_out != nullptr && lane == 0) lse_out[row] = empty ? -INFINITY : M * kLn2 + logf(L);
 }
 
 cudaError_t launch_merge(const float* o_part, const float* m_part, const float* l_part,
@@ -151,8 +179,11 @@ cudaError_t launch_merge(const float* o_part, const float* m_part, const float* 
                          attn_dtype_t out_dtype, cudaStream_t stream, int fixed_pps,
                          const int* pps_dev) {
   if (rows <= 0) return cudaSuccess;
-  // Few rows and many splits: spread each row's splits over 8 warps.
-  const bool wide = rows < 512 && num_splits > 4;
+  // Few rows and many splits: spread each row's splits over 8 warps. With
+  // fixed-size splits (the batch-invariant mode) always 8: the order in which
+  // a row's splits are summed then depends on that row's split count alone,
+  // not on the batch's rows or grid width.
+  const bool wide = fixed_pps > 0 || (rows < 512 && num_splits > 4);
   const dim3 grid(wide ? rows : (rows + 7) / 8);
   const dim3 block(256);
   const bool bf = out_dtype == ATTN_DTYPE_BF16;
