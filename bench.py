@@ -360,20 +360,19 @@ def run_gpu(args, world, rank, local):
         hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
         ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
         hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-        dq_, dk_, dv_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
         hdq = dq.cpu().pin_memory()
         htab, hseq = table.cpu().pin_memory(), seq.cpu().pin_memory()
         hdo = torch.empty(do.shape, dtype=do.dtype).pin_memory()
         hdl = torch.empty(dlse.shape, dtype=dlse.dtype).pin_memory()
         ddq, dtab, dseq = torch.empty_like(dq), torch.empty_like(table), torch.empty_like(seq)
 
+        # Host-buffer entry point: the copies in and out run inside the call,
+        # pipelined over groups of KV heads against the attention.
+        hscratch = torch.empty(attn.attn_prefill_host_scratch_bytes(PREFILL.T, PREFILL.h, PREFILL.h_kv,
+                                                                    PREFILL.d_h), dtype=torch.uint8, device=dev)
+
         def e2e_prefill():
-            dq_.copy_(hq, non_blocking=True)
-            dk_.copy_(hk, non_blocking=True)
-            dv_.copy_(hv, non_blocking=True)
-            attn.attn_prefill(dq_, dk_, dv_, True, PREFILL.scale, o=o, lse=lse, workspace=pws)
-            ho.copy_(o, non_blocking=True)
-            hl.copy_(lse, non_blocking=True)
+            attn.attn_prefill_host(hq, hk, hv, True, PREFILL.scale, o=ho, lse=hl, scratch=hscratch)
 
         def e2e_decode():
             ddq.copy_(hdq, non_blocking=True)

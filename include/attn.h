@@ -117,6 +117,44 @@ attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o,
                            void* stream);
 
 /*
+ * attn_prefill_host -- attn_prefill with Q, K, V in host memory and O, LSE
+ * written back to host memory, copies included in the call ([NA] (3), as
+ * attn_prefill; heads are independent, so the layer is cut into n_chunks
+ * groups of h_kv / n_chunks KV heads with their query heads, and group c+1's
+ * inputs copy in while group c computes and group c-1's outputs copy out).
+ * Results are bitwise those of attn_prefill on the same inputs.
+ *
+ *   q, k, v, o, lse   host pointers, same shapes, dtypes and layouts as
+ *                     attn_prefill; lse may be NULL. Page-locked memory
+ *                     (cudaHostAlloc / cudaHostRegister) lets the copies run
+ *                     asynchronously and overlap; pageable memory works but
+ *                     copies through staging.
+ *   n_chunks          number of groups, dividing h_kv (at most 64); 0 picks 4
+ *                     or 2 when h_kv allows, else 1
+ *   scratch           device memory, 256-byte aligned, at least
+ *                     attn_prefill_host_scratch_bytes(T, h, h_kv, d_h, dtype)
+ *                     bytes: device copies of q, k, v, o, lse and the
+ *                     prefill workspace
+ *   stream            the caller's stream: the call is ordered after the work
+ *                     already queued on it, runs the attention on it, and the
+ *                     stream continues only after the last output copy; the
+ *                     host buffers may be read after that work completes
+ *                     (e.g. cudaStreamSynchronize). Returns once queued.
+ * Two copy streams and an event pool per device are created on the first
+ * call (which therefore must not be inside a stream capture) and kept;
+ * later calls, including captured ones, create nothing. Calls from several
+ * host threads are serialised while they queue work.
+ * Errors: as attn_prefill, plus INVALID_ARG for n_chunks < 0, n_chunks > 64,
+ * h_kv % n_chunks != 0, a NULL or misaligned scratch or one that is too
+ * small; ATTN_ERR_CUDA if a copy, event or launch fails.
+ */
+size_t attn_prefill_host_scratch_bytes(int T, int h, int h_kv, int d_h, attn_dtype_t dtype);
+attn_status_t attn_prefill_host(const void* q, const void* k, const void* v, void* o, float* lse,
+                                int T, int h, int h_kv, int d_h, int causal, float scale,
+                                attn_dtype_t dtype, int n_chunks, void* scratch,
+                                size_t scratch_bytes, void* stream);
+
+/*
  * attn_prefill_paged -- exact attention for a batch of variable-length query
  * rows over a paged KV cache (chunked prefill, and mixed batches of prefill
  * and decode rows). Row b has the q_len_b = cu_seqlens_q[b+1] - cu_seqlens_q[b]

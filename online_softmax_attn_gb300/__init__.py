@@ -63,6 +63,10 @@ def library() -> ctypes.CDLL:
     lib.attn_prefill_workspace_bytes.restype = S
     lib.attn_prefill.argtypes = [P, P, P, P, P, I, I, I, I, I, F, I, P, S, P]
     lib.attn_prefill.restype = I
+    lib.attn_prefill_host_scratch_bytes.argtypes = [I, I, I, I, I]
+    lib.attn_prefill_host_scratch_bytes.restype = S
+    lib.attn_prefill_host.argtypes = [P, P, P, P, P, I, I, I, I, I, F, I, I, P, S, P]
+    lib.attn_prefill_host.restype = I
     lib.attn_prefill_paged_workspace_bytes.argtypes = [I]
     lib.attn_prefill_paged_workspace_bytes.restype = S
     lib.attn_prefill_paged_v16_workspace_bytes.argtypes = [I, I, I, I]
@@ -162,6 +166,49 @@ def attn_prefill(q, k, v, causal: bool, scale: float | None = None, o=None, lse=
                                 int(bool(causal)), scale, dt, _ptr(workspace), ws_bytes,
                                 _stream(stream))
     _check("attn_prefill", st)
+    return o, lse
+
+
+def attn_prefill_host_scratch_bytes(T: int, h: int, h_kv: int, d_h: int, dtype=torch.bfloat16) -> int:
+    """Device scratch bytes of attn_prefill_host."""
+    dt = ATTN_DTYPE_BF16 if dtype == torch.bfloat16 else ATTN_DTYPE_F32
+    n = library().attn_prefill_host_scratch_bytes(T, h, h_kv, d_h, dt)
+    _need(n != (1 << 64) - 1, "invalid prefill shape")
+    return int(n)
+
+
+def attn_prefill_host(q, k, v, causal: bool, scale: float | None = None, o=None, lse=None,
+                      return_lse: bool = True, scratch=None, n_chunks: int = 0, stream=None):
+    """attn_prefill on host tensors: q [h,T,d], k/v [h_kv,T,d] (bf16 or fp32,
+    CPU, contiguous; pinned memory lets the copies overlap the compute). The
+    copies in and out run inside the call, pipelined over groups of KV heads
+    on the current CUDA device. Returns host (o, lse); they are complete once
+    ``stream`` (default: the current stream) has run the queued work."""
+    for t in (q, k, v):
+        _need(t.device.type == "cpu" and t.is_contiguous(), "q, k, v must be contiguous CPU tensors")
+    _need(q.dim() == 3 and k.dim() == 3 and v.shape == k.shape, "expected q [h,T,d], k/v [h_kv,T,d]")
+    _need(q.dtype == k.dtype == v.dtype and q.dtype in (torch.bfloat16, torch.float32),
+          "q, k, v must share dtype bf16 or fp32")
+    h, T, d = q.shape
+    h_kv = k.shape[0]
+    _need(k.shape[1] == T and k.shape[2] == d, "q and k/v disagree in T or d")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if o is None:
+        o = torch.empty(q.shape, dtype=q.dtype, pin_memory=q.is_pinned())
+    if lse is None and return_lse:
+        lse = torch.empty((h, T), dtype=torch.float32, pin_memory=q.is_pinned())
+    for t in (o, lse):
+        _need(t is None or (t.device.type == "cpu" and t.is_contiguous()), "o, lse must be contiguous CPU tensors")
+    if scratch is None:
+        scratch = torch.empty(max(attn_prefill_host_scratch_bytes(T, h, h_kv, d, q.dtype), 256),
+                              dtype=torch.uint8, device=torch.cuda.current_device())
+    _need(scratch.is_cuda and scratch.dtype == torch.uint8 and scratch.is_contiguous(),
+          "scratch must be a contiguous uint8 CUDA tensor")
+    dt = ATTN_DTYPE_BF16 if q.dtype == torch.bfloat16 else ATTN_DTYPE_F32
+    st = library().attn_prefill_host(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), T, h, h_kv, d,
+                                     int(bool(causal)), scale, dt, int(n_chunks), _ptr(scratch),
+                                     scratch.numel(), _stream(stream))
+    _check("attn_prefill_host", st)
     return o, lse
 
 

@@ -25,7 +25,7 @@ LIB_NAME = "libattn_gb300.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
 
 SOURCES = ["api.cu", "merge.cu", "decode.cu", "prefill_simt.cu", "prefill_tc.cu",
-           "decode_static.cu"]
+           "decode_static.cu", "host_prefill.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

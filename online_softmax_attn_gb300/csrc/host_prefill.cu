@@ -1,0 +1,190 @@
+// host_prefill.cu -- attn_prefill_host: the prefill of attn_prefill with Q, K
+// and V read from host memory and O, LSE written back to host memory, in one
+// call.
+//
+// The layer is cut into groups of KV heads, each with its query heads (heads
+// are the outermost dimension, so a group is one contiguous slice of every
+// tensor). Group c+1's inputs copy in while group c computes and group c-1's
+// outputs copy out: the copies run on two library-owned streams, the
+// attention on the caller's stream, ordered by events (fork from and join
+// back to the caller's stream, which CUDA graph capture follows). Each group
+// is an independent prefill over its heads ("Naive attention and the online
+// softmax": every query row's recurrence reads only its own head's Q and its
+// KV head's K, V), so results are bitwise those of attn_prefill.
+#include <cmath>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace attn {
+namespace {
+
+constexpr int kMaxChunks = 64;
+constexpr int kMaxDevices = 64;
+
+bool aligned_to(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Per device: an inbound and an outbound copy stream and an event pool,
+// created on the first call and kept for the life of the process.
+struct HostPipe {
+  cudaStream_t in = nullptr, out = nullptr;
+  cudaEvent_t ev[2 * kMaxChunks + 2] = {};
+  bool ready = false;
+};
+std::mutex g_pipe_mu;  // guards creation and the enqueue sequence (shared events)
+HostPipe g_pipes[kMaxDevices];
+
+void destroy_pipe(HostPipe& p) {
+  for (cudaEvent_t& e : p.ev)
+    if (e) (void)cudaEventDestroy(e), e = nullptr;
+  if (p.in) (void)cudaStreamDestroy(p.in), p.in = nullptr;
+  if (p.out) (void)cudaStreamDestroy(p.out), p.out = nullptr;
+}
+
+cudaError_t pipe_for_current_device(HostPipe** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  HostPipe& p = g_pipes[dev];
+  if (!p.ready) {
+    e = cudaStreamCreateWithFlags(&p.in, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p.out, cudaStreamNonBlocking);
+    for (int i = 0; e == cudaSuccess && i < 2 * kMaxChunks + 2; ++i)
+      e = cudaEventCreateWithFlags(&p.ev[i], cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+      destroy_pipe(p);
+      return e;
+    }
+    p.ready = true;
+  }
+  *out = &p;
+  return cudaSuccess;
+}
+
+// Device scratch: q, k, v, o, lse copies, then the prefill workspace (fp16 V
+// copy and tile flags), each region 256-byte aligned.
+struct HostScratch {
+  size_t q, k, v, o, lse, ws, total;
+};
+HostScratch host_scratch(int T, int h, int h_kv, int d_h, size_t elem, size_t ws_bytes) {
+  HostScratch L;
+  const size_t qn = size_t(h) * T * d_h * elem, kn = size_t(h_kv) * T * d_h * elem;
+  L.q = 0;
+  L.k = L.q + align256(qn);
+  L.v = L.k + align256(kn);
+  L.o = L.v + align256(kn);
+  L.lse = L.o + align256(qn);
+  L.ws = L.lse + align256(size_t(h) * T * sizeof(float));
+  L.total = L.ws + ws_bytes;
+  return L;
+}
+
+// Groups per call when the caller passes 0: enough to overlap copies and
+// compute, few enough that each group's launch still fills the GPU.
+int auto_chunks(int h_kv) {
+  for (int c : {4, 2})
+    if (h_kv % c == 0) return c;
+  return 1;
+}
+
+}  // namespace
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" {
+
+size_t attn_prefill_host_scratch_bytes(int T, int h, int h_kv, int d_h, attn_dtype_t dtype) {
+  if (T < 0 || h < 1 || h_kv < 1 || h % h_kv != 0 || (d_h != 64 && d_h != 128))
+    return static_cast<size_t>(-1);
+  if (dtype != ATTN_DTYPE_F32 && dtype != ATTN_DTYPE_BF16) return static_cast<size_t>(-1);
+  if (T == 0) return 0;
+  const size_t elem = dtype == ATTN_DTYPE_F32 ? 4 : 2;
+  const size_t ws = dtype == ATTN_DTYPE_BF16 ? prefill_layout(T, h_kv, d_h).total : 0;
+  return host_scratch(T, h, h_kv, d_h, elem, ws).total;
+}
+
+attn_status_t attn_prefill_host(const void* q, const void* k, const void* v, void* o, float* lse,
+                                int T, int h, int h_kv, int d_h, int causal, float scale,
+                                attn_dtype_t dtype, int n_chunks, void* scratch,
+                                size_t scratch_bytes, void* stream) {
+  if (T < 0 || h < 1 || h_kv < 1 || h % h_kv != 0 || h > 65535 || !std::isfinite(scale) ||
+      !(scale > 0.f))
+    return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_DTYPE_F32 && dtype != ATTN_DTYPE_BF16) return ATTN_ERR_INVALID_ARG;
+  if (d_h != 64 && d_h != 128) return ATTN_ERR_UNSUPPORTED;
+  if (n_chunks < 0 || n_chunks > kMaxChunks || (n_chunks > 0 && h_kv % n_chunks != 0))
+    return ATTN_ERR_INVALID_ARG;
+  if (T == 0) return ATTN_OK;
+  if (!q || !k || !v || !o || !scratch) return ATTN_ERR_INVALID_ARG;
+  if (!aligned_to(scratch, 256) ||
+      scratch_bytes < attn_prefill_host_scratch_bytes(T, h, h_kv, d_h, dtype))
+    return ATTN_ERR_INVALID_ARG;
+  const int chunks = n_chunks > 0 ? n_chunks : auto_chunks(h_kv);
+  const size_t elem = dtype == ATTN_DTYPE_F32 ? 4 : 2;
+  const size_t ws_bytes = dtype == ATTN_DTYPE_BF16 ? prefill_layout(T, h_kv, d_h).total : 0;
+  const HostScratch L = host_scratch(T, h, h_kv, d_h, elem, ws_bytes);
+  uint8_t* base = static_cast<uint8_t*>(scratch);
+  uint8_t *dq = base + L.q, *dk = base + L.k, *dv = base + L.v, *dO = base + L.o;
+  float* dl = reinterpret_cast<float*>(base + L.lse);
+  void* dws = dtype == ATTN_DTYPE_BF16 ? base + L.ws : nullptr;
+
+  const int g = h / h_kv, kvc = h_kv / chunks, hc = kvc * g;
+  const size_t q_bytes = size_t(hc) * T * d_h * elem;   // one group's Q (and O)
+  const size_t kv_bytes = size_t(kvc) * T * d_h * elem;  // one group's K (and V)
+  const size_t l_bytes = size_t(hc) * T * sizeof(float);
+  const auto* hq = static_cast<const uint8_t*>(q);
+  const auto* hk = static_cast<const uint8_t*>(k);
+  const auto* hv = static_cast<const uint8_t*>(v);
+  auto* ho = static_cast<uint8_t*>(o);
+  auto* hl = reinterpret_cast<uint8_t*>(lse);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  std::lock_guard<std::mutex> lock(g_pipe_mu);
+  HostPipe* P = nullptr;
+  cudaError_t e = pipe_for_current_device(&P);
+  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  cudaEvent_t ev_start = P->ev[0], ev_done = P->ev[1];
+  // Both copy streams start after the work already queued on the caller's
+  // stream (which may still be using the scratch).
+  e = cudaEventRecord(ev_start, s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(P->in, ev_start, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(P->out, ev_start, 0);
+  for (int c = 0; e == cudaSuccess && c < chunks; ++c) {
+    cudaEvent_t ev_in = P->ev[2 + c], ev_cmp = P->ev[2 + kMaxChunks + c];
+    const size_t oq = size_t(c) * q_bytes, okv = size_t(c) * kv_bytes, ol = size_t(c) * l_bytes;
+    e = cudaMemcpyAsync(dk + okv, hk + okv, kv_bytes, cudaMemcpyHostToDevice, P->in);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dv + okv, hv + okv, kv_bytes, cudaMemcpyHostToDevice, P->in);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dq + oq, hq + oq, q_bytes, cudaMemcpyHostToDevice, P->in);
+    if (e == cudaSuccess) e = cudaEventRecord(ev_in, P->in);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ev_in, 0);
+    if (e == cudaSuccess) {
+      if (dtype == ATTN_DTYPE_F32)
+        e = launch_prefill_f32(reinterpret_cast<const float*>(dq + oq),
+                               reinterpret_cast<const float*>(dk + okv),
+                               reinterpret_cast<const float*>(dv + okv),
+                               reinterpret_cast<float*>(dO + oq), dl + size_t(c) * hc * T, T, hc,
+                               kvc, d_h, causal != 0, scale, s);
+      else
+        e = launch_prefill_bf16(dq + oq, dk + okv, dv + okv, dO + oq, dl + size_t(c) * hc * T, T,
+                                hc, kvc, d_h, causal != 0, scale, dws, s);
+    }
+    if (e == cudaSuccess) e = cudaEventRecord(ev_cmp, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(P->out, ev_cmp, 0);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(ho + oq, dO + oq, q_bytes, cudaMemcpyDeviceToHost, P->out);
+    if (e == cudaSuccess && hl)
+      e = cudaMemcpyAsync(hl + ol, reinterpret_cast<uint8_t*>(dl) + ol, l_bytes,
+                          cudaMemcpyDeviceToHost, P->out);
+  }
+  // Join: the caller's stream continues after the last output copy. Done
+  // even after an error, so both copy streams are joined back.
+  cudaError_t ej = cudaEventRecord(ev_done, P->out);
+  if (ej == cudaSuccess) ej = cudaStreamWaitEvent(s, ev_done, 0);
+  if (e == cudaSuccess) e = ej;
+  if (e == cudaErrorNotSupported) return ATTN_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // extern "C"

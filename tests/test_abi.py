@@ -150,6 +150,26 @@ def test_invalid_arguments_rejected_before_launch(lib):
     assert S(bad) == "invalid argument"
 
 
+def test_prefill_host_scratch_bytes(lib):
+    """Device copies of q, k, v, o, lse, then the prefill workspace, each region 256-byte aligned."""
+    lib.attn_prefill_host_scratch_bytes.argtypes = [ctypes.c_int] * 5
+    lib.attn_prefill_host_scratch_bytes.restype = ctypes.c_size_t
+    lib.attn_prefill_workspace_bytes.argtypes = [ctypes.c_int] * 4
+    lib.attn_prefill_workspace_bytes.restype = ctypes.c_size_t
+    f = lib.attn_prefill_host_scratch_bytes
+    a = lambda x: -(-x // 256) * 256
+    T, h, h_kv, d = 333, 8, 2, 64
+    qb, kb, lb = h * T * d * 2, h_kv * T * d * 2, h * T * 4
+    ws = lib.attn_prefill_workspace_bytes(T, h_kv, d, 1)
+    assert ws == 85248 + 256
+    assert f(T, h, h_kv, d, 1) == a(qb) + 2 * a(kb) + a(qb) + a(lb) + ws
+    assert f(256, 1, 1, 64, 0) == 2 * a(256 * 64 * 4) + 2 * a(256 * 64 * 4) + a(256 * 4)  # fp32: no workspace
+    assert f(0, h, h_kv, d, 1) == 0
+    none = (1 << 64) - 1
+    for bad in [(-1, 8, 2, 64, 1), (64, 8, 3, 64, 1), (64, 8, 2, 96, 1), (64, 8, 2, 64, 7), (64, 0, 1, 64, 1)]:
+        assert f(*bad) == none, bad
+
+
 def test_prefill_paged_v16_workspace_bytes(lib):
     """Tile offsets, then flags [B, h_kv, ceil(max_blocks/8)] int32, then the fp16 V copy
     [B, ceil(max_blocks/8) * 128, h_kv, d_h], each region 256-byte aligned."""
