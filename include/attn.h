@@ -22,9 +22,11 @@
  * Conventions shared by every entry point
  *   - All tensor pointers are DEVICE pointers (cudaMalloc / PyTorch CUDA
  *     memory) unless a parameter says otherwise; the caller owns every buffer.
- *     The library never allocates, frees or synchronises: each call only
- *     enqueues kernels on `stream` (a cudaStream_t; NULL = legacy default
- *     stream) and returns.
+ *     The library never allocates memory, frees or synchronises: each call
+ *     only enqueues work on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and returns. The one exception is attn_prefill_host, whose
+ *     first call on a device creates two copy streams and an event pool that
+ *     it keeps (no memory allocation).
  *   - Tensors are dense, row-major, with the shapes given below. Tensor base
  *     pointers must be 16-byte aligned (TMA and 128-bit vector loads);
  *     `workspace` must be 256-byte aligned.

@@ -1,7 +1,8 @@
 // api.cu -- the C ABI declared in include/attn.h: host-side validation,
 // workspace carve-up, tensor-map encoding and kernel launches. No entry point
-// allocates, frees or synchronises (except attn_get_device_error, which is a
-// synchronising query by contract).
+// here allocates, frees or synchronises (except attn_get_device_error, which
+// is a synchronising query by contract); the host-memory prefill, with its
+// copy streams, lives in host_prefill.cu.
 #include <cudaTypedefs.h>
 
 #include <cmath>
