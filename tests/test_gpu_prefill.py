@@ -157,6 +157,20 @@ def test_gqa_T8192_sampled_rows(shape):
     check_lse(lse[heads, rows], L_ref)
 
 
+@pytest.mark.parametrize("causal", [True, False])
+def test_widened_logits_every_row(causal):
+    """Q and K x3 (logit standard deviation 9): rows move their reference
+    often and many of their keys sit 6-20 log2 units below the row max, where
+    the kernel's reference headroom makes the fp16 weights subnormal. Every
+    row of a 12-tile sequence with a ragged tail against the oracle."""
+    shape = W.PrefillShape("widened_T1500", 8, 2, 128, 1500, torch.bfloat16, causal, 3.0)
+    q, k, v = W.prefill_inputs(shape, 9)
+    o, lse = run(q, k, v, causal, shape.scale)
+    O_ref, L_ref = oracle.attention_ref(q, k, v, shape.scale, causal)
+    check_out(o, O_ref, torch.bfloat16)
+    check_lse(lse, L_ref)
+
+
 def test_bf16_output_guard_bands_untouched():
     shape = W.PrefillShape("t", 4, 2, 128, 200, torch.bfloat16, True)
     q, k, v = W.prefill_inputs(shape, 5)

@@ -170,3 +170,22 @@ def test_row_beyond_capacity_is_skipped(workspace):
     assert (o[int(cu[2]):] == 7.0).all()
     O_ref, _ = oracle.prefill_paged_ref(q[:int(cu[2])], kc, vc, table[:2], cu[:3], seq[:2], scale, True)
     check_out(o[:int(cu[2])], O_ref, torch.bfloat16)
+
+
+@pytest.mark.parametrize("workspace", ["auto", None], ids=["fp16V", "bf16V"])
+def test_widened_logits_mixed_batch(workspace):
+    """Q and K x3 (logit standard deviation 9) through the paged kernel:
+    frequent reference moves and fp16-subnormal weights, every row checked."""
+    q_lens, ctx = MIXED
+    h, h_kv, d = 8, 2, 128
+    q, kc, vc, table, cu, seq = paged_batch(q_lens, ctx, h, h_kv, d, 10)
+    q = (q.float() * 3).to(torch.bfloat16)
+    kc = (kc.float() * 3).to(torch.bfloat16)
+    scale = 1.0 / d ** 0.5
+    o, lse = attn.attn_prefill_paged(q.cuda(), kc.cuda(), vc.cuda(), table.cuda(), cu.cuda(), seq.cuda(),
+                                     max(q_lens), True, scale, workspace=workspace)
+    torch.cuda.synchronize()
+    assert attn.attn_get_device_error() == 0
+    O_ref, L_ref = oracle.prefill_paged_ref(q, kc, vc, table, cu, seq, scale, True)
+    check_out(o, O_ref, torch.bfloat16)
+    check_lse(lse, L_ref)
