@@ -25,6 +25,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -102,10 +103,10 @@ class ClockSampler:
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
+    def __init__(self, index: int, out_dir: str | None = None):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+        self.path = os.path.join(out_dir or tempfile.gettempdir(), f"attn_bench_clocks_rank{index}.csv")
 
     def _gpu_id(self):
         """nvidia-smi index of this rank's GPU (None: the only one visible)."""
@@ -322,7 +323,7 @@ def run_gpu(args, world, rank, local):
     if attn.attn_get_device_error() != 0:
         raise RuntimeError("device error during warm-up")
 
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(local, args.clocks_dir)
     clocks.start()
     barrier(world)
     torch.cuda.synchronize()
@@ -628,6 +629,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=16.0)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--clocks-dir", default=None,
+                    help="where to keep the raw nvidia-smi clock samples (default: the temp directory)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the measurements outside the step (deterministic / adaptive decode, "
