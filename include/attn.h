@@ -111,7 +111,8 @@ size_t attn_prefill_workspace_bytes(int T, int h_kv, int d_h, attn_dtype_t dtype
  * Errors: INVALID_ARG for NULL q/k/v/o (T > 0), T < 0, h < 1, h > 65535,
  * h_kv < 1, h % h_kv != 0, misaligned pointers, scale not finite and > 0, a
  * non-NULL workspace that is misaligned or smaller than required;
- * UNSUPPORTED for other d_h. T == 0 is a no-op returning ATTN_OK.
+ * UNSUPPORTED for other d_h, and for bf16 with more than 65535 query tiles
+ * of 128 (T > 8388480). T == 0 is a no-op returning ATTN_OK.
  */
 attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o, float* lse,
                            int T, int h, int h_kv, int d_h, int causal, float scale,
@@ -203,8 +204,9 @@ attn_status_t attn_prefill_host(const void* q, const void* k, const void* v, voi
  * caches and o; 4 for the int32 arrays and lse), B < 0, total_q < 0,
  * max_q_len < 1 with total_q > 0, h < 1, h > 65535, h % h_kv != 0,
  * num_blocks < 1, max_blocks_per_seq < 1, scale not finite and > 0, a small
- * workspace; UNSUPPORTED for d_h other than 64 / 128 or page_size != 16.
- * B == 0 or total_q == 0 is a no-op.
+ * workspace; UNSUPPORTED for d_h other than 64 / 128, page_size != 16, or
+ * more than 65535 query tiles in the launch (min(ceil(total_q / 128) + B,
+ * B * ceil(max_q_len / 128))). B == 0 or total_q == 0 is a no-op.
  */
 size_t attn_prefill_paged_workspace_bytes(int B);
 /*

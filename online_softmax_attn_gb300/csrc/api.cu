@@ -270,7 +270,9 @@ attn_status_t attn_prefill_paged(const void* q, const void* k_cache, const void*
   a.scale = scale;
   a.o = o;
   a.lse = lse;
-  return from_cuda(launch_prefill_paged(a, static_cast<cudaStream_t>(stream)));
+  const cudaError_t e = launch_prefill_paged(a, static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) return ATTN_ERR_UNSUPPORTED;
+  return from_cuda(e);
 }
 
 attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* v_cache,

@@ -202,13 +202,15 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int hq0 = blockIdx.y * NQ;
+  // Grid (head pairs, query tiles): the block scheduler walks x fastest, so
+  // every head pair's longest query tile starts before any shorter one.
+  const int hq0 = blockIdx.x * NQ;
   const int kvh = hq0 / (h / h_kv);
   int qb, nkv, n_kv_all;
   // Paged rows: the row, its first query token, query count and key count.
   int pb = 0, q_tok0 = 0, q_len = 0, ctx = 0, n_pages = 0;
   if constexpr (PAGED) {
-    const int tile = int(blockIdx.x);
+    const int tile = int(blockIdx.y);
     if (tile >= pa.tile_off[pa.B]) return;  // surplus CTA of the fixed grid
     int lo = 0, hi = pa.B - 1;              // last row whose first tile <= tile
     while (lo < hi) {
@@ -230,7 +232,7 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
     nkv = (key_end + kBN - 1) / kBN;
     n_kv_all = nkv;
   } else {
-    qb = causal ? (n_qblk - 1 - int(blockIdx.x)) : int(blockIdx.x);
+    qb = causal ? (n_qblk - 1 - int(blockIdx.y)) : int(blockIdx.y);
     n_kv_all = (T + kBN - 1) / kBN;
     nkv = causal ? min(qb + 1, n_kv_all) : n_kv_all;
   }
@@ -765,7 +767,8 @@ cudaError_t launch(const void* q, const void* k, const void* v, const void* v16,
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   const int n_qblk = (T + kBM - 1) / kBM;
-  const dim3 grid(n_qblk, h / NQ);
+  if (n_qblk > 65535) return cudaErrorNotSupported;  // query tiles index grid y
+  const dim3 grid(h / NQ, n_qblk);
   kern<<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tv16, v16 ? vwide : nullptr,
                                                static_cast<__nv_bfloat16*>(o), lse, T, h, h_kv,
                                                causal, scale * kLog2e, n_qblk, PagedArgs{});
@@ -846,7 +849,8 @@ cudaError_t launch_paged(const PagedPrefill& a, cudaStream_t stream) {
   const long long by_row = static_cast<long long>(a.B) * ((a.max_q_len + kBM - 1) / kBM);
   const long long tiles = by_total < by_row ? by_total : by_row;
   if (tiles <= 0) return cudaSuccess;
-  const dim3 grid(static_cast<unsigned>(tiles), a.h / NQ);
+  if (tiles > 65535) return cudaErrorNotSupported;  // query tiles index grid y
+  const dim3 grid(a.h / NQ, static_cast<unsigned>(tiles));
   PagedArgs pa{a.block_table, a.cu_q,      a.seq_lens,   a.tile_off,
                a.B,           a.max_blocks, a.num_blocks, max_tiles};
   kern<<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tv16, a.v16 ? a.vwide : nullptr,
