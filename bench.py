@@ -50,8 +50,8 @@ KERNEL_FILES = {
 KERNEL_FILES["prefill_paged"] = KERNEL_FILES["prefill"]
 NCU_TRAFFIC = {
     # kind: (dram read + write bytes per launch, sha256[:16] of the kernel's files)
-    "prefill": (132.13e6, "61f8f9d01d054440"),  # profiles/prefill_bf16_T8192_causal.md
-    "prefill_paged": (470.14e6, "61f8f9d01d054440"),  # profiles/prefill_paged_B8_q1024_ctx8192.md
+    "prefill": (131.84e6, "f9683cfa6f282de6"),  # profiles/prefill_bf16_T8192_causal.md
+    "prefill_paged": (460.70e6, "f9683cfa6f282de6"),  # profiles/prefill_paged_B8_q1024_ctx8192.md
     # decode: 16-row capture (303.9 MB for 299.5 MB algorithmic) scaled by KV bytes to the
     # 66-row batch (profiles/decode_split_paged_B16.md)
     "decode": (2.1514e9, "2dcc49156d4ec784"),
