@@ -446,6 +446,18 @@ attn_status_t attn_merge_lse_pair(const void* o_a, const float* lse_a, const voi
  */
 attn_status_t attn_get_device_error(void* stream, unsigned int* bits);
 
+/*
+ * attn_selftest_wait_timeout -- exercise the failure path of the kernels'
+ * bounded waits without a fault: one thread of one CTA waits, with the same
+ * routine the kernels use, on an mbarrier that nothing ever arrives on, with
+ * a limit of limit_us microseconds. The wait gives up, raises
+ * ATTN_DEVERR_WAIT_TIMEOUT in the device error word (read it with
+ * attn_get_device_error) and the kernel returns; the context stays usable.
+ * limit_us in [1, 1000000]. Errors: INVALID_ARG outside that range,
+ * ATTN_ERR_CUDA if the launch fails.
+ */
+attn_status_t attn_selftest_wait_timeout(unsigned int limit_us, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

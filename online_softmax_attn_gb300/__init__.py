@@ -63,6 +63,8 @@ def library() -> ctypes.CDLL:
     lib.attn_prefill_workspace_bytes.restype = S
     lib.attn_prefill.argtypes = [P, P, P, P, P, I, I, I, I, I, F, I, P, S, P]
     lib.attn_prefill.restype = I
+    lib.attn_selftest_wait_timeout.argtypes = [ctypes.c_uint, P]
+    lib.attn_selftest_wait_timeout.restype = I
     lib.attn_prefill_host_scratch_bytes.argtypes = [I, I, I, I, I]
     lib.attn_prefill_host_scratch_bytes.restype = S
     lib.attn_prefill_host.argtypes = [P, P, P, P, P, I, I, I, I, I, F, I, I, P, S, P]
@@ -443,6 +445,13 @@ def attn_merge_lse_pair(o_a, lse_a, o_b, lse_b, out_dtype=torch.bfloat16, o=None
                                        dt_in, _ptr(o), _ptr(lse), dt_out, _stream(stream))
     _check("attn_merge_lse_pair", st)
     return o, lse
+
+
+def attn_selftest_wait_timeout(limit_us: int = 1000, stream=None) -> None:
+    """Run a kernel whose bounded wait runs out (nothing arrives on its
+    barrier) after ``limit_us`` microseconds: it raises the wait-timeout bit
+    of the device error word and returns. For failure-detection tests."""
+    _check("attn_selftest_wait_timeout", library().attn_selftest_wait_timeout(int(limit_us), _stream(stream)))
 
 
 def attn_get_device_error(stream=None) -> int:

@@ -361,6 +361,12 @@ attn_status_t attn_merge_lse_pair(const void* o_a, const float* lse_a, const voi
                                      out_dtype, static_cast<cudaStream_t>(stream)));
 }
 
+attn_status_t attn_selftest_wait_timeout(unsigned int limit_us, void* stream) {
+  if (limit_us < 1 || limit_us > 1000000) return ATTN_ERR_INVALID_ARG;
+  return from_cuda(launch_wait_timeout_selftest(uint64_t(limit_us) * 1000ull,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
 attn_status_t attn_get_device_error(void* stream, unsigned int* bits) {
   if (bits == nullptr) return ATTN_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -135,19 +135,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait for the phase with the given parity to complete.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned int* err) {
+// Bounded wait for the phase with the given parity to complete: false, with
+// ATTN_DEVERR_WAIT_TIMEOUT raised in *err, once limit_ns have passed.
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, unsigned int* err,
+                                              uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer_ns() - t0 > ATTN_WAIT_LIMIT_NS) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       atomicOr(err, ATTN_DEVERR_WAIT_TIMEOUT);
       return false;
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned int* err) {
+  return mbar_wait_for(bar, parity, err, ATTN_WAIT_LIMIT_NS);
 }
 
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {

@@ -421,6 +421,23 @@ cudaError_t launch_decode_split(const DecodeArgs& a, cudaStream_t stream) {
   return launch_d<64>(a, tk, tv, stream);
 }
 
+// Failure-detection self-test: one thread waits, with the kernels' bounded
+// wait, on an mbarrier that nothing arrives on. The wait gives up after
+// limit_ns, raises ATTN_DEVERR_WAIT_TIMEOUT in this module's error word, and
+// the kernel returns.
+__global__ void wait_timeout_selftest_kernel(uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = smem_u32(&bar);
+  mbar_init(b, 1u);
+  fence_barrier_init();
+  (void)mbar_wait_for(b, 0, &g_decode_err, limit_ns);
+}
+
+cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, cudaStream_t stream) {
+  wait_timeout_selftest_kernel<<<1, 1, 0, stream>>>(limit_ns);
+  return cudaGetLastError();
+}
+
 unsigned int decode_read_and_clear_error(cudaStream_t stream, cudaError_t* st) {
   unsigned int v = 0, zero = 0;
   cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_decode_err, sizeof(v), 0,

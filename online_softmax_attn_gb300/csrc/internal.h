@@ -64,6 +64,7 @@ cudaError_t launch_decode_plan(const int32_t* seq_lens, int B, int h_kv, int max
                                int num_sms, int max_splits, int* pps_out, cudaStream_t stream);
 cudaError_t launch_decode_split(const DecodeArgs& a, cudaStream_t stream);
 unsigned int decode_read_and_clear_error(cudaStream_t stream, cudaError_t* st);
+cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, cudaStream_t stream);
 
 // prefill_simt.cu ----------------------------------------------------------
 cudaError_t launch_prefill_f32(const float* q, const float* k, const float* v, float* o,

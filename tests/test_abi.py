@@ -260,3 +260,11 @@ def test_decode_adaptive_workspace(lib):
     d = P(256)
     assert lib.attn_decode_paged_adaptive(d, d, d, d, d, 3, 32, 8, 128, 16, 100, 64, 16, 0.1, d, need,
                                           d, None, None) == attn.ATTN_ERR_INVALID_ARG
+
+
+def test_selftest_wait_timeout_arguments(lib):
+    """The limit is checked on the host before any launch."""
+    lib.attn_selftest_wait_timeout.argtypes = [ctypes.c_uint, ctypes.c_void_p]
+    lib.attn_selftest_wait_timeout.restype = ctypes.c_int
+    assert lib.attn_selftest_wait_timeout(0, None) == attn.ATTN_ERR_INVALID_ARG
+    assert lib.attn_selftest_wait_timeout(1000001, None) == attn.ATTN_ERR_INVALID_ARG
