@@ -460,6 +460,7 @@ def run_gpu(args, world, rank, local):
     # ---- pairwise (O, LSE) merge (prefix / suffix combine), outside the step ----
     extras = args.only is None and not args.no_extras
     merge_pair = measure_merge_pair(dev, flush, hbm_peak, peak_kind) if extras else None
+    decode_b1 = measure_decode_batch1(dev, hbm_peak, peak_kind) if extras else None
     prefill_paged = measure_prefill_paged(dev, flush, tc_peak, peak_kind) if extras else None
 
     # ---- CPU oracle baseline (rank 0, N = 1 only) ----
@@ -528,6 +529,7 @@ def run_gpu(args, world, rank, local):
             "adaptive": adaptive,
         },
         "merge_pair": merge_pair,
+        "decode_batch1": decode_b1,
         "prefill_paged": prefill_paged,
         "prefill_ms": pre_avg,
         "e2e": e2e,
@@ -584,6 +586,63 @@ def measure_prefill_paged(dev, flush, tc_peak, peak_kind, iters=10):
                          "frac": tf / tc_peak, "traffic": traffic_for("prefill_paged"),
                          "kernel": "prefill_bf16_kernel (paged)",
                          "peak_source": f"{peak_kind} bf16 burst"}}
+
+
+def measure_decode_batch1(dev, hbm_peak, peak_kind):
+    """Batch-1 decode (one query token per call) over a contiguous 32768-key
+    cache: h=32 / h_kv=8 at 16 splits, and the 70B tensor-parallel shard
+    h=8 / h_kv=1 at 64 splits. A single call is a few microseconds, so each
+    is timed as a CUDA graph of back-to-back calls whose KV caches rotate over
+    copies larger than twice L2 (every call reads its cache from HBM)."""
+    import online_softmax_attn_gb300 as attn
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    out = {}
+    for shape, splits in ((W.DECODE_S32K, 16), (W.DECODE_70B_TP8, 64)):
+        q, kc, vc, tab, seq = W.decode_inputs(shape, 0, device=dev, contiguous=True)
+        tab, seq = tab.to(dev), seq.to(dev)
+        lens = seq.tolist()
+        nbytes = decode_bytes(lens, shape)
+        kv = kc.numel() * kc.element_size() * 2
+        copies = max(2, -(-2 * l2 // kv))
+        caches = [(kc.clone(), vc.clone()) for _ in range(copies)]
+        ws = torch.empty(max(attn.attn_decode_workspace_bytes(1, shape.h, shape.d_h, splits), 256),
+                         dtype=torch.uint8, device=dev)
+        o = torch.empty_like(q)
+        lse = torch.empty((1, shape.h), dtype=torch.float32, device=dev)
+        n = 4 * copies
+
+        def calls():
+            for i in range(n):
+                k_, v_ = caches[i % copies]
+                attn.attn_decode_paged(q, k_, v_, tab, seq, splits, shape.scale, workspace=ws, o=o, lse=lse)
+
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            calls()  # warm-up outside the capture
+        torch.cuda.synchronize(dev)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(graph, stream=side):
+                calls()
+        graph.replay()
+        torch.cuda.synchronize(dev)
+        ms = []
+        for _ in range(5):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            graph.replay()
+            b.record()
+            b.synchronize()
+            ms.append(a.elapsed_time(b) / n)
+        t = statistics.median(ms)
+        gbs = nbytes / (t * 1e-3) / 1e9
+        out[shape.name] = {"us_per_call": t * 1e3, "value": gbs, "unit": "GB/s", "num_splits": splits,
+                           "kv_bytes": nbytes, "frac_of_hbm": gbs / hbm_peak,
+                           "peak_source": f"{peak_kind} copy bandwidth", "timing": f"CUDA graph of {n} calls"}
+        del caches, graph
+    return out
 
 
 def measure_merge_pair(dev, flush, hbm_peak, peak_kind, iters=20):
