@@ -63,7 +63,7 @@ const char* attn_status_string(attn_status_t status) {
   return "unknown status";
 }
 
-int attn_version(void) { return 200; }
+int attn_version(void) { return 201; }
 
 int attn_decode_split_plan(int seq_len, int page_size, int num_splits, int* pages_per_split) {
   if (seq_len < 0 || page_size < 1 || num_splits < 1) return -1;

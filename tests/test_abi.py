@@ -268,3 +268,8 @@ def test_selftest_wait_timeout_arguments(lib):
     lib.attn_selftest_wait_timeout.restype = ctypes.c_int
     assert lib.attn_selftest_wait_timeout(0, None) == attn.ATTN_ERR_INVALID_ARG
     assert lib.attn_selftest_wait_timeout(1000001, None) == attn.ATTN_ERR_INVALID_ARG
+
+
+def test_version(lib):
+    lib.attn_version.restype = ctypes.c_int
+    assert lib.attn_version() == 201
