@@ -11,7 +11,8 @@
 // few rows to fill the GPU, and always 8 for fixed-size splits); lane j owns d_h/32 consecutive output elements,
 // so each split's O~ row is read as one coalesced 128-bit (d_h=128) or 64-bit
 // (d_h=64) access per lane. Warp w of a row takes splits w, w + WPR, ... in
-// batches of 4 whose m, l and O~ loads are issued together; the first batch
+// batches (4 splits per warp, 8 with WPR = 8) whose m, l and O~ loads are
+// issued together; the first batch
 // is issued beside the load that gives the active-split count (it stays
 // inside the partial buffers, which hold all S splits, and a split found
 // inactive is skipped, never multiplied by zero), so a row costs one memory
@@ -36,7 +37,9 @@ __global__ void __launch_bounds__(256)
   constexpr int VEC = D / 32;
   static_assert(VEC == 2 || VEC == 4, "d_h must be 64 or 128");
   constexpr int RPC = 8 / WPR;  // rows per CTA of 8 warps
-  constexpr int U = 4;          // splits per warp whose loads are in flight together
+  // Splits per warp whose loads are in flight together: with 8 warps per row
+  // a first batch of 8 covers 64 splits in one round trip.
+  constexpr int U = WPR > 1 ? 8 : 4;
   __shared__ float red_acc[WPR > 1 ? WPR * D : 1];
   __shared__ float red_m[WPR], red_l[WPR];
   const int lane = threadIdx.x & 31;
