@@ -50,11 +50,11 @@ KERNEL_FILES = {
 KERNEL_FILES["prefill_paged"] = KERNEL_FILES["prefill"]
 NCU_TRAFFIC = {
     # kind: (dram read + write bytes per launch, sha256[:16] of the kernel's files)
-    "prefill": (131.84e6, "f9683cfa6f282de6"),  # profiles/prefill_bf16_T8192_causal.md
-    "prefill_paged": (460.70e6, "f9683cfa6f282de6"),  # profiles/prefill_paged_B8_q1024_ctx8192.md
-    # decode: 16-row capture (303.9 MB for 299.5 MB algorithmic) scaled by KV bytes to the
+    "prefill": (131.56e6, "fc47ea8d2a2af230"),  # profiles/prefill_bf16_T8192_causal.md
+    "prefill_paged": (465.41e6, "fc47ea8d2a2af230"),  # profiles/prefill_paged_B8_q1024_ctx8192.md
+    # decode: 16-row capture (304.1 MB for 299.5 MB algorithmic) scaled by KV bytes to the
     # 66-row batch (profiles/decode_split_paged_B16.md)
-    "decode": (2.1514e9, "2dcc49156d4ec784"),
+    "decode": (2.1527e9, "2a89913c613ae05d"),
 }
 
 
