@@ -114,3 +114,37 @@ def test_cascade_prefix_suffix_equals_full_decode(prefix_pages):
     assert torch.isneginf(ls[2]).all()  # the empty suffix
     check_out(o, O_ref, torch.bfloat16)
     check_lse(lse, L_ref)
+
+
+@pytest.mark.parametrize("prefix_pages", [64, 1])
+def test_cascade_shared_prefix_on_tensor_cores(prefix_pages):
+    """The shared prefix attended once for all rows: the B decode queries form
+    one row of attn_prefill_paged (q_len = B, non-causal, the prefix pages as
+    its cache), so the prefix K/V are read once and the B queries are MMA
+    rows; each row's own suffix goes through the decode kernel; the pair merge
+    joins them. Equals the attention over prefix + suffix."""
+    shape = W.DECODE_S32K  # h=32, h_kv=8, d_h=128
+    B = 6
+    g = torch.Generator().manual_seed(12)
+    suffix = torch.randint(1, 700, (B,), generator=g).tolist()
+    suffix[4] = 0
+    pre_len = prefix_pages * W.PAGE_SIZE
+    pool, full, pre_tab, sfx_tab = cascade_layout(B, prefix_pages, suffix, 6)
+    q = W.normal((B, shape.h, shape.d_h), 50, torch.bfloat16)
+    kc = W.normal((pool, W.PAGE_SIZE, shape.h_kv, shape.d_h), 51, torch.bfloat16)
+    vc = W.normal((pool, W.PAGE_SIZE, shape.h_kv, shape.d_h), 52, torch.bfloat16)
+    full_len = torch.tensor([pre_len + s for s in suffix], dtype=torch.int32)
+    O_ref, L_ref = oracle.decode_paged_ref(q, kc, vc, full, full_len, shape.scale)
+
+    dq, dk, dv = q.cuda(), kc.cuda(), vc.cuda()
+    op, lp = attn.attn_prefill_paged(dq, dk, dv, pre_tab[:1].contiguous().cuda(),
+                                     torch.tensor([0, B], dtype=torch.int32).cuda(),
+                                     torch.tensor([pre_len], dtype=torch.int32).cuda(), B,
+                                     causal=False, scale=shape.scale)
+    os_, ls = attn.attn_decode_paged(dq, dk, dv, sfx_tab.cuda(),
+                                     torch.tensor(suffix, dtype=torch.int32).cuda(), 4, shape.scale)
+    o, lse = attn.attn_merge_lse_pair(op, lp, os_, ls)
+    torch.cuda.synchronize()
+    assert attn.attn_get_device_error() == 0
+    check_out(o, O_ref, torch.bfloat16)
+    check_lse(lse, L_ref)
