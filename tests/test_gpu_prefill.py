@@ -62,6 +62,7 @@ def test_fp32_path_shapes(h, h_kv, d, T, causal):
     (4, 1, 128, 127, True),
     (4, 1, 128, 128, False),
     (4, 1, 128, 129, True),
+    (8, 1, 128, 300, True),    # g=8: four head pairs share a KV head
 ])
 def test_bf16_tc_shapes(h, h_kv, d, T, causal):
     shape = W.PrefillShape("t", h, h_kv, d, T, torch.bfloat16, causal)
@@ -93,7 +94,7 @@ def test_bf16_wide_values_keep_exact_path(d):
     q, k, v = W.prefill_inputs(shape, 21)
     v[0, 130, 5] = 3.0e5     # key tile 1 of KV head 0
     v[1, 300, 7] = -7.0e4    # key tile 2 of KV head 1
-    v[1, 20, 0] = 65504.0    # largest fp16 value: tile 0 stays fp16
+    v[1, 20, 0] = 65280.0    # largest bf16 below 2^16 (fits fp16): tile 0 stays fp16
     O_ref, L_ref = oracle.attention_ref(q, k, v, shape.scale, True)
     o, lse = run(q, k, v, True, shape.scale)
     check_out(o, O_ref, torch.bfloat16)
