@@ -126,3 +126,15 @@ def test_decode_output_guard_bands_untouched():
     assert torch.all(torch.isnan(buf[:1024].float())) and torch.all(torch.isnan(buf[-1024:].float()))
     O_ref, _ = oracle.decode_paged_ref(q, kc, vc, table, seq, shape.scale)
     check_out(o, O_ref, torch.bfloat16)
+
+
+def test_decode_max_split_count():
+    """The largest split count the API accepts (1024) on a 32k-key row: two
+    pages per split, 1024 partial states per head merged by the 8-warp merge."""
+    shape = W.DECODE_70B_TP8
+    q, kc, vc, table, seq = W.decode_inputs(shape, seed=3, contiguous=True)
+    O_ref, L_ref = oracle.decode_paged_ref(q, kc, vc, table, seq, shape.scale)
+    o, lse = run_decode(q, kc, vc, table, seq, attn.ATTN_MAX_SPLITS)
+    assert attn.attn_get_device_error() == 0
+    check_out(o, O_ref, torch.bfloat16)
+    check_lse(lse, L_ref)

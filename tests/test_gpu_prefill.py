@@ -187,3 +187,17 @@ def test_bf16_output_guard_bands_untouched():
     O_ref, L_ref = oracle.attention_ref(q, k, v, shape.scale, True)
     check_out(o, O_ref, torch.bfloat16)
     check_lse(lse, L_ref)
+
+
+def test_bf16_long_sequence_sampled_rows():
+    """T = 32768 (four times the benchmark length, 256 query tiles per head):
+    sampled rows, including the first, the last and rows around tile edges."""
+    shape = W.PrefillShape("long_T32768", 4, 1, 128, 32768, torch.bfloat16, True)
+    q, k, v = W.prefill_inputs(shape, 13)
+    o, lse = run(q, k, v, True, shape.scale)
+    rows = [0, 1, 127, 128, 16383, 16384, 32639, 32640, 32767]
+    heads = [i % shape.h for i in range(len(rows))]
+    O_ref, L_ref = oracle.attention_rows_ref(q, k, v, shape.scale, True, heads, rows)
+    check_out(o[heads, rows], O_ref, torch.bfloat16)
+    check_lse(lse[heads, rows], L_ref)
+    assert attn.attn_get_device_error() == 0
