@@ -40,6 +40,8 @@ def test_single_head_fp32_T256():
     (4, 2, 64, 257, False),
     (2, 2, 128, 129, True),
     (3, 1, 64, 64, True),
+    (8, 2, 64, 1000, True),   # enough query blocks: no key split
+    (1, 1, 128, 96, False),   # 3 key tiles over a cluster of 2
 ])
 def test_fp32_path_shapes(h, h_kv, d, T, causal):
     shape = W.PrefillShape("t", h, h_kv, d, T, torch.float32, causal)
