@@ -45,16 +45,17 @@ DECODE = W.DECODE_PAGED_B64
 KERNEL_FILES = {
     "prefill": ["online_softmax_attn_gb300/csrc/prefill_tc.cu", "online_softmax_attn_gb300/csrc/tc.cuh",
                 "online_softmax_attn_gb300/csrc/common.cuh"],
-    "decode": ["online_softmax_attn_gb300/csrc/decode.cu", "online_softmax_attn_gb300/csrc/common.cuh"],
+    "decode": ["online_softmax_attn_gb300/csrc/decode.cu", "online_softmax_attn_gb300/csrc/common.cuh",
+               "online_softmax_attn_gb300/csrc/pdl.cuh"],
 }
 KERNEL_FILES["prefill_paged"] = KERNEL_FILES["prefill"]
 NCU_TRAFFIC = {
     # kind: (dram read + write bytes per launch, sha256[:16] of the kernel's files)
     "prefill": (131.56e6, "fc47ea8d2a2af230"),  # profiles/prefill_bf16_T8192_causal.md
     "prefill_paged": (465.41e6, "fc47ea8d2a2af230"),  # profiles/prefill_paged_B8_q1024_ctx8192.md
-    # decode: 16-row capture (304.1 MB for 299.5 MB algorithmic) scaled by KV bytes to the
+    # decode: 16-row capture (304.2 MB for 299.5 MB algorithmic) scaled by KV bytes to the
     # 66-row batch (profiles/decode_split_paged_B16.md)
-    "decode": (2.1527e9, "2a89913c613ae05d"),
+    "decode": (2.1535e9, "a06cbe0e185ddfce"),
 }
 
 

@@ -41,6 +41,7 @@
 //     short rows return at once (CUDA-graph friendly).
 #include "common.cuh"
 #include "internal.h"
+#include "pdl.cuh"
 
 namespace attn {
 
@@ -115,6 +116,9 @@ __global__ void __launch_bounds__(NW * 32, 1)
   const int lane = tid & 31;
   const int gid = lane >> 2;  // MMA row (query head) / key / dim held by this lane
   const int tq = lane & 3;    // column pair within the fragment
+
+  pdl_wait();     // q, seq_lens, the split plan and the partials' buffers are the previous kernel's
+  pdl_trigger();  // the merge may be scheduled once every split CTA is running
 
   // q fragments first: they do not depend on the row length. A-operand
   // layout of m16n8k16: a0 = (row gid, k 2tq..2tq+1), a2 = (row gid, k+8).
@@ -341,11 +345,10 @@ cudaError_t launch_cfg(const DecodeArgs& a, const CUtensorMap& tk, const CUtenso
   if (e != cudaSuccess) return e;
   const dim3 grid(a.num_splits, a.h_kv, a.B);
   const float qscale = a.scale * kLog2e;
-  kern<<<grid, NW * 32, C::SMEM, stream>>>(
-      tk, tv, static_cast<const __nv_bfloat16*>(a.q), a.block_table, a.seq_lens, a.h,
-      a.max_blocks_per_seq, a.num_blocks, a.num_splits, a.fixed_pps, a.pps_dev, qscale, a.o_part,
-      a.m_part, a.l_part);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3(NW * 32), C::SMEM, stream, tk, tv,
+                    static_cast<const __nv_bfloat16*>(a.q), a.block_table, a.seq_lens, a.h,
+                    a.max_blocks_per_seq, a.num_blocks, a.num_splits, a.fixed_pps, a.pps_dev,
+                    qscale, a.o_part, a.m_part, a.l_part);
 }
 
 template <int D>

@@ -22,6 +22,7 @@
 // shared memory.
 #include "common.cuh"
 #include "internal.h"
+#include "pdl.cuh"
 
 namespace attn {
 
@@ -46,6 +47,8 @@ __global__ void __launch_bounds__(256)
   const int warp = threadIdx.x >> 5;
   const int wr = warp % WPR;  // this warp's share of the row
   const int row = blockIdx.x * RPC + warp / WPR;
+  pdl_wait();  // the partials are the previous kernel's output
+  pdl_trigger();
   if (WPR == 1 && row >= rows) return;
   const bool live = row < rows;  // WPR > 1: one row per CTA, always live
 
@@ -190,11 +193,11 @@ cudaError_t launch_merge(const float* o_part, const float* m_part, const float* 
   const dim3 grid(wide ? rows : (rows + 7) / 8);
   const dim3 block(256);
   const bool bf = out_dtype == ATTN_DTYPE_BF16;
-#define ATTN_MERGE_LAUNCH(D, BF, W)                                                              \
-  merge_states_kernel<D, BF, W><<<grid, block, 0, stream>>>(o_part, m_part, l_part, n_active,   \
-                                                            seq_lens, heads_per_seq, page_size, \
-                                                            max_len, rows, num_splits, o, lse, \
-                                                            fixed_pps, pps_dev)
+  cudaError_t e = cudaSuccess;
+#define ATTN_MERGE_LAUNCH(D, BF, W)                                                               \
+  e = launch_pdl(merge_states_kernel<D, BF, W>, grid, block, 0, stream, o_part, m_part, l_part, \
+                 n_active, seq_lens, heads_per_seq, page_size, max_len, rows, num_splits, o, lse, \
+                 fixed_pps, pps_dev)
   if (d_h == 128) {
     if (bf) { if (wide) ATTN_MERGE_LAUNCH(128, true, 8); else ATTN_MERGE_LAUNCH(128, true, 1); }
     else { if (wide) ATTN_MERGE_LAUNCH(128, false, 8); else ATTN_MERGE_LAUNCH(128, false, 1); }
@@ -203,7 +206,7 @@ cudaError_t launch_merge(const float* o_part, const float* m_part, const float* 
     else { if (wide) ATTN_MERGE_LAUNCH(64, false, 8); else ATTN_MERGE_LAUNCH(64, false, 1); }
   }
 #undef ATTN_MERGE_LAUNCH
-  return cudaGetLastError();
+  return e;
 }
 
 // ---------------------------------------------------------------------------
