@@ -51,8 +51,8 @@ KERNEL_FILES = {
 KERNEL_FILES["prefill_paged"] = KERNEL_FILES["prefill"]
 NCU_TRAFFIC = {
     # kind: (dram read + write bytes per launch, sha256[:16] of the kernel's files)
-    "prefill": (131.56e6, "fc47ea8d2a2af230"),  # profiles/prefill_bf16_T8192_causal.md
-    "prefill_paged": (465.41e6, "fc47ea8d2a2af230"),  # profiles/prefill_paged_B8_q1024_ctx8192.md
+    "prefill": (134.78e6, "802fda2386e2b0b1"),  # profiles/prefill_bf16_T8192_causal.md
+    "prefill_paged": (470.27e6, "802fda2386e2b0b1"),  # profiles/prefill_paged_B8_q1024_ctx8192.md
     # decode: 16-row capture (304.2 MB for 299.5 MB algorithmic) scaled by KV bytes to the
     # 66-row batch (profiles/decode_split_paged_B16.md)
     "decode": (2.1535e9, "a06cbe0e185ddfce"),

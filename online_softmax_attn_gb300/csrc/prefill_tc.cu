@@ -624,21 +624,44 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
       const bool empty = !(l > 0.f);
       const float inv = empty ? 0.f : 1.f / l;
       const size_t orow_idx = PAGED ? size_t(q_tok0 + row) * h + hq : size_t(hq) * T + row;
-      __nv_bfloat16* orow = o + orow_idx * D;
+      // O leaves through this warp's quarter of its head's Q tile (the head's
+      // last S MMA, Q's last reader, completed before o_final). Each thread
+      // writes its row there in 16-byte chunks, chunk index XOR (row mod 8) so
+      // the 8 rows of a store phase hit distinct banks; then the warp stores
+      // whole rows, 256 (d_h = 128) or 128 contiguous bytes per row, instead of
+      // 32 rows x 16 bytes per instruction.
+      constexpr int RB = D * 2;    // bytes per O row
+      constexpr int CH = RB / 16;  // 16-byte chunks per row
+      constexpr int RPI = 32 / CH; // rows per warp store instruction
+      uint8_t* stage = smem + C::Q_OFF + t * C::QTILE + wq * (32 * RB);
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t ov[32];
         tc::ld32(tO + c * 32, ov);
         tc::wait_ld();
-        if (row_valid) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            uint4 pk;
-            pk.x = pack_bf16x2(__uint_as_float(ov[8 * i + 0]) * inv, __uint_as_float(ov[8 * i + 1]) * inv);
-            pk.y = pack_bf16x2(__uint_as_float(ov[8 * i + 2]) * inv, __uint_as_float(ov[8 * i + 3]) * inv);
-            pk.z = pack_bf16x2(__uint_as_float(ov[8 * i + 4]) * inv, __uint_as_float(ov[8 * i + 5]) * inv);
-            pk.w = pack_bf16x2(__uint_as_float(ov[8 * i + 6]) * inv, __uint_as_float(ov[8 * i + 7]) * inv);
-            *reinterpret_cast<uint4*>(orow + c * 32 + 8 * i) = pk;
+        for (int i = 0; i < 4; ++i) {
+          uint4 pk;
+          pk.x = pack_bf16x2(__uint_as_float(ov[8 * i + 0]) * inv, __uint_as_float(ov[8 * i + 1]) * inv);
+          pk.y = pack_bf16x2(__uint_as_float(ov[8 * i + 2]) * inv, __uint_as_float(ov[8 * i + 3]) * inv);
+          pk.z = pack_bf16x2(__uint_as_float(ov[8 * i + 4]) * inv, __uint_as_float(ov[8 * i + 5]) * inv);
+          pk.w = pack_bf16x2(__uint_as_float(ov[8 * i + 6]) * inv, __uint_as_float(ov[8 * i + 7]) * inv);
+          const int ch = c * 4 + i;
+          *reinterpret_cast<uint4*>(stage + lane * RB + ((ch ^ (lane & 7)) << 4)) = pk;
+        }
+      }
+      __syncwarp();
+      {
+        const int ch = lane % CH;
+#pragma unroll
+        for (int it = 0; it < 32 / RPI; ++it) {
+          const int rr = it * RPI + lane / CH;  // row within this warp's 32
+          const int qrow = qb * kBM + wq * 32 + rr;
+          if (PAGED ? qrow < q_len : qrow < T) {
+            const uint4 x =
+                *reinterpret_cast<const uint4*>(stage + rr * RB + ((ch ^ (rr & 7)) << 4));
+            const size_t oi = PAGED ? size_t(q_tok0 + qrow) * h + hq : size_t(hq) * T + qrow;
+            *reinterpret_cast<uint4*>(o + oi * D + ch * 8) = x;
           }
         }
       }
