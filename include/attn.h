@@ -57,7 +57,8 @@ typedef enum {
   ATTN_ERR_INVALID_ARG = 1,
   ATTN_ERR_UNSUPPORTED = 2,
   ATTN_ERR_CUDA = 3,
-  ATTN_ERR_DEVICE = 4
+  ATTN_ERR_DEVICE = 4,        /* a device error bit other than a wait timeout */
+  ATTN_ERR_DEVICE_TIMEOUT = 5 /* a kernel's bounded wait gave up               */
 } attn_status_t;
 
 typedef enum { ATTN_DTYPE_F32 = 0, ATTN_DTYPE_BF16 = 1 } attn_dtype_t;
@@ -445,6 +446,17 @@ attn_status_t attn_merge_lse_pair(const void* o_a, const float* lse_a, const voi
  * into *bits. Returns ATTN_ERR_CUDA if the synchronisation fails.
  */
 attn_status_t attn_get_device_error(void* stream, unsigned int* bits);
+
+/*
+ * attn_get_last_device_error -- the same query as a status: synchronise
+ * `stream`, read and clear the device error word, and return ATTN_OK when it
+ * was 0, ATTN_ERR_DEVICE_TIMEOUT when ATTN_DEVERR_WAIT_TIMEOUT was set (a
+ * bounded wait gave up; that kernel's outputs are undefined), ATTN_ERR_DEVICE
+ * for any other bit (a page index outside the cache, a clamped seq_len, a
+ * failed tensor-memory allocation), or ATTN_ERR_CUDA if the synchronisation
+ * fails.
+ */
+attn_status_t attn_get_last_device_error(void* stream);
 
 /*
  * attn_selftest_wait_timeout -- exercise the failure path of the kernels'

@@ -25,12 +25,14 @@ __all__ = [
     "attn_recommended_splits",
     "attn_decode_workspace_bytes",
     "attn_get_device_error",
+    "attn_get_last_device_error",
     "attn_status_string",
     "library",
     "ATTN_MAX_SPLITS",
 ]
 
-ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_DEVICE = range(5)
+(ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_DEVICE,
+ ATTN_ERR_DEVICE_TIMEOUT) = range(6)
 ATTN_DTYPE_F32, ATTN_DTYPE_BF16 = 0, 1
 ATTN_MAX_SPLITS = 1024
 DEVERR_NAMES = {0x1: "wait timeout", 0x2: "page index outside cache",
@@ -96,6 +98,8 @@ def library() -> ctypes.CDLL:
     lib.attn_merge_lse_pair.restype = I
     lib.attn_get_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint)]
     lib.attn_get_device_error.restype = I
+    lib.attn_get_last_device_error.argtypes = [P]
+    lib.attn_get_last_device_error.restype = I
     _lib = lib
     return lib
 
@@ -460,6 +464,16 @@ def attn_get_device_error(stream=None) -> int:
     st = library().attn_get_device_error(_stream(stream), ctypes.byref(bits))
     _check("attn_get_device_error", st)
     return bits.value
+
+
+def attn_get_last_device_error(stream=None) -> int:
+    """Synchronise the stream, clear the device error bits, and return them as
+    a status: ATTN_OK, ATTN_ERR_DEVICE_TIMEOUT (a bounded wait gave up) or
+    ATTN_ERR_DEVICE (any other bit). A failed synchronisation raises."""
+    st = library().attn_get_last_device_error(_stream(stream))
+    if st == ATTN_ERR_CUDA:
+        _check("attn_get_last_device_error", st)
+    return st
 
 
 ATTN_DECODE_STATIC_SCRATCH_BYTES = 16 * 1024 * 1024

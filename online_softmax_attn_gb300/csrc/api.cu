@@ -1,7 +1,7 @@
 // api.cu -- the C ABI declared in include/attn.h: host-side validation,
 // workspace carve-up, tensor-map encoding and kernel launches. No entry point
-// here allocates, frees or synchronises (except attn_get_device_error, which
-// is a synchronising query by contract); the host-memory prefill, with its
+// here allocates, frees or synchronises (except attn_get_device_error and
+// attn_get_last_device_error, synchronising queries by contract); the host-memory prefill, with its
 // copy streams, lives in host_prefill.cu.
 #include <cudaTypedefs.h>
 
@@ -59,11 +59,12 @@ const char* attn_status_string(attn_status_t status) {
     case ATTN_ERR_UNSUPPORTED: return "unsupported shape or dtype";
     case ATTN_ERR_CUDA: return "CUDA error";
     case ATTN_ERR_DEVICE: return "device-side error";
+    case ATTN_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
   }
   return "unknown status";
 }
 
-int attn_version(void) { return 201; }
+int attn_version(void) { return 202; }
 
 int attn_decode_split_plan(int seq_len, int page_size, int num_splits, int* pages_per_split) {
   if (seq_len < 0 || page_size < 1 || num_splits < 1) return -1;
@@ -377,6 +378,14 @@ attn_status_t attn_get_device_error(void* stream, unsigned int* bits) {
   *bits = v;
   if (e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess) return ATTN_ERR_CUDA;
   return ATTN_OK;
+}
+
+attn_status_t attn_get_last_device_error(void* stream) {
+  unsigned int bits = 0;
+  const attn_status_t st = attn_get_device_error(stream, &bits);
+  if (st != ATTN_OK) return st;
+  if (bits & ATTN_DEVERR_WAIT_TIMEOUT) return ATTN_ERR_DEVICE_TIMEOUT;
+  return bits ? ATTN_ERR_DEVICE : ATTN_OK;
 }
 
 }  // extern "C"

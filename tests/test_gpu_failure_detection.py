@@ -34,6 +34,15 @@ def test_wait_runs_out_and_is_reported():
     assert attn.attn_get_device_error() == 0  # read clears
 
 
+def test_timeout_as_status():
+    """The status form of the query: ATTN_ERR_DEVICE_TIMEOUT after a wait ran
+    out, ATTN_OK once read."""
+    assert attn.attn_get_last_device_error() == attn.ATTN_OK
+    attn.attn_selftest_wait_timeout(300)
+    assert attn.attn_get_last_device_error() == attn.ATTN_ERR_DEVICE_TIMEOUT
+    assert attn.attn_get_last_device_error() == attn.ATTN_OK
+
+
 def test_context_usable_after_timeout():
     attn.attn_selftest_wait_timeout(500)
     assert attn.attn_get_device_error() & WAIT_TIMEOUT
