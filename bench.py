@@ -49,6 +49,8 @@ KERNEL_FILES = {
                "online_softmax_attn_gb300/csrc/pdl.cuh"],
 }
 KERNEL_FILES["prefill_paged"] = KERNEL_FILES["prefill"]
+KERNEL_FILES["merge_pair"] = ["online_softmax_attn_gb300/csrc/merge.cu", "online_softmax_attn_gb300/csrc/common.cuh",
+                              "online_softmax_attn_gb300/csrc/pdl.cuh"]
 NCU_TRAFFIC = {
     # kind: (dram read + write bytes per launch, sha256[:16] of the kernel's files)
     "prefill": (134.78e6, "802fda2386e2b0b1"),  # profiles/prefill_bf16_T8192_causal.md
@@ -56,6 +58,9 @@ NCU_TRAFFIC = {
     # decode: 16-row capture (304.2 MB for 299.5 MB algorithmic) scaled by KV bytes to the
     # 66-row batch (profiles/decode_split_paged_B16.md)
     "decode": (2.1535e9, "a06cbe0e185ddfce"),
+    # merge_pair: full-size capture; reads are the compulsory 136.3 MB, writes 38.2 MB of the
+    # 68.2 MB output (the rest still in L2 at exit) (profiles/merge_pair_262144x128.md)
+    "merge_pair": (174.55e6, "d3208992c70651d7"),
 }
 
 
@@ -284,6 +289,13 @@ def run_gpu(args, world, rank, local):
         res = measure_prefill_paged(dev, flush, tc_peak, peak_kind, iters=max(1, args.steps))
         if rank == 0:
             print(json.dumps({"only": "prefill_paged", "prefill_paged": res}), flush=True)
+        return
+    if args.only == "merge_pair":
+        # The pairwise merge measurement alone (profiler captures).
+        flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+        res = measure_merge_pair(dev, flush, hbm_peak, peak_kind, iters=max(1, args.steps))
+        if rank == 0:
+            print(json.dumps({"only": "merge_pair", "merge_pair": res}), flush=True)
         return
 
     # ---- inputs, resident in HBM before the timed region ----
@@ -649,36 +661,59 @@ def measure_decode_batch1(dev, hbm_peak, peak_kind):
 def measure_merge_pair(dev, flush, hbm_peak, peak_kind, iters=20):
     """Pairwise (O, LSE) merge of two prefill-shaped results (32 heads x 8192
     tokens, d_h 128, bf16 in and out): the prefix / suffix combine. HBM-bound;
-    204 MB per call, L2 flushed before each call."""
+    204 MB per call. A single call is ~35 us, so the host's launch time would
+    show in an event pair around one call: the calls are timed as a CUDA graph
+    of back-to-back calls alternating between two input sets (268 MB of
+    inputs, twice L2), so every call reads its inputs from HBM. `flush` is
+    unused (kept for the common signature)."""
     import online_softmax_attn_gb300 as attn
 
     rows, d = PREFILL.h * PREFILL.T, PREFILL.d_h
     g = torch.Generator(device=dev)
     g.manual_seed(7)
-    oa = torch.randn(rows, d, generator=g, device=dev).to(torch.bfloat16)
-    ob = torch.randn(rows, d, generator=g, device=dev).to(torch.bfloat16)
-    la = torch.randn(rows, generator=g, device=dev) * 20
-    lb = torch.randn(rows, generator=g, device=dev) * 20
-    o = torch.empty_like(oa)
-    lse = torch.empty_like(la)
-    for _ in range(3):
-        attn.attn_merge_lse_pair(oa, la, ob, lb, o=o, lse=lse)
+    sets = []
+    for _ in range(2):
+        oa = torch.randn(rows, d, generator=g, device=dev).to(torch.bfloat16)
+        ob = torch.randn(rows, d, generator=g, device=dev).to(torch.bfloat16)
+        la = torch.randn(rows, generator=g, device=dev) * 20
+        lb = torch.randn(rows, generator=g, device=dev) * 20
+        sets.append((oa, la, ob, lb))
+    o = torch.empty_like(sets[0][0])
+    lse = torch.empty_like(sets[0][1])
+    n = 10
+
+    def calls():
+        for i in range(n):
+            oa, la, ob, lb = sets[i % 2]
+            attn.attn_merge_lse_pair(oa, la, ob, lb, o=o, lse=lse)
+
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        calls()  # warm-up outside the capture
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            calls()
+    graph.replay()
+    torch.cuda.synchronize(dev)
     ms = []
-    for _ in range(iters):
-        flush.fill_(1)
+    for _ in range(max(3, iters)):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
-        attn.attn_merge_lse_pair(oa, la, ob, lb, o=o, lse=lse)
+        graph.replay()
         b.record()
         b.synchronize()
-        ms.append(a.elapsed_time(b))
+        ms.append(a.elapsed_time(b) / n)
     t = statistics.median(ms)
     nbytes = rows * (2 * d * 2 + 2 * 4 + d * 2 + 4)
     gbs = nbytes / (t * 1e-3) / 1e9
     return {"value": gbs, "unit": "GB/s", "ms": t, "rows": rows, "d_h": d, "bytes": nbytes,
+            "timing": f"CUDA graph of {n} calls",
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": gbs / hbm_peak, "traffic": None, "kernel": "merge_pair_kernel",
-                         "peak_source": f"{peak_kind} copy bandwidth"}}
+                         "frac": gbs / hbm_peak, "traffic": traffic_for("merge_pair"),
+                         "kernel": "merge_pair_kernel", "peak_source": f"{peak_kind} copy bandwidth"}}
 
 
 def main():
@@ -695,9 +730,9 @@ def main():
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the measurements outside the step (deterministic / adaptive decode, "
                          "pair merge, paged prefill), e.g. for a launch list of the step alone")
-    ap.add_argument("--only", choices=["prefill", "decode", "prefill_paged"], default=None,
-                    help="run one half of the step, or the paged prefill measurement alone "
-                         "(profiler captures; not a bench line)")
+    ap.add_argument("--only", choices=["prefill", "decode", "prefill_paged", "merge_pair"], default=None,
+                    help="run one half of the step, or the paged prefill or pair merge measurement "
+                         "alone (profiler captures; not a bench line)")
     ap.add_argument("--decode-rows", type=int, default=0,
                     help="truncate the decode batch (profiler captures; not a bench line)")
     args = ap.parse_args()
