@@ -474,6 +474,7 @@ def run_gpu(args, world, rank, local):
     extras = args.only is None and not args.no_extras
     merge_pair = measure_merge_pair(dev, flush, hbm_peak, peak_kind) if extras else None
     decode_b1 = measure_decode_batch1(dev, hbm_peak, peak_kind) if extras else None
+    prefill_2048 = measure_prefill_t2048(dev, flush, tc_peak, peak_kind) if extras else None
     prefill_paged = measure_prefill_paged(dev, flush, tc_peak, peak_kind) if extras else None
 
     # ---- CPU oracle baseline (rank 0, N = 1 only) ----
@@ -543,6 +544,7 @@ def run_gpu(args, world, rank, local):
         },
         "merge_pair": merge_pair,
         "decode_batch1": decode_b1,
+        "prefill_T2048": prefill_2048,
         "prefill_paged": prefill_paged,
         "prefill_ms": pre_avg,
         "e2e": e2e,
@@ -598,6 +600,73 @@ def measure_prefill_paged(dev, flush, tc_peak, peak_kind, iters=10):
             "roofline": {"bound": "tensor", "achieved": tf, "peak": tc_peak, "unit": "TFLOP/s",
                          "frac": tf / tc_peak, "traffic": traffic_for("prefill_paged"),
                          "kernel": "prefill_bf16_kernel (paged)",
+                         "peak_source": f"{peak_kind} bf16 burst"}}
+
+
+def measure_prefill_t2048(dev, flush, tc_peak, peak_kind, iters=15):
+    """The T=2048 causal GQA layer (h=32, h_kv=8, d_h=128, bf16 N(0,1)): a
+    call is ~40 us, so it is timed two ways -- an event pair around one call
+    after an L2 flush, and a CUDA graph of back-to-back calls whose inputs
+    rotate over copies larger than three times L2."""
+    import online_softmax_attn_gb300 as attn
+
+    sh = W.GQA_T2048_CAUSAL
+    q, k, v = W.prefill_inputs(sh, 0, device=dev)
+    flops = prefill_flops(sh)
+    ws = torch.empty(attn.attn_prefill_workspace_bytes(sh.T, sh.h_kv, sh.d_h), dtype=torch.uint8,
+                     device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((sh.h, sh.T), dtype=torch.float32, device=dev)
+    for _ in range(3):
+        attn.attn_prefill(q, k, v, True, sh.scale, o=o, lse=lse, workspace=ws)
+    ms = []
+    for _ in range(iters):
+        flush.fill_(1)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        attn.attn_prefill(q, k, v, True, sh.scale, o=o, lse=lse, workspace=ws)
+        b.record()
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    t_ev = statistics.median(ms)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    per = (q.numel() + k.numel() + v.numel()) * q.element_size() * 2  # inputs and output
+    copies = max(2, -(-3 * l2 // per))
+    sets = [(q.clone(), k.clone(), v.clone(), torch.empty_like(o), torch.empty_like(lse))
+            for _ in range(copies)]
+    n = 4 * copies
+
+    def calls():
+        for i in range(n):
+            q_, k_, v_, o_, l_ = sets[i % copies]
+            attn.attn_prefill(q_, k_, v_, True, sh.scale, o=o_, lse=l_, workspace=ws)
+
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        calls()
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            calls()
+    graph.replay()
+    torch.cuda.synchronize(dev)
+    gms = []
+    for _ in range(5):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        graph.replay()
+        b.record()
+        b.synchronize()
+        gms.append(a.elapsed_time(b) / n)
+    t_g = statistics.median(gms)
+    tf = flops / (t_g * 1e-3) / 1e12
+    return {"value": tf, "unit": "TFLOP/s", "us_per_call": t_g * 1e3, "flops": flops,
+            "timing": f"CUDA graph of {n} calls", "event_single_call_us": t_ev * 1e3,
+            "event_single_call_tflops": flops / (t_ev * 1e-3) / 1e12,
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": tc_peak, "unit": "TFLOP/s",
+                         "frac": tf / tc_peak, "traffic": None, "kernel": "prefill_bf16_kernel",
                          "peak_source": f"{peak_kind} bf16 burst"}}
 
 
