@@ -44,7 +44,7 @@ DECODE = W.DECODE_PAGED_B64
 # valid only for the kernel source it was taken on (hash of its files).
 KERNEL_FILES = {
     "prefill": ["online_softmax_attn_gb300/csrc/prefill_tc.cu", "online_softmax_attn_gb300/csrc/tc.cuh",
-                "online_softmax_attn_gb300/csrc/common.cuh"],
+                "online_softmax_attn_gb300/csrc/common.cuh", "online_softmax_attn_gb300/csrc/pdl.cuh"],
     "decode": ["online_softmax_attn_gb300/csrc/decode.cu", "online_softmax_attn_gb300/csrc/common.cuh",
                "online_softmax_attn_gb300/csrc/pdl.cuh"],
 }
@@ -53,14 +53,14 @@ KERNEL_FILES["merge_pair"] = ["online_softmax_attn_gb300/csrc/merge.cu", "online
                               "online_softmax_attn_gb300/csrc/pdl.cuh"]
 NCU_TRAFFIC = {
     # kind: (dram read + write bytes per launch, sha256[:16] of the kernel's files)
-    "prefill": (134.78e6, "802fda2386e2b0b1"),  # profiles/prefill_bf16_T8192_causal.md
-    "prefill_paged": (470.27e6, "802fda2386e2b0b1"),  # profiles/prefill_paged_B8_q1024_ctx8192.md
+    "prefill": (135.69e6, "da3696db4c148a93"),  # profiles/prefill_bf16_T8192_causal.md
+    "prefill_paged": (476.59e6, "da3696db4c148a93"),  # profiles/prefill_paged_B8_q1024_ctx8192.md
     # decode: 16-row capture (304.2 MB for 299.5 MB algorithmic) scaled by KV bytes to the
     # 66-row batch (profiles/decode_split_paged_B16.md)
-    "decode": (2.1535e9, "a06cbe0e185ddfce"),
+    "decode": (2.1535e9, "e4b016c0f09f5526"),
     # merge_pair: full-size capture; reads are the compulsory 136.3 MB, writes 38.2 MB of the
     # 68.2 MB output (the rest still in L2 at exit) (profiles/merge_pair_262144x128.md)
-    "merge_pair": (174.55e6, "d3208992c70651d7"),
+    "merge_pair": (174.55e6, "054155b75fe86019"),
 }
 
 

@@ -1,9 +1,10 @@
-// pdl.cuh -- programmatic dependent launch (sm_90 and later) for the decode
-// pair: the split kernel lets the merge kernel be scheduled while it runs, and
-// each kernel holds its first dependent memory access until the previous grid
-// on the stream has finished and its writes are visible. A kernel launched
+// pdl.cuh -- programmatic dependent launch (sm_90 and later): the decode
+// split kernel lets the merge kernel be scheduled while it runs, and the
+// prefill's V pass lets the attention kernel set up and load Q and K; each
+// dependent kernel holds its first access to the previous grid's output until
+// that grid has finished and its writes are visible. A kernel launched
 // without the attribute passes the wait at once; ordering is never weaker
-// than plain stream order.
+// than plain stream order for the data the wait guards.
 #pragma once
 #include <cuda_runtime.h>
 

@@ -38,6 +38,7 @@
 //   word, drains its copies and MMAs (bounded), frees tensor memory and exits.
 #include "common.cuh"
 #include "internal.h"
+#include "pdl.cuh"
 #include "tc.cuh"
 
 namespace attn {
@@ -326,6 +327,9 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
         load_tile(sbase + C::K_OFF + sk * C::KTILE, &tmap_k, bars.k_full(sk), j);
         k_issued = j + 1;
         if (j >= NSV && !wait_or_abort(bars.v_empty(sv), ((j / NSV) - 1) & 1, abort_flag)) break;
+        // Q and K are older than the V pass, so they load before this wait;
+        // the fp16 V copy and the tile flags are the V pass's output.
+        if (j == 0) pdl_wait();
         mbar_arrive_expect_tx(bars.v_full(sv), C::KTILE);
         const bool v_wide = is_wide(j);
         if (PAGED && !v_wide) {
@@ -413,6 +417,7 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
       // Order per key tile j: P_0 V_j, S_0(j+1), P_1 V_j, S_1(j+1): each head's
       // next QK^T follows its own P V (P aliases S in tensor memory), and the
       // other head's softmax runs while these MMAs execute.
+      pdl_wait();  // the tile flags below are the V pass's output
       for (int j = 0; ok && j < nkv; ++j) {
         const int sv = j % NSV;
         const int sk1 = (j + 1) % NSK;
@@ -458,6 +463,7 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
     float m_ref = -INFINITY;
     float l = 0.f;
     bool ok = true;
+    pdl_wait();  // the tile flags are the V pass's output
     for (int j = 0; j < nkv; ++j) {
       // The format of P follows the format of this key tile's V.
       const bool wide = is_wide(j);
@@ -686,6 +692,9 @@ __global__ void __launch_bounds__(256)
     v_to_f16_kernel(const uint4* __restrict__ v, uint4* __restrict__ v16, int* __restrict__ vwide,
                     int T, int chunks_per_row, int n_tiles) {
   const int tile = blockIdx.x, kvh = blockIdx.y;
+  // The attention kernel (a programmatic dependent) may start its CTAs'
+  // set-up and Q, K loads now; it waits for this grid before touching V.
+  pdl_trigger();
   const int rows = min(kBN, T - tile * kBN);
   const size_t base = (size_t(kvh) * T + size_t(tile) * kBN) * chunks_per_row;
   const int n = rows * chunks_per_row;
@@ -794,7 +803,14 @@ cudaError_t launch(const void* q, const void* k, const void* v, const void* v16,
   const int n_qblk = (T + kBM - 1) / kBM;
   if (n_qblk > 65535) return cudaErrorNotSupported;  // query tiles index grid y
   const dim3 grid(h / NQ, n_qblk);
-  kern<<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tv16, v16 ? vwide : nullptr,
+  // After the V pass the kernel is its programmatic dependent (it waits for
+  // that grid before reading V or the flags); without one it follows
+  // whatever precedes it on the stream in plain order.
+  if (v16)
+    return launch_pdl(kern, grid, dim3(C::THREADS), C::SMEM, stream, tq, tk, tv, tv16, vwide,
+                      static_cast<__nv_bfloat16*>(o), lse, T, h, h_kv, causal, scale * kLog2e,
+                      n_qblk, PagedArgs{});
+  kern<<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tv16, nullptr,
                                                static_cast<__nv_bfloat16*>(o), lse, T, h, h_kv,
                                                causal, scale * kLog2e, n_qblk, PagedArgs{});
   return cudaGetLastError();
