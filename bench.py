@@ -53,8 +53,8 @@ KERNEL_FILES["merge_pair"] = ["online_softmax_attn_gb300/csrc/merge.cu", "online
                               "online_softmax_attn_gb300/csrc/pdl.cuh"]
 NCU_TRAFFIC = {
     # kind: (dram read + write bytes per launch, sha256[:16] of the kernel's files)
-    "prefill": (135.69e6, "da3696db4c148a93"),  # profiles/prefill_bf16_T8192_causal.md
-    "prefill_paged": (476.59e6, "da3696db4c148a93"),  # profiles/prefill_paged_B8_q1024_ctx8192.md
+    "prefill": (135.65e6, "54c8b6f9626d119d"),  # profiles/prefill_bf16_T8192_causal.md
+    "prefill_paged": (465.07e6, "54c8b6f9626d119d"),  # profiles/prefill_paged_B8_q1024_ctx8192.md
     # decode: 16-row capture (304.2 MB for 299.5 MB algorithmic) scaled by KV bytes to the
     # 66-row batch (profiles/decode_split_paged_B16.md)
     "decode": (2.1535e9, "e4b016c0f09f5526"),

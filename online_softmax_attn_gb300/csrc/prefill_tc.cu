@@ -699,19 +699,33 @@ __global__ void __launch_bounds__(256)
   const size_t base = (size_t(kvh) * T + size_t(tile) * kBN) * chunks_per_row;
   const int n = rows * chunks_per_row;
   uint32_t mx = 0;
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    const uint4 x = v[base + i];
-    uint32_t m2;
-    asm("max.u16x2 %0, %1, %2;" : "=r"(m2) : "r"(x.x & 0x7fff7fffu), "r"(x.y & 0x7fff7fffu));
-    asm("max.u16x2 %0, %0, %1;" : "+r"(m2) : "r"(x.z & 0x7fff7fffu));
-    asm("max.u16x2 %0, %0, %1;" : "+r"(m2) : "r"(x.w & 0x7fff7fffu));
-    asm("max.u16x2 %0, %0, %1;" : "+r"(mx) : "r"(m2));
-    uint4 y;
-    y.x = pack_f16x2(bf16lo(x.x), bf16hi(x.x));
-    y.y = pack_f16x2(bf16lo(x.y), bf16hi(x.y));
-    y.z = pack_f16x2(bf16lo(x.z), bf16hi(x.z));
-    y.w = pack_f16x2(bf16lo(x.w), bf16hi(x.w));
-    v16[base + i] = y;
+  // All of a thread's loads (8 at d_h = 128) are in flight before the first
+  // conversion: the pass is latency-bound at small T otherwise.
+  constexpr int kU = 8;
+  for (int i0 = threadIdx.x; i0 < n; i0 += kU * blockDim.x) {
+    uint4 x[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int i = i0 + u * blockDim.x;
+      if (i < n) x[u] = v[base + i];
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int i = i0 + u * blockDim.x;
+      if (i < n) {
+        uint32_t m2;
+        asm("max.u16x2 %0, %1, %2;" : "=r"(m2) : "r"(x[u].x & 0x7fff7fffu), "r"(x[u].y & 0x7fff7fffu));
+        asm("max.u16x2 %0, %0, %1;" : "+r"(m2) : "r"(x[u].z & 0x7fff7fffu));
+        asm("max.u16x2 %0, %0, %1;" : "+r"(m2) : "r"(x[u].w & 0x7fff7fffu));
+        asm("max.u16x2 %0, %0, %1;" : "+r"(mx) : "r"(m2));
+        uint4 y;
+        y.x = pack_f16x2(bf16lo(x[u].x), bf16hi(x[u].x));
+        y.y = pack_f16x2(bf16lo(x[u].y), bf16hi(x[u].y));
+        y.z = pack_f16x2(bf16lo(x[u].z), bf16hi(x[u].z));
+        y.w = pack_f16x2(bf16lo(x[u].w), bf16hi(x[u].w));
+        v16[base + i] = y;
+      }
+    }
   }
   // bf16 bits 0x4780 = 2^16: the first magnitude fp16 cannot hold.
   const int wide = __syncthreads_or((mx & 0xffffu) >= 0x4780u || (mx >> 16) >= 0x4780u);
