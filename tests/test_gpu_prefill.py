@@ -25,9 +25,9 @@ def run(q, k, v, causal, scale):
 
 
 def test_single_head_fp32_T256():
-    """The fp32 single-head workload, exactly as specified, full comparison."""
+    """The fp32 single-head workload, exactly as specified (seeds 0-4), full comparison."""
     shape = W.SINGLE_HEAD_T256
-    for seed in range(3):
+    for seed in range(5):
         q, k, v = W.prefill_inputs(shape, seed)
         O_ref, L_ref = oracle.attention_ref(q, k, v, shape.scale, causal=False)
         o, lse = run(q, k, v, False, shape.scale)
