@@ -55,9 +55,9 @@ NCU_TRAFFIC = {
     # kind: (dram read + write bytes per launch, sha256[:16] of the kernel's files)
     "prefill": (135.65e6, "54c8b6f9626d119d"),  # profiles/prefill_bf16_T8192_causal.md
     "prefill_paged": (465.07e6, "54c8b6f9626d119d"),  # profiles/prefill_paged_B8_q1024_ctx8192.md
-    # decode: 16-row capture (304.2 MB for 299.5 MB algorithmic) scaled by KV bytes to the
+    # decode: 16-row capture (304.1 MB for 299.5 MB algorithmic) scaled by KV bytes to the
     # 66-row batch (profiles/decode_split_paged_B16.md)
-    "decode": (2.1535e9, "e4b016c0f09f5526"),
+    "decode": (2.1524e9, "47156151a0f7135e"),
     # merge_pair: full-size capture; reads are the compulsory 136.3 MB, writes 38.2 MB of the
     # 68.2 MB output (the rest still in L2 at exit) (profiles/merge_pair_262144x128.md)
     "merge_pair": (174.55e6, "054155b75fe86019"),
@@ -289,6 +289,12 @@ def run_gpu(args, world, rank, local):
         res = measure_prefill_paged(dev, flush, tc_peak, peak_kind, iters=max(1, args.steps))
         if rank == 0:
             print(json.dumps({"only": "prefill_paged", "prefill_paged": res}), flush=True)
+        return
+    if args.only == "decode_batch1":
+        # The batch-1 decode measurements alone (profiler captures).
+        res = measure_decode_batch1(dev, hbm_peak, peak_kind)
+        if rank == 0:
+            print(json.dumps({"only": "decode_batch1", "decode_batch1": res}), flush=True)
         return
     if args.only == "merge_pair":
         # The pairwise merge measurement alone (profiler captures).
@@ -673,14 +679,14 @@ def measure_prefill_t2048(dev, flush, tc_peak, peak_kind, iters=15):
 def measure_decode_batch1(dev, hbm_peak, peak_kind):
     """Batch-1 decode (one query token per call) over a contiguous 32768-key
     cache: h=32 / h_kv=8 at 16 splits, and the 70B tensor-parallel shard
-    h=8 / h_kv=1 at 64 splits. A single call is a few microseconds, so each
+    h=8 / h_kv=1 at 132 splits. A single call is a few microseconds, so each
     is timed as a CUDA graph of back-to-back calls whose KV caches rotate over
     copies larger than twice L2 (every call reads its cache from HBM)."""
     import online_softmax_attn_gb300 as attn
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     out = {}
-    for shape, splits in ((W.DECODE_S32K, 16), (W.DECODE_70B_TP8, 64)):
+    for shape, splits in ((W.DECODE_S32K, 16), (W.DECODE_70B_TP8, 132)):
         q, kc, vc, tab, seq = W.decode_inputs(shape, 0, device=dev, contiguous=True)
         tab, seq = tab.to(dev), seq.to(dev)
         lens = seq.tolist()
@@ -799,7 +805,8 @@ def main():
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the measurements outside the step (deterministic / adaptive decode, "
                          "pair merge, paged prefill), e.g. for a launch list of the step alone")
-    ap.add_argument("--only", choices=["prefill", "decode", "prefill_paged", "merge_pair"], default=None,
+    ap.add_argument("--only", choices=["prefill", "decode", "prefill_paged", "merge_pair", "decode_batch1"],
+                    default=None,
                     help="run one half of the step, or the paged prefill or pair merge measurement "
                          "alone (profiler captures; not a bench line)")
     ap.add_argument("--decode-rows", type=int, default=0,

@@ -95,6 +95,15 @@ __device__ __forceinline__ uint32_t page_chunk(uint32_t page, int row, int chunk
   return page + (chunk >> 3) * (kPage * 128) + row * 128 + (((chunk & 7) ^ (row & 7)) << 4);
 }
 
+// TMA prefetch of a 4-D tile into L2 (nothing is written to shared memory).
+__device__ __forceinline__ void tma_prefetch_l2_4d(const void* tmap, int c0, int c1, int c2,
+                                                   int c3) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+               : "memory");
+}
+
 template <int D, int G, int NW, int NST>
 __global__ void __launch_bounds__(NW * 32, 1)
     decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
@@ -117,6 +126,35 @@ __global__ void __launch_bounds__(NW * 32, 1)
   const int gid = lane >> 2;  // MMA row (query head) / key / dim held by this lane
   const int tq = lane & 3;    // column pair within the fragment
 
+  // Before the dependency wait, warm L2 with this warp's first NST pages (a
+  // TMA prefetch lands nothing in this SM). The seq_len, split plan and table
+  // entries read here only steer the prefetch: were an earlier kernel still
+  // writing them, some other page would be warmed, and the loads after the
+  // wait read the right ones (L2 is the point of coherence). Only the first
+  // wave of CTAs (one per SM) can start before the previous kernel ends; the
+  // later ones would only request their first pages twice.
+  uint32_t n_sm;
+  asm("mov.u32 %0, %%nsmid;" : "=r"(n_sm));
+  const uint32_t cta = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+  if (lane == 0 && cta < n_sm) {
+    const int sl = min(max(seq_lens[b], 0), max_blocks * kPage);
+    int pps0 = 0;
+    const int n0 = split_plan_fixed(sl, kPage, num_splits, pps_dev ? *pps_dev : fixed_pps, &pps0);
+    if (split < n0) {
+      const int lo = split * pps0, hi = min(lo + pps0, (sl + kPage - 1) / kPage);
+      for (int i = 0; i < NST; ++i) {
+        const int p = lo + warp + NW * i;
+        if (p >= hi) break;
+        const int phys = block_table[size_t(b) * max_blocks + p];
+        if (phys < 0 || phys >= num_blocks) continue;
+#pragma unroll
+        for (int hf = 0; hf < D / 64; ++hf) {
+          tma_prefetch_l2_4d(&tmap_k, hf * 64, kvh, 0, phys);
+          tma_prefetch_l2_4d(&tmap_v, hf * 64, kvh, 0, phys);
+        }
+      }
+    }
+  }
   pdl_wait();     // q, seq_lens, the split plan and the partials' buffers are the previous kernel's
   pdl_trigger();  // the merge may be scheduled once every split CTA is running
 
