@@ -55,9 +55,9 @@ NCU_TRAFFIC = {
     # kind: (dram read + write bytes per launch, sha256[:16] of the kernel's files)
     "prefill": (135.65e6, "54c8b6f9626d119d"),  # profiles/prefill_bf16_T8192_causal.md
     "prefill_paged": (465.07e6, "54c8b6f9626d119d"),  # profiles/prefill_paged_B8_q1024_ctx8192.md
-    # decode: 16-row capture (304.1 MB for 299.5 MB algorithmic) scaled by KV bytes to the
+    # decode: 16-row capture (303.7 MB for 299.5 MB algorithmic) scaled by KV bytes to the
     # 66-row batch (profiles/decode_split_paged_B16.md)
-    "decode": (2.1524e9, "47156151a0f7135e"),
+    "decode": (2.1496e9, "c43dc21389d4e5ce"),
     # merge_pair: full-size capture; reads are the compulsory 136.3 MB, writes 38.2 MB of the
     # 68.2 MB output (the rest still in L2 at exit) (profiles/merge_pair_262144x128.md)
     "merge_pair": (174.55e6, "054155b75fe86019"),

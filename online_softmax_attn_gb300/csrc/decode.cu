@@ -138,10 +138,14 @@ __global__ void __launch_bounds__(NW * 32, 1)
   const uint32_t cta = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
   if (lane == 0 && cta < n_sm) {
     const int sl = min(max(seq_lens[b], 0), max_blocks * kPage);
-    int pps0 = 0;
-    const int n0 = split_plan_fixed(sl, kPage, num_splits, pps_dev ? *pps_dev : fixed_pps, &pps0);
-    if (split < n0) {
-      const int lo = split * pps0, hi = min(lo + pps0, (sl + kPage - 1) / kPage);
+    const int np = (sl + kPage - 1) / kPage;  // 0 .. max_blocks
+    // Pages per split as the plan takes them. A value read this early may be
+    // anything (the plan kernel may not have written it yet), so it is
+    // bounded before use and every table index stays in [0, np).
+    const int fp = pps_dev ? *pps_dev : fixed_pps;
+    const int pps0 = fp > 0 ? min(fp, max(np, 1)) : (np + num_splits - 1) / num_splits;
+    if (pps0 >= 1 && static_cast<long long>(split) * pps0 < np) {
+      const int lo = split * pps0, hi = min(lo + pps0, np);
       for (int i = 0; i < NST; ++i) {
         const int p = lo + warp + NW * i;
         if (p >= hi) break;
