@@ -123,9 +123,9 @@ attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o,
 /*
  * attn_prefill_host -- attn_prefill with Q, K, V in host memory and O, LSE
  * written back to host memory, copies included in the call ([NA] (3), as
- * attn_prefill; heads are independent, so the layer is cut into n_chunks
- * groups of h_kv / n_chunks KV heads with their query heads, and group c+1's
- * inputs copy in while group c computes and group c-1's outputs copy out).
+ * attn_prefill; heads are independent, so the layer is cut into groups of
+ * KV heads with their query heads, and group c+1's inputs copy in while
+ * group c computes and group c-1's outputs copy out).
  * Results are bitwise those of attn_prefill on the same inputs.
  *
  *   q, k, v, o, lse   host pointers, same shapes, dtypes and layouts as
@@ -133,8 +133,11 @@ attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o,
  *                     (cudaHostAlloc / cudaHostRegister) lets the copies run
  *                     asynchronously and overlap; pageable memory works but
  *                     copies through staging.
- *   n_chunks          number of groups, dividing h_kv (at most 64); 0 picks 4
- *                     or 2 when h_kv allows, else 1
+ *   n_chunks          > 0: that many equal groups, dividing h_kv (at most
+ *                     64). 0: with h_kv >= 4, four groups in the proportions
+ *                     3 : 2 : 2 : 1 (the compute and copy-out that nothing
+ *                     overlaps stay short); with h_kv < 4, 2 equal groups
+ *                     when h_kv is even, else 1
  *   scratch           device memory, 256-byte aligned, at least
  *                     attn_prefill_host_scratch_bytes(T, h, h_kv, d_h, dtype)
  *                     bytes: device copies of q, k, v, o, lse and the

@@ -81,12 +81,28 @@ HostScratch host_scratch(int T, int h, int h_kv, int d_h, size_t elem, size_t ws
   return L;
 }
 
-// Groups per call when the caller passes 0: enough to overlap copies and
-// compute, few enough that each group's launch still fills the GPU.
-int auto_chunks(int h_kv) {
-  for (int c : {4, 2})
-    if (h_kv % c == 0) return c;
-  return 1;
+// KV heads per group. n_chunks > 0: equal groups. n_chunks == 0 and
+// h_kv >= 4: four groups in the proportions 3 : 2 : 2 : 1 (a large first
+// group computes while the rest copies in; the small last group keeps short
+// the compute and copy-out that nothing overlaps). Measured with 8 KV heads
+// (T = 8192): 3,2,2,1 ran 0.75 ms against 0.79 for four equal groups, 0.77
+// for 1,2,2,2,1 and 0.80 for 1,3,3,1. With h_kv < 4: 2 equal groups when
+// h_kv is even, else 1. Returns the group count.
+int chunk_plan(int h_kv, int n_chunks, int* sizes) {
+  if (n_chunks == 0 && h_kv >= 4) {
+    const int w[4] = {3, 2, 2, 1};
+    int rest = 0;
+    for (int i = 1; i < 4; ++i) {
+      sizes[i] = (h_kv * w[i] + 4) / 8 > 1 ? (h_kv * w[i] + 4) / 8 : 1;
+      rest += sizes[i];
+    }
+    sizes[0] = h_kv - rest;  // >= 1 for h_kv >= 4
+    return 4;
+  }
+  int c = n_chunks;
+  if (c == 0) c = (h_kv % 2 == 0) ? 2 : 1;
+  for (int i = 0; i < c; ++i) sizes[i] = h_kv / c;
+  return c;
 }
 
 }  // namespace
@@ -122,7 +138,8 @@ attn_status_t attn_prefill_host(const void* q, const void* k, const void* v, voi
   if (!aligned_to(scratch, 256) ||
       scratch_bytes < attn_prefill_host_scratch_bytes(T, h, h_kv, d_h, dtype))
     return ATTN_ERR_INVALID_ARG;
-  const int chunks = n_chunks > 0 ? n_chunks : auto_chunks(h_kv);
+  int sizes[kMaxChunks];
+  const int chunks = chunk_plan(h_kv, n_chunks, sizes);
   const size_t elem = dtype == ATTN_DTYPE_F32 ? 4 : 2;
   const size_t ws_bytes = dtype == ATTN_DTYPE_BF16 ? prefill_layout(T, h_kv, d_h).total : 0;
   const HostScratch L = host_scratch(T, h, h_kv, d_h, elem, ws_bytes);
@@ -131,10 +148,9 @@ attn_status_t attn_prefill_host(const void* q, const void* k, const void* v, voi
   float* dl = reinterpret_cast<float*>(base + L.lse);
   void* dws = dtype == ATTN_DTYPE_BF16 ? base + L.ws : nullptr;
 
-  const int g = h / h_kv, kvc = h_kv / chunks, hc = kvc * g;
-  const size_t q_bytes = size_t(hc) * T * d_h * elem;   // one group's Q (and O)
-  const size_t kv_bytes = size_t(kvc) * T * d_h * elem;  // one group's K (and V)
-  const size_t l_bytes = size_t(hc) * T * sizeof(float);
+  const int g = h / h_kv;
+  const size_t q_head = size_t(T) * d_h * elem;  // one head's Q (and O) or K (and V)
+  const size_t l_head = size_t(T) * sizeof(float);
   const auto* hq = static_cast<const uint8_t*>(q);
   const auto* hk = static_cast<const uint8_t*>(k);
   const auto* hv = static_cast<const uint8_t*>(v);
@@ -152,9 +168,13 @@ attn_status_t attn_prefill_host(const void* q, const void* k, const void* v, voi
   e = cudaEventRecord(ev_start, s);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(P->in, ev_start, 0);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(P->out, ev_start, 0);
-  for (int c = 0; e == cudaSuccess && c < chunks; ++c) {
+  for (int c = 0, kv0 = 0; e == cudaSuccess && c < chunks; kv0 += sizes[c], ++c) {
     cudaEvent_t ev_in = P->ev[2 + c], ev_cmp = P->ev[2 + kMaxChunks + c];
-    const size_t oq = size_t(c) * q_bytes, okv = size_t(c) * kv_bytes, ol = size_t(c) * l_bytes;
+    const int kvc = sizes[c], hc = kvc * g;
+    const size_t oq = size_t(kv0) * g * q_head, okv = size_t(kv0) * q_head;
+    const size_t ol = size_t(kv0) * g * l_head;
+    const size_t q_bytes = size_t(hc) * q_head, kv_bytes = size_t(kvc) * q_head;
+    const size_t l_bytes = size_t(hc) * l_head;
     e = cudaMemcpyAsync(dk + okv, hk + okv, kv_bytes, cudaMemcpyHostToDevice, P->in);
     if (e == cudaSuccess) e = cudaMemcpyAsync(dv + okv, hv + okv, kv_bytes, cudaMemcpyHostToDevice, P->in);
     if (e == cudaSuccess) e = cudaMemcpyAsync(dq + oq, hq + oq, q_bytes, cudaMemcpyHostToDevice, P->in);
@@ -165,10 +185,12 @@ attn_status_t attn_prefill_host(const void* q, const void* k, const void* v, voi
         e = launch_prefill_f32(reinterpret_cast<const float*>(dq + oq),
                                reinterpret_cast<const float*>(dk + okv),
                                reinterpret_cast<const float*>(dv + okv),
-                               reinterpret_cast<float*>(dO + oq), dl + size_t(c) * hc * T, T, hc,
+                               reinterpret_cast<float*>(dO + oq),
+                               reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(dl) + ol), T, hc,
                                kvc, d_h, causal != 0, scale, s);
       else
-        e = launch_prefill_bf16(dq + oq, dk + okv, dv + okv, dO + oq, dl + size_t(c) * hc * T, T,
+        e = launch_prefill_bf16(dq + oq, dk + okv, dv + okv, dO + oq,
+                                reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(dl) + ol), T,
                                 hc, kvc, d_h, causal != 0, scale, dws, s);
     }
     if (e == cudaSuccess) e = cudaEventRecord(ev_cmp, s);

@@ -40,6 +40,17 @@ def test_bitwise_equal_to_device_call(causal, n_chunks):
     assert torch.equal(o, o_ref) and torch.equal(lse, l_ref)
 
 
+def test_tapered_groups_bitwise():
+    """n_chunks = 0 with 8 KV heads: unequal groups of 3, 2, 2 and 1 KV heads."""
+    shape = W.PrefillShape("host_taper", 16, 8, 64, 257, torch.bfloat16, True)
+    q, k, v = W.prefill_inputs(shape, 6)
+    hq, hk, hv = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    o, lse = attn.attn_prefill_host(hq, hk, hv, True, shape.scale, n_chunks=0)
+    torch.cuda.synchronize()
+    o_ref, l_ref = device_result(q, k, v, True, shape.scale)
+    assert torch.equal(o, o_ref) and torch.equal(lse, l_ref)
+
+
 def test_matches_oracle_and_pageable_memory():
     shape = W.PrefillShape("host_gqa_small", 4, 2, 64, 200, torch.bfloat16, True)
     q, k, v = W.prefill_inputs(shape, 6)  # pageable host memory
