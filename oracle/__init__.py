@@ -10,6 +10,9 @@ Contents (each function cites the passage it follows):
                              head, mask by index sets, safe (max-shifted)
                              softmax, P V.  Returns O and the natural-log LSE.
 * ``attention_rows_ref``   - the same definition evaluated for chosen rows only.
+* ``attention_heads_ref``  - the same definition for chosen query heads, every
+                             row, each row's allowed keys taken as a prefix
+                             slice (whole long layers, head by head).
 * ``decode_paged_ref``     - the definition for one query token per row over
                              keys gathered through a page table.
 * ``block_state`` / ``merge_states`` / ``finalize_state`` - the (m, l, a)
@@ -22,6 +25,7 @@ Contents (each function cites the passage it follows):
 """
 from .attention import (  # noqa: F401
     EMPTY_M,
+    attention_heads_ref,
     attention_ref,
     attention_rows_ref,
     block_state,

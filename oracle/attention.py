@@ -129,6 +129,78 @@ def attention_rows_ref(q, k, v, scale: float, causal: bool, heads, rows):
     return O, LSE
 
 
+def _softmax_prefix_rows_times_v(S: np.ndarray, n_allowed, V: np.ndarray):
+    """``_softmax_rows_times_v`` for rows whose allowed keys form a prefix.
+
+    Row i may attend keys 0 .. n_allowed[i]-1: the causal rule j <= i gives
+    n_allowed[i] = i + 1, and no mask gives every key. The allowed set is then
+    a slice of S and V, so no index array is built and nothing is copied; the
+    three passes ([NA] §(2) "Safe softmax") are those of
+    ``_softmax_rows_times_v``. A row with no allowed key has zero output and
+    LSE = -inf ([MRG]). Returns (O [n, d], LSE [n]).
+    """
+    n = S.shape[0]
+    d = V.shape[1]
+    O = np.zeros((n, d), dtype=np.float64)
+    LSE = np.full(n, EMPTY_M, dtype=np.float64)
+    for i in range(n):
+        c = int(n_allowed[i])
+        if c == 0:
+            continue  # all-masked row: zero output, LSE = -inf ([MRG])
+        x = S[i, :c]
+        M = x.max()                      # pass 1: max
+        p = np.exp(x - M)                # pass 2: shifted exponentials
+        ell = p.sum()                    #          and their sum
+        O[i] = (p / ell) @ V[:c]         # pass 3: normalise, weight the values
+        LSE[i] = M + math.log(ell)       # LSE = m + ln(l)
+    return O, LSE
+
+
+def attention_heads_ref(q, k, v, scale: float, causal: bool, heads, threads: int = 1):
+    """``attention_ref`` for the listed query heads, every query row.
+
+    The definition of [NA]'s opening section (query head hq reads KV head
+    hq // (h / h_kv); S = scale * q K^T materialised per head) with each row's
+    allowed keys taken as a prefix of the key axis (``_softmax_prefix_rows_times_v``),
+    which is what equal query and key lengths give under the causal rule j <= i.
+    This is the form a whole long layer is checked with: one head at a time,
+    optionally several heads at once on ``threads`` host threads (each head is
+    independent; numpy releases the interpreter lock inside its loops).
+
+    Returns O [len(heads), T, d] and LSE [len(heads), T] in float64, in the
+    order of ``heads``.
+    """
+    q64, k64, v64 = to_f64(q), to_f64(k), to_f64(v)
+    h, Tq, _ = q64.shape
+    h_kv, Tk, _ = k64.shape
+    d = v64.shape[2]
+    if h % h_kv:
+        raise ValueError("h must be a multiple of h_kv")
+    if causal and Tq != Tk:
+        raise ValueError("causal masking is defined here for equal query/key lengths")
+    g = h // h_kv
+    heads = [int(x) for x in heads]
+    n_allowed = np.arange(1, Tq + 1) if causal else np.full(Tq, Tk)
+    O = np.zeros((len(heads), Tq, d), dtype=np.float64)
+    LSE = np.full((len(heads), Tq), EMPTY_M, dtype=np.float64)
+
+    def one(idx):
+        hq = heads[idx]
+        kvh = hq // g
+        S = scale * (q64[hq] @ k64[kvh].T)
+        O[idx], LSE[idx] = _softmax_prefix_rows_times_v(S, n_allowed, v64[kvh])
+
+    if threads <= 1:
+        for idx in range(len(heads)):
+            one(idx)
+    else:
+        from concurrent.futures import ThreadPoolExecutor
+
+        with ThreadPoolExecutor(threads) as ex:
+            list(ex.map(one, range(len(heads))))
+    return O, LSE
+
+
 def decode_paged_ref(q, k_cache, v_cache, block_table, seq_lens, scale: float, rows=None):
     """One query token per row attending to its row's keys through a page table.
 

@@ -30,3 +30,13 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    # Parity statistics of the CUDA-vs-oracle checks run in this session.
+    try:
+        import parity
+    except Exception:  # pragma: no cover
+        return
+    for line in parity.summary_lines():
+        terminalreporter.write_line(line)

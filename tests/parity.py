@@ -1,13 +1,21 @@
 """Tolerances and comparison helpers for CUDA-vs-oracle parity.
 
 Tolerances (stated once, used by every parity test):
-  * bf16 outputs: |o_gpu - o_ref| <= 2e-3 + ulp_bf16(|o_ref|) element-wise.
-    The 2e-3 absolute bound is the stated target; one bf16 ulp of the exact
-    value is added because rounding the exact result to bf16 alone already
-    costs up to half an ulp, which exceeds 2e-3 once |o| >= 0.5.
+  * bf16 outputs: |o_gpu - o_ref| <= 2e-3 + ulp_bf16(|o_ref| + 2e-3) / 2
+    element-wise. The stated bound is a max-abs error of 2e-3, which no bf16
+    output can meet once |o| >= 0.5: rounding even the exact value to bf16
+    costs up to half an ulp (2^-9 = 1.95e-3 on [0.5, 1), 2^-8 on [1, 2)).
+    Reading: the kernel's fp32 result before its final rounding is within
+    2e-3 of the exact value, and the rounding then moves it by at most half
+    a bf16 ulp at its own magnitude, which is at most |o_ref| + 2e-3.
   * fp32 outputs (the fp32 single-head workload): |o_gpu - o_ref| <= 1e-4.
   * LSE (fp32): |lse_gpu - lse_ref| <= 1e-4; an empty row must give -inf
     exactly on both sides.
+
+Every check also records how much of the slack it used: the raw max-abs
+error, how many elements exceed the bare 2e-3, the largest error in bf16 ulps
+of the reference, and how many elements equal the reference rounded to bf16.
+``STATS`` collects them; the test session prints a summary at its end.
 """
 from __future__ import annotations
 
@@ -18,12 +26,19 @@ BF16_ABS = 2e-3
 F32_ABS = 1e-4
 LSE_ABS = 1e-4
 
+STATS: list[dict] = []
+
 
 def ulp_bf16(x: np.ndarray) -> np.ndarray:
     """Spacing of bf16 numbers at |x| (8 significant bits)."""
     ax = np.abs(x)
     e = np.floor(np.log2(np.maximum(ax, 2.0 ** -126)))
     return np.exp2(e - 7)
+
+
+def bf16_tol(r: np.ndarray) -> np.ndarray:
+    """Element-wise bound for a bf16 output whose exact value is r."""
+    return BF16_ABS + 0.5 * ulp_bf16(np.abs(r) + BF16_ABS)
 
 
 def to_np(t) -> np.ndarray:
@@ -35,22 +50,40 @@ def to_np(t) -> np.ndarray:
     return np.asarray(t, dtype=np.float64)
 
 
+def _bf16_round(r: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(np.ascontiguousarray(r)).to(torch.bfloat16).double().numpy()
+
+
+def _record(what: str, dtype, o: np.ndarray, r: np.ndarray, err: np.ndarray):
+    rec = {"what": what, "n": int(err.size),
+           "max_abs": float(err.max()) if err.size else 0.0}
+    if dtype == torch.bfloat16 and err.size:
+        rec["above_2e-3"] = int((err > BF16_ABS).sum())
+        rec["max_ulp"] = float((err / ulp_bf16(r)).max())
+        rec["rounded_ref"] = float((o == _bf16_round(r)).mean())
+    STATS.append(rec)
+    extra = ""
+    if "max_ulp" in rec:
+        extra = (f" above_2e-3={rec['above_2e-3']} max_ulp={rec['max_ulp']:.2f}"
+                 f" equal_to_bf16(ref)={rec['rounded_ref']:.4f}")
+    print(f"parity {what}: n={rec['n']} max_abs={rec['max_abs']:.3e}{extra}")
+    return rec
+
+
 def check_out(out, ref, dtype, what="o"):
     o = to_np(out)
     r = np.asarray(ref, dtype=np.float64)
     assert o.shape == r.shape, (o.shape, r.shape)
     assert np.all(np.isfinite(o)), f"{what}: non-finite output"
     err = np.abs(o - r)
-    if dtype == torch.bfloat16:
-        tol = BF16_ABS + ulp_bf16(r)
-    else:
-        tol = np.full_like(r, F32_ABS)
+    tol = bf16_tol(r) if dtype == torch.bfloat16 else np.full_like(r, F32_ABS)
     bad = err > tol
     if bad.any():
         i = np.unravel_index(np.argmax(err - tol), err.shape)
         raise AssertionError(
             f"{what}: {int(bad.sum())} of {err.size} elements out of tolerance; worst at {i}: "
             f"gpu={o[i]!r} ref={r[i]!r} err={err[i]:.3e} tol={tol[i]:.3e}")
+    _record(what, dtype, o, r, err)
     return float(err.max()) if err.size else 0.0
 
 
@@ -64,5 +97,35 @@ def check_lse(out, ref, what="lse"):
         err = np.abs(o[~empty] - r[~empty])
         assert np.all(np.isfinite(o[~empty])), f"{what}: non-finite"
         assert err.max() <= LSE_ABS, f"{what}: max err {err.max():.3e} > {LSE_ABS}"
+        STATS.append({"what": what, "n": int(err.size), "max_abs": float(err.max()), "lse": True})
         return float(err.max())
     return 0.0
+
+
+def summary_lines() -> list[str]:
+    """Compact report of every check made in this session (worst cases)."""
+    if not STATS:
+        return []
+    outs = [s for s in STATS if not s.get("lse")]
+    lses = [s for s in STATS if s.get("lse")]
+    bf = [s for s in outs if "max_ulp" in s]
+    lines = [f"parity summary (passing checks): {len(outs)} outputs ({sum(s['n'] for s in outs)} elements), "
+             f"{len(lses)} LSE"]
+    if bf:
+        w = max(bf, key=lambda s: s["max_abs"])
+        lines.append(f"  bf16: worst max_abs {w['max_abs']:.3e} ({w['what']}), "
+                     f"elements above the bare 2e-3: {sum(s['above_2e-3'] for s in bf)}, "
+                     f"worst {max(s['max_ulp'] for s in bf):.2f} ulp")
+    if lses:
+        w = max(lses, key=lambda s: s["max_abs"])
+        lines.append(f"  lse: worst max_abs {w['max_abs']:.3e} ({w['what']})")
+    groups: dict[str, list[dict]] = {}
+    for s in bf:
+        if s["what"].startswith("bench"):
+            groups.setdefault(s["what"].split(" heads")[0], []).append(s)
+    for name, ss in groups.items():
+        lines.append(f"  {name}: n={sum(s['n'] for s in ss)} "
+                     f"max_abs={max(s['max_abs'] for s in ss):.3e} "
+                     f"above_2e-3={sum(s['above_2e-3'] for s in ss)} "
+                     f"max_ulp={max(s['max_ulp'] for s in ss):.2f}")
+    return lines

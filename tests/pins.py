@@ -251,6 +251,11 @@ def pin_brute_force_prefill(A):
         Ob, Lb = _brute_attention(q.tolist(), k.tolist(), v.tolist(), 0.7, causal)
         assert np.allclose(O, Ob, rtol=1e-12, atol=1e-12)
         assert np.allclose(L, Lb, rtol=1e-12, atol=1e-12)
+        # The whole-layer form (prefix slices), in a shuffled head order.
+        order = list(range(h))[::-1]
+        Oh, Lh = A.attention_heads_ref(q, k, v, 0.7, causal, order)
+        assert np.allclose(Oh, Ob[order], rtol=1e-12, atol=1e-12)
+        assert np.allclose(Lh, Lb[order], rtol=1e-12, atol=1e-12)
         # Sampled rows agree with the full definition.
         heads = [0, h - 1, h // 2]
         rows = [T - 1, 0, T // 2]
@@ -318,7 +323,11 @@ def pin_library_sdpa(A):
         logits = 0.25 * tq @ tk.transpose(1, 2)
         if causal:
             logits = logits.masked_fill(torch.ones(T, T, dtype=torch.bool).triu(1), float("-inf"))
-        assert np.allclose(L, torch.logsumexp(logits, dim=-1).numpy(), rtol=1e-12, atol=1e-12)
+        lse_t = torch.logsumexp(logits, dim=-1).numpy()
+        assert np.allclose(L, lse_t, rtol=1e-12, atol=1e-12)
+        Oh, Lh = A.attention_heads_ref(q, k, v, 0.25, causal, range(h), threads=2)
+        assert np.allclose(Oh, ref.numpy(), rtol=1e-11, atol=1e-11)
+        assert np.allclose(Lh, lse_t, rtol=1e-12, atol=1e-12)
 
 
 def pin_merge_partials(A):

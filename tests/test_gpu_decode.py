@@ -56,6 +56,26 @@ def test_decode_contiguous_32k_split_independent(shape, splits):
         check_out(torch.from_numpy(o), outs[0].astype(np.float64), torch.bfloat16, "split independence")
 
 
+@pytest.mark.parametrize("which", ["recommended", "other"])
+def test_decode_paged_batch_every_row(which):
+    """The 66-row paged batch the benchmark times (64 lengths U[1, 16384],
+    2 empty rows, shuffled pages): every row and head against the oracle, at
+    the benchmark's split count and at a quarter of it plus one."""
+    shape = W.DECODE_PAGED_B64
+    q, kc, vc, table, seq = W.decode_inputs(shape, seed=0)
+    lens = seq.tolist()
+    S = attn.attn_recommended_splits(len(lens), shape.h_kv, max(lens), sum(lens))
+    if which == "other":
+        S = S // 4 + 1
+    o, lse = run_decode(q, kc, vc, table, seq, S)
+    O_ref, L_ref = oracle.decode_paged_ref(q, kc, vc, table, seq, shape.scale)
+    check_out(o, O_ref, torch.bfloat16, f"bench paged decode o S={S}")
+    check_lse(lse, L_ref, f"bench paged decode lse S={S}")
+    for r in (i for i, s in enumerate(lens) if s == 0):
+        assert torch.all(o[r] == 0) and torch.all(torch.isneginf(lse[r]))
+    assert attn.attn_get_device_error() == 0
+
+
 def test_decode_paged_batch_full_size_sampled_rows():
     """Paged batch of 64 random lengths in [1, 16384] plus 2 empty rows, shuffled
     physical pages; the split count the benchmark uses; oracle on sampled rows."""

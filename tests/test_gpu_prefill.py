@@ -1,4 +1,6 @@
 """attn_prefill (CUDA: tcgen05 bf16 path and fp32 SIMT path) against the oracle."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -116,11 +118,13 @@ def test_bf16_without_workspace(d, causal):
 
 
 @pytest.mark.parametrize("causal", [True, False])
-def test_bf16_extreme_logits_take_row_max_pass(causal):
+def test_bf16_extreme_logits(causal):
     """Logits far outside fp32's exponent range relative to the carried
-    reference: one key 2^10 (log2 units) above the rest of its row (an inf
-    weight sum sends the tile back for its row max), and query rows whose
-    first key tile lies 2^10 below zero (a zero weight sum on the first tile)."""
+    reference: one key 2^10 (log2 units) above the rest of its row (the
+    reference must move to that tile's row max, which every tile takes before
+    it exponentiates, or its weight overflows), and query rows whose first key
+    tile lies 2^10 below zero (weights taken against that tile's own max, not
+    against zero, or they all underflow)."""
     shape = W.PrefillShape("t", 4, 2, 128, 300, torch.bfloat16, causal)
     q, k, v = W.prefill_inputs(shape, 13)
     ones = torch.ones(128, dtype=torch.bfloat16)
@@ -135,21 +139,50 @@ def test_bf16_extreme_logits_take_row_max_pass(causal):
     assert attn.attn_get_device_error() == 0
 
 
+def _oracle_threads():
+    try:
+        n = len(os.sched_getaffinity(0))
+    except AttributeError:
+        n = os.cpu_count() or 1
+    return max(1, min(8, n))
+
+
 def test_gqa_T2048_causal_full():
-    """The Llama-3-8B GQA layer at T = 2048, causal; full comparison."""
+    """The Llama-3-8B GQA layer at T = 2048, causal; every element of O and
+    LSE against the oracle."""
     shape = W.GQA_T2048_CAUSAL
     q, k, v = W.prefill_inputs(shape, 0)
-    O_ref, L_ref = oracle.attention_ref(q, k, v, shape.scale, True)
+    O_ref, L_ref = oracle.attention_heads_ref(q, k, v, shape.scale, True, range(shape.h),
+                                              threads=_oracle_threads())
     o, lse = run(q, k, v, True, shape.scale)
-    err = check_out(o, O_ref, torch.bfloat16)
-    check_lse(lse, L_ref)
-    print(f"max abs err {err:.3e}")
+    check_out(o, O_ref, torch.bfloat16, "bench T2048 causal o")
+    check_lse(lse, L_ref, "bench T2048 causal lse")
+
+
+@pytest.mark.parametrize("shape", [W.GQA_T8192_CAUSAL, W.GQA_T8192_FULL], ids=lambda s: s.name)
+def test_gqa_T8192_every_element(shape):
+    """The T = 8192 layer the benchmark times (Q, K x3), causal and not:
+    every element of O and LSE, all 32 heads x 8192 rows, against the oracle,
+    head by head on the host cores."""
+    q, k, v = W.prefill_inputs(shape, 0)
+    o, lse = run(q, k, v, shape.causal, shape.scale)
+    o, lse = o.cpu(), lse.cpu()
+    tag = "causal" if shape.causal else "non-causal"
+    # Eight heads (two KV-head groups) per oracle call bounds the host memory.
+    for h0 in range(0, shape.h, 8):
+        heads = list(range(h0, h0 + 8))
+        O_ref, L_ref = oracle.attention_heads_ref(q, k, v, shape.scale, shape.causal, heads,
+                                                  threads=_oracle_threads())
+        check_out(o[h0:h0 + 8], O_ref, torch.bfloat16, f"bench T8192 {tag} o heads {h0}-{h0 + 7}")
+        check_lse(lse[h0:h0 + 8], L_ref, f"bench T8192 {tag} lse heads {h0}-{h0 + 7}")
+    assert attn.attn_get_device_error() == 0
 
 
 @pytest.mark.parametrize("shape", [W.GQA_T8192_CAUSAL, W.GQA_T8192_FULL], ids=lambda s: s.name)
 def test_gqa_T8192_sampled_rows(shape):
     """T = 8192 with logits widened (Q, K x3); oracle on sampled rows that
-    include the first and last rows and rows in the last tile."""
+    include the first and last rows and rows in the last tile (a quick check;
+    the every-element comparison follows)."""
     q, k, v = W.prefill_inputs(shape, 0)
     o, lse = run(q, k, v, shape.causal, shape.scale)
     rng = np.random.default_rng(1)

@@ -11,6 +11,7 @@ import pins
 
 _orig_attention_ref = A.attention_ref
 _orig_softmax_rows = A._softmax_rows_times_v
+_orig_softmax_prefix = A._softmax_prefix_rows_times_v
 
 
 def _attention_variant(kv_of=None, allowed_of=None, swap_kv=False, drop_scale=False):
@@ -83,6 +84,11 @@ def _softmax_rows_no_shift_sum(S, allowed, V):
         O[i] = (p / ell) @ V[cols]
         L[i] = M + math.log(ell)
     return O, L
+
+
+def _softmax_prefix_drops_last(S, n_allowed, V):
+    # wrong index: each row's prefix stops one key short (causal j < i)
+    return _orig_softmax_prefix(S, [max(int(c) - 1, 1) for c in n_allowed], V)
 
 
 def _merge_partials_no_rescale(o_part, m_part, l_part, n_active=None):
@@ -175,6 +181,8 @@ MUTANTS = {
     "lse_in_log2": ({"_softmax_rows_times_v": _softmax_rows_log2}, pins.pin_worked_example),
     "normaliser_term_dropped": ({"_softmax_rows_times_v": _softmax_rows_no_shift_sum},
                                 pins.pin_closed_forms),
+    "heads_prefix_one_short": ({"_softmax_prefix_rows_times_v": _softmax_prefix_drops_last},
+                               pins.pin_brute_force_prefill),
     "split_partials_not_rescaled": ({"merge_partials_ref": _merge_partials_no_rescale},
                                     pins.pin_merge_partials),
     "pair_merge_unweighted": ({"merge_lse_pair_ref": _merge_pair_unweighted}, pins.pin_merge_lse_pair),
