@@ -20,6 +20,14 @@ Readings taken where the pages are silent:
     query i iff j <= i. For a paged row with fewer queries than keys, the
     queries are the last key positions (bottom-right alignment).
   * Inputs are upcast to float64 exactly as stored (bf16 / fp32 values).
+  * Non-finite inputs follow IEEE arithmetic on the definition over each
+    row's allowed keys ([NA] "The base case is a NaN factory" shows how a
+    NaN, once made, spreads through the weighted sums): a NaN logit (a NaN
+    in q or in an attended k) makes the row's output and LSE NaN; a NaN or
+    +-inf in an attended v_j[e] makes column e of the output NaN or +-inf;
+    keys a row does not attend (masked, or past its length) are excluded
+    and never reach it. Every max below propagates NaN (numpy's max does;
+    Python's built-in max would drop a NaN depending on argument order).
 """
 from __future__ import annotations
 
@@ -28,6 +36,13 @@ import math
 import numpy as np
 
 EMPTY_M = -np.inf
+
+
+def _max_nan(a: float, b: float) -> float:
+    """max(a, b), NaN if either is NaN."""
+    if math.isnan(a) or math.isnan(b):
+        return math.nan
+    return max(a, b)
 
 
 def to_f64(x) -> np.ndarray:
@@ -349,7 +364,7 @@ def merge_states(a, b):
     -inf - (-inf) is NaN, so that case branches to the empty state instead.
     """
     (ma, la, xa), (mb, lb, xb) = a, b
-    m = max(ma, mb)
+    m = _max_nan(ma, mb)
     if np.isneginf(m):
         return empty_state(len(xa))
     wa = math.exp(ma - m) if not np.isneginf(ma) else 0.0
@@ -382,7 +397,7 @@ def online_softmax_attention(x, values, block: int):
     alphas = []
     for j in range(0, x.shape[0], block):
         xb, vb = x[j:j + block], values[j:j + block]
-        m_new = max(m, xb.max())
+        m_new = _max_nan(m, xb.max())
         if np.isneginf(m_new):
             # Nothing unmasked seen yet: exp(-inf - (-inf)) would be NaN, so
             # the block is skipped ([NA] "The base case is a NaN factory").
@@ -450,7 +465,7 @@ def merge_lse_pair_ref(o_a, lse_a, o_b, lse_b):
     O = np.zeros_like(oa)
     LSE = np.full(la.shape, EMPTY_M, dtype=np.float64)
     for r in range(la.shape[0]):
-        M = max(la[r], lb[r])
+        M = _max_nan(la[r], lb[r])
         if np.isneginf(M):
             continue
         ea = math.exp(la[r] - M) if not np.isneginf(la[r]) else 0.0

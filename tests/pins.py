@@ -437,6 +437,51 @@ def pin_paged_prefill(A):
     assert np.allclose(On[cu[2]], Od[0], atol=1e-12) and np.allclose(Ln[cu[2]], Ld[0], atol=1e-12)
 
 
+def pin_nonfinite_inputs(A):
+    """IEEE arithmetic on the definition over the allowed keys: a NaN logit
+    makes its row NaN; a NaN / inf in v_j[e] reaches column e of exactly the
+    rows that attend key j and no other element; a masked key's NaN reaches
+    nothing. The merges carry a NaN state in either argument order."""
+    rng = np.random.default_rng(31)
+    h, h_kv, T, d = 2, 1, 6, 4
+    q = rng.normal(size=(h, T, d))
+    k = rng.normal(size=(h_kv, T, d))
+    v = rng.normal(size=(h_kv, T, d))
+    O0, L0 = A.attention_ref(q, k, v, 0.5, causal=True)
+    with np.errstate(invalid="ignore"):
+        kn = k.copy()
+        kn[0, 3, 1] = np.nan  # logit of key 3 is NaN for every query
+        O, L = A.attention_ref(q, kn, v, 0.5, causal=True)
+        assert np.all(np.isnan(O[:, 3:])) and np.all(np.isnan(L[:, 3:]))
+        assert np.array_equal(O[:, :3], O0[:, :3]) and np.array_equal(L[:, :3], L0[:, :3])
+        for val in (np.nan, np.inf, -np.inf):
+            vn = v.copy()
+            vn[0, 2, 1] = val  # rows 2.. attend key 2 (weight > 0), rows 0, 1 do not
+            O, L = A.attention_ref(q, k, vn, 0.5, causal=True)
+            col = O[:, 2:, 1]
+            assert (np.all(np.isnan(col)) if np.isnan(val) else np.all(col == val))
+            keep = np.ones(O.shape, bool)
+            keep[:, 2:, 1] = False
+            assert np.array_equal(O[keep], O0[keep]) and np.array_equal(L, L0)
+        # the same through the whole-layer and paged forms
+        Oh, Lh = A.attention_heads_ref(q, kn, v, 0.5, True, range(h))
+        assert np.all(np.isnan(Oh[:, 3:])) and np.array_equal(Oh[:, :3], O0[:, :3])
+        # merges: a NaN state is not an empty one, in either order
+        e = A.empty_state(d)
+        bad = (np.nan, 1.0, np.ones(d))
+        for a, b in ((e, bad), (bad, e)):
+            assert np.isnan(A.merge_states(a, b)[0])
+        for la, lb in ((np.nan, -np.inf), (-np.inf, np.nan), (np.nan, 0.5)):
+            Om, Lm = A.merge_lse_pair_ref(np.ones((1, d)), np.array([la]), np.ones((1, d)),
+                                          np.array([lb]))
+            assert np.all(np.isnan(Om)) and np.isnan(Lm[0])
+        Op, Lp = A.merge_partials_ref(np.ones((1, 3, d)), np.array([[0.0, np.nan, 1.0]]),
+                                      np.ones((1, 3)))
+        assert np.all(np.isnan(Op)) and np.isnan(Lp[0])
+        o, lse, _ = A.online_softmax_attention(np.array([-np.inf, np.nan, 1.0]), np.ones((3, d)), 1)
+        assert np.all(np.isnan(o)) and np.isnan(lse)
+
+
 ALL_PINS = [
     pin_worked_example,
     pin_max_jump_rescale,
@@ -450,4 +495,5 @@ ALL_PINS = [
     pin_merge_partials,
     pin_merge_lse_pair,
     pin_paged_prefill,
+    pin_nonfinite_inputs,
 ]

@@ -91,6 +91,23 @@ def _softmax_prefix_drops_last(S, n_allowed, V):
     return _orig_softmax_prefix(S, [max(int(c) - 1, 1) for c in n_allowed], V)
 
 
+def _merge_pair_drops_nan(o_a, lse_a, o_b, lse_b):
+    # Python's max: max(-inf, nan) is -inf, so a NaN side can pass as empty
+    oa, ob = A.to_f64(o_a), A.to_f64(o_b)
+    la, lb = A.to_f64(lse_a), A.to_f64(lse_b)
+    O = np.zeros_like(oa)
+    L = np.full(la.shape, -np.inf)
+    for r in range(la.shape[0]):
+        M = max(la[r], lb[r])
+        if np.isneginf(M):
+            continue
+        ea = math.exp(la[r] - M) if not np.isneginf(la[r]) else 0.0
+        eb = math.exp(lb[r] - M) if not np.isneginf(lb[r]) else 0.0
+        O[r] = (ea * oa[r] + eb * ob[r]) / (ea + eb)
+        L[r] = math.log(ea + eb) + M
+    return O, L
+
+
 def _merge_partials_no_rescale(o_part, m_part, l_part, n_active=None):
     o, m, l = A.to_f64(o_part), A.to_f64(m_part), A.to_f64(l_part)
     rows, S, d = o.shape
@@ -186,6 +203,7 @@ MUTANTS = {
     "split_partials_not_rescaled": ({"merge_partials_ref": _merge_partials_no_rescale},
                                     pins.pin_merge_partials),
     "pair_merge_unweighted": ({"merge_lse_pair_ref": _merge_pair_unweighted}, pins.pin_merge_lse_pair),
+    "pair_merge_drops_nan": ({"merge_lse_pair_ref": _merge_pair_drops_nan}, pins.pin_nonfinite_inputs),
     "page_and_slot_swapped": ({"decode_paged_ref": _decode_slot_swapped}, pins.pin_brute_force_decode),
     "paged_queries_top_left": ({"prefill_paged_ref": _paged_variant(top_left=True)},
                                pins.pin_paged_prefill),
