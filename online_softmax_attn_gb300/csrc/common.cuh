@@ -95,6 +95,16 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// Maximum that returns NaN when either operand is NaN (fmaxf returns the
+// other one). Running maxima use it so that a NaN logit or state reaches the
+// row's result as IEEE arithmetic on the definition would carry it, instead
+// of dropping out of the max.
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

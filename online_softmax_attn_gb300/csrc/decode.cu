@@ -262,6 +262,19 @@ __global__ void __launch_bounds__(NW * 32, 1)
     const uint32_t vp = kp + C::PAGE_BYTES;
     const int page = p_begin + warp + NW * i;
     const int valid = min(kPage, seq_len - page * kPage);
+    if (valid < kPage) {
+      // The row's last page: its slots past seq_len hold whatever the cache
+      // holds there (possibly NaN or inf). Their weights are 0, but 0 * NaN
+      // is NaN in the P V product, so those V rows are zeroed first.
+      constexpr int CPR = D / 8;  // 16-byte chunks per row
+      for (int c = lane; c < (kPage - valid) * CPR; c += 32)
+        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(
+                         page_chunk(vp, valid + c / CPR, c % CPR)),
+                     "r"(0u)
+                     : "memory");
+      fence_proxy_async_smem();  // before the stage is refilled by the copy engine
+      __syncwarp();
+    }
 
     // ---- S = q K^T: two 8-key n-tiles, KS k-steps ----
     float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -283,10 +296,12 @@ __global__ void __launch_bounds__(NW * 32, 1)
     }
 
     // ---- online update (one rescale per page) ----
-    float mx = fmaxf(fmaxf(s[0], s[1]), fmaxf(s[2], s[3]));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    const float m_new = fmaxf(m_run, mx);  // finite: every page has a valid key
+    float mx = fmax_nan(fmax_nan(s[0], s[1]), fmax_nan(s[2], s[3]));
+    mx = fmax_nan(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmax_nan(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    // Finite (every page has a valid key) unless a logit is NaN, which then
+    // carries through m, alpha, p, l and O~ to the row's result.
+    const float m_new = fmax_nan(m_run, mx);
     const float alpha = ex2_approx(m_run - m_new);  // 0 while m_run = -inf
     m_run = m_new;
     float p[4];
@@ -360,7 +375,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
     const int e = idx % D;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < NW; ++w) M = fmaxf(M, ml_s[(w * G + hh) * 2]);
+    for (int w = 0; w < NW; ++w) M = fmax_nan(M, ml_s[(w * G + hh) * 2]);
     float A = 0.f, L = 0.f;
 #pragma unroll
     for (int w = 0; w < NW; ++w) {

@@ -8,7 +8,8 @@
 // evaluating -inf - (-inf)).
 //
 // Layout: WPR warps per output row (1 for many rows, 8 when there are too
-// few rows to fill the GPU, and always 8 for fixed-size splits); lane j owns d_h/32 consecutive output elements,
+// few rows to fill the GPU, 32 for fewer than 128 rows of more than 64
+// splits, and always 8 for fixed-size splits); lane j owns d_h/32 consecutive output elements,
 // so each split's O~ row is read as one coalesced 128-bit (d_h=128) or 64-bit
 // (d_h=64) access per lane. Warp w of a row takes splits w, w + WPR, ... in
 // batches (4 splits per warp, 8 with WPR = 8) whose m, l and O~ loads are
@@ -29,7 +30,7 @@ namespace attn {
 static __device__ unsigned int g_merge_err;
 
 template <int D, bool kOutBf16, int WPR>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(WPR > 8 ? WPR * 32 : 256)
     merge_states_kernel(const float* __restrict__ o_part, const float* __restrict__ m_part,
                         const float* __restrict__ l_part, const int32_t* __restrict__ n_active,
                         const int32_t* __restrict__ seq_lens, int heads_per_seq, int page_size,
@@ -37,10 +38,11 @@ __global__ void __launch_bounds__(256)
                         int fixed_pps, const int* __restrict__ pps_dev) {
   constexpr int VEC = D / 32;
   static_assert(VEC == 2 || VEC == 4, "d_h must be 64 or 128");
-  constexpr int RPC = 8 / WPR;  // rows per CTA of 8 warps
+  constexpr int RPC = WPR > 8 ? 1 : 8 / WPR;  // rows per CTA (8 warps, or WPR warps for one row)
   // Splits per warp whose loads are in flight together: with 8 warps per row
-  // a first batch of 8 covers 64 splits in one round trip.
-  constexpr int U = WPR > 1 ? 8 : 4;
+  // a first batch of 8 covers 64 splits in one round trip, with 32 warps a
+  // batch of 5 (what fits the 64 registers of a 1024-thread CTA) covers 160.
+  constexpr int U = WPR > 8 ? 5 : (WPR > 1 ? 8 : 4);
   __shared__ float red_acc[WPR > 1 ? WPR * D : 1];
   __shared__ float red_m[WPR], red_l[WPR];
   const int lane = threadIdx.x & 31;
@@ -98,9 +100,9 @@ __global__ void __launch_bounds__(256)
     float bm = -INFINITY;
 #pragma unroll
     for (int u = 0; u < U; ++u)
-      if (base + u * WPR < n) bm = fmaxf(bm, mi[u] * kLog2e);
+      if (base + u * WPR < n) bm = fmax_nan(bm, mi[u] * kLog2e);
     if (bm == -INFINITY) return;  // no active split with keys in this batch
-    const float Mn = fmaxf(Mw, bm);
+    const float Mn = fmax_nan(Mw, bm);
     const float sc = (Mw == -INFINITY) ? 0.f : ex2_approx(Mw - Mn);
     Lw *= sc;
 #pragma unroll
@@ -136,7 +138,7 @@ __global__ void __launch_bounds__(256)
     if (wr != 0 || !live) return;
     M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < WPR; ++w) M = fmaxf(M, red_m[w]);
+    for (int w = 0; w < WPR; ++w) M = fmax_nan(M, red_m[w]);
     L = 0.f;
 #pragma unroll
     for (int e = 0; e < VEC; ++e) acc[e] = 0.f;
@@ -151,7 +153,9 @@ __global__ void __launch_bounds__(256)
     }
   }
 
-  const bool empty = !(L > 0.f);  // also catches NaN mass and rows with no active split
+  // No active split with a key (M = -inf) is the empty row. A NaN state
+  // (NaN m, l or O~ in an active split) is not: it propagates to o and lse.
+  const bool empty = M == -INFINITY;
   const float inv = empty ? 0.f : 1.f / L;
 #pragma unroll
   for (int e = 0; e < VEC; ++e) acc[e] = empty ? 0.f : acc[e] * inv;
@@ -185,13 +189,16 @@ cudaError_t launch_merge(const float* o_part, const float* m_part, const float* 
                          attn_dtype_t out_dtype, cudaStream_t stream, int fixed_pps,
                          const int* pps_dev) {
   if (rows <= 0) return cudaSuccess;
-  // Few rows and many splits: spread each row's splits over 8 warps. With
-  // fixed-size splits (the batch-invariant mode) always 8: the order in which
-  // a row's splits are summed then depends on that row's split count alone,
-  // not on the batch's rows or grid width.
+  // Few rows and many splits: spread each row's splits over 8 warps, or over
+  // 32 (one 1024-thread CTA per row) when there are more than 64 splits and
+  // under 128 rows, so that every split's loads go out in the first batch.
+  // With fixed-size splits (the batch-invariant mode) always 8: the order in
+  // which a row's splits are summed then depends on that row's split count
+  // alone, not on the batch's rows or grid width.
   const bool wide = fixed_pps > 0 || (rows < 512 && num_splits > 4);
+  const bool wider = fixed_pps == 0 && rows < 128 && num_splits > 64;
   const dim3 grid(wide ? rows : (rows + 7) / 8);
-  const dim3 block(256);
+  const dim3 block(wider ? 1024 : 256);
   const bool bf = out_dtype == ATTN_DTYPE_BF16;
   cudaError_t e = cudaSuccess;
 #define ATTN_MERGE_LAUNCH(D, BF, W)                                                               \
@@ -199,11 +206,25 @@ cudaError_t launch_merge(const float* o_part, const float* m_part, const float* 
                  n_active, seq_lens, heads_per_seq, page_size, max_len, rows, num_splits, o, lse, \
                  fixed_pps, pps_dev)
   if (d_h == 128) {
-    if (bf) { if (wide) ATTN_MERGE_LAUNCH(128, true, 8); else ATTN_MERGE_LAUNCH(128, true, 1); }
-    else { if (wide) ATTN_MERGE_LAUNCH(128, false, 8); else ATTN_MERGE_LAUNCH(128, false, 1); }
+    if (bf) {
+      if (wider) ATTN_MERGE_LAUNCH(128, true, 32);
+      else if (wide) ATTN_MERGE_LAUNCH(128, true, 8);
+      else ATTN_MERGE_LAUNCH(128, true, 1);
+    } else {
+      if (wider) ATTN_MERGE_LAUNCH(128, false, 32);
+      else if (wide) ATTN_MERGE_LAUNCH(128, false, 8);
+      else ATTN_MERGE_LAUNCH(128, false, 1);
+    }
   } else {
-    if (bf) { if (wide) ATTN_MERGE_LAUNCH(64, true, 8); else ATTN_MERGE_LAUNCH(64, true, 1); }
-    else { if (wide) ATTN_MERGE_LAUNCH(64, false, 8); else ATTN_MERGE_LAUNCH(64, false, 1); }
+    if (bf) {
+      if (wider) ATTN_MERGE_LAUNCH(64, true, 32);
+      else if (wide) ATTN_MERGE_LAUNCH(64, true, 8);
+      else ATTN_MERGE_LAUNCH(64, true, 1);
+    } else {
+      if (wider) ATTN_MERGE_LAUNCH(64, false, 32);
+      else if (wide) ATTN_MERGE_LAUNCH(64, false, 8);
+      else ATTN_MERGE_LAUNCH(64, false, 1);
+    }
   }
 #undef ATTN_MERGE_LAUNCH
   return e;
@@ -249,7 +270,7 @@ __global__ void __launch_bounds__(256)
     float va[8], vb[8], r[8];
     load8<kInBf16>(o_a, off, va);
     load8<kInBf16>(o_b, off, vb);
-    const float M = fmaxf(la, lb);
+    const float M = fmax_nan(la, lb);  // a NaN side is not an empty one
     float L;
     if (M == -INFINITY) {  // both sides empty: no -inf - -inf
 #pragma unroll

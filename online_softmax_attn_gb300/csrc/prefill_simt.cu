@@ -138,11 +138,11 @@ __global__ void __launch_bounds__(256)
       const int key = k0 + j;
       const bool ok = key < T && row < T && (!causal || key <= row);
       s[jj] = ok ? a * scale : -INFINITY;
-      mx = fmaxf(mx, s[jj]);
+      mx = fmax_nan(mx, s[jj]);
     }
 #pragma unroll
-    for (int off = 1; off < kTPR; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    const float m_new = fmaxf(m, mx);
+    for (int off = 1; off < kTPR; off <<= 1) mx = fmax_nan(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    const float m_new = fmax_nan(m, mx);  // NaN once a logit is NaN: it then reaches O and the LSE
     // A tile with no allowed key for this row leaves the state unchanged
     // (and avoids -inf - -inf).
     const bool any = m_new != -INFINITY;
@@ -162,8 +162,11 @@ __global__ void __launch_bounds__(256)
       m = m_new;
 #pragma unroll
       for (int e = 0; e < OC; ++e) acc[e] *= alpha;
+      // Only the keys this row may attend: a masked key's weight is 0, but
+      // 0 * NaN (or inf) in its V row would still reach the sum.
+      const int j_end = min(kKeys, (causal ? min(row + 1, T) : T) - k0);
 #pragma unroll 4
-      for (int j = 0; j < kKeys; ++j) {
+      for (int j = 0; j < j_end; ++j) {
         const float p = p_s[r * (kKeys + 1) + j];
 #pragma unroll
         for (int e = 0; e < OC; ++e) acc[e] = fmaf(p, v_s[j * LD + c + kTPR * e], acc[e]);
@@ -174,7 +177,7 @@ __global__ void __launch_bounds__(256)
 
   if (S == 1) {
     if (row < T) {
-      const bool empty = !(l > 0.f);
+      const bool empty = l == 0.f;  // no allowed key; a NaN l is not empty
       const float inv = empty ? 0.f : 1.f / l;
       float* orow = o + (size_t(hq) * T + row) * D;
 #pragma unroll
@@ -210,7 +213,7 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       mi[i] = i < S ? *cluster.map_shared_rank(m_s + rl, i) : -INFINITY;
-      M = fmaxf(M, mi[i]);
+      M = fmax_nan(M, mi[i]);
     }
     float L = 0.f;
 #pragma unroll
@@ -218,7 +221,7 @@ __global__ void __launch_bounds__(256)
       w[i] = (M != -INFINITY && mi[i] != -INFINITY) ? expf(mi[i] - M) : 0.f;
       if (w[i] != 0.f) L += w[i] * *cluster.map_shared_rank(l_s + rl, i);
     }
-    const bool empty = !(L > 0.f);
+    const bool empty = M == -INFINITY;  // no CTA saw an allowed key; NaN states propagate
     if (grow < T) {
       float* orow = o + (size_t(hq) * T + grow) * D;
       for (int col = col0; col < D; col += tpr) {

@@ -73,7 +73,7 @@ struct PfCfg {
   // q_full, k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV], s_full[NQ],
   // p_full[NQ], o_final[NQ], mma_done
   static constexpr int NBAR = 1 + 2 * NSK + 2 * NSV + 3 * NQ + 1;
-  static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;  // tensor-memory slot, abort flag
+  static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;  // tensor-memory slot, abort flag, tail tile
   static constexpr int SMEM = MISC_OFF + 16 + 1024;    // + alignment slack
   static constexpr int TMEM_COLS = NQ == 1 ? 256 : 512;
   // NQ softmax warpgroups + one control warpgroup (TMA warp, MMA warp, two
@@ -186,7 +186,10 @@ struct PagedArgs {
   int max_tiles;  // 128-key tiles per row in the fp16 V copy: ceil(max_blocks / 8)
 };
 
-template <int D, int NQ, int NSK, int NSV, bool PAGED>
+// PAGED: variable-length rows over a paged cache. PCOPY (paged only): V is
+// read from the workspace copy that paged_v_to_f16_kernel made (fp16 bits
+// for normal tiles, bf16 bits for flagged ones), else from the cache itself.
+template <int D, int NQ, int NSK, int NSV, bool PAGED, bool PCOPY>
 __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
     prefill_bf16_kernel(const __grid_constant__ CUtensorMap tmap_q,
                         const __grid_constant__ CUtensorMap tmap_k,
@@ -202,6 +205,11 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
   Bars bars{sbase + C::BAR_OFF, NSK, NSV, NQ};
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
+  // Paged rows read from the cache whose last page is partial: the key tile
+  // holding that page, then (packed) the first slot past the row's last key
+  // within the tile and the number of such slots up to the page's end. Kept
+  // in shared memory so that no warp holds registers for it.
+  int* tail_info = reinterpret_cast<int*>(smem + C::MISC_OFF + 8);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -255,6 +263,10 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
       mbar_init(bar, is_p ? 128u : 1u);
     }
     *abort_flag = 0;
+    if constexpr (PAGED && !PCOPY) {
+      tail_info[0] = ctx % 16 != 0 ? ctx / kBN : -1;
+      tail_info[1] = (ctx % kBN) | ((16 - ctx % 16) << 8);
+    }
     fence_barrier_init();
   }
   if (warp == C::MMA_WARP) tc::alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -332,9 +344,11 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
         if (j == 0) pdl_wait();
         mbar_arrive_expect_tx(bars.v_full(sv), C::KTILE);
         const bool v_wide = is_wide(j);
-        if (PAGED && !v_wide) {
-          // The row's fp16 copy is token-contiguous: one 128-token box per
-          // 64-element column block instead of one box per page.
+        if (PAGED && PCOPY) {
+          // The row's copy is token-contiguous: one 128-token box per
+          // 64-element column block instead of one box per page. It holds
+          // fp16 bits, or bf16 bits for a flagged tile (a byte copy: the map's
+          // fp16 type only sets the element size).
           const int tok = pb * pa.max_tiles * kBN + j * kBN;
           for (int s = 0; s < C::SUBS; ++s)
             tma_load_3d(sbase + C::V_OFF + sv * C::KTILE + s * C::SUB_BYTES, &tmap_v16,
@@ -471,6 +485,32 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
       if (!__all_sync(0xffffffffu, wait_or_abort(bars.s_full(t), j & 1, abort_flag))) {
         ok = false;
         break;
+      }
+      if constexpr (PAGED && !PCOPY) {
+        if (t == 0 && j == tail_info[0]) {
+          // Slots of the row's last page past its last key hold whatever the
+          // cache holds (possibly NaN or inf). Their weights are 0, but 0 * NaN
+          // is NaN in the P V product, so they are zeroed in the V tile before
+          // this head's arrival lets the MMA warp issue the tile's P V (the
+          // workspace copy, when there is one, has them zeroed already). The tile's V phase cannot
+          // move on before that P V, so the wait sees this tile's copy. Done
+          // before the S tile is loaded, while few registers are live.
+          const int sv = j % NSV;
+          if (wait_or_abort(bars.v_full(sv), (j / NSV) & 1, abort_flag)) {
+            // Thread r clears 16-byte chunk r % 8 of slot r / 8 past the last
+            // key, in every 64-column block (16 slots x 8 chunks = 128 threads).
+            if ((r >> 3) < (tail_info[1] >> 8)) {
+              const uint32_t a = sbase + C::V_OFF + sv * C::KTILE +
+                                 ((tail_info[1] & 0xff) + (r >> 3)) * 128 + (r & 7) * 16;
+#pragma unroll
+              for (int sub = 0; sub < C::SUBS; ++sub)
+                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a + sub * C::SUB_BYTES),
+                             "r"(0u)
+                             : "memory");
+            }
+            fence_proxy_async_smem();  // the MMA reads V through the async proxy
+          }
+        }
       }
       tc::fence_after();
       int lim = kBN;
@@ -627,7 +667,10 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
     if (ok) ok = __all_sync(0xffffffffu, wait_or_abort(bars.o_final(t), 0, abort_flag));
     if (ok) {
       tc::fence_after();
-      const bool empty = !(l > 0.f);
+      // A row with no allowed key has l = 0 exactly (every weight is ex2 of
+      // -inf). A NaN l (a NaN logit, or 0 * inf) is not empty: it reaches O
+      // and the LSE.
+      const bool empty = l == 0.f;
       const float inv = empty ? 0.f : 1.f / l;
       const size_t orow_idx = PAGED ? size_t(q_tok0 + row) * h + hq : size_t(hq) * T + row;
       // O leaves through this warp's quarter of its head's Q tile (the head's
@@ -732,19 +775,25 @@ __global__ void __launch_bounds__(256)
   if (threadIdx.x == 0) vwide[size_t(kvh) * n_tiles + tile] = wide;
 }
 
-// Paged V -> fp16 copy of the pages each row uses, token-contiguous per row:
+// Paged V -> a copy of the keys each row uses, token-contiguous per row:
 // [B, max_tiles * 128, h_kv, d_h] (row b's key t at token b * max_tiles * 128
-// + t), and flags [B, h_kv, max_tiles] with v_to_f16_kernel's meaning. Pages
-// from the row's last page to the end of its last 128-key tile, and
-// block-table entries outside the cache, are written as zeros: what the
-// bf16 path reads for them. Rows the attention kernel skips (query count
-// above the row's capacity) are left alone. The key count is clamped as the
-// attention kernel clamps it. One CTA per (tile, row, KV head).
+// + t), and flags [B, h_kv, max_tiles] with v_to_f16_kernel's meaning. A tile
+// is written as fp16 when every value converts exactly, else (flagged) as
+// the bf16 values themselves, so the attention kernel reads every V tile of
+// the row from this copy. Keys from the row's last key to the end of its last
+// 128-key tile, and pages whose block-table entry lies outside the cache, are
+// written as zeros, whatever the cache holds there. Rows the attention kernel
+// skips (query count above the row's capacity) are left alone. The key count
+// is clamped as the attention kernel clamps it. One CTA per (tile, row, KV
+// head); each thread holds its CPR / 2 chunks of 16 bytes between the range
+// check and the store.
+template <int CPR>
 __global__ void __launch_bounds__(256)
     paged_v_to_f16_kernel(const uint4* __restrict__ vc, const int32_t* __restrict__ block_table,
                           const int32_t* __restrict__ cu_q, const int32_t* __restrict__ seq_lens,
-                          int max_blocks, int num_blocks, int h_kv, int chunks_per_row,
-                          int max_tiles, uint4* __restrict__ v16, int* __restrict__ vwide) {
+                          int max_blocks, int num_blocks, int h_kv, int max_tiles,
+                          uint4* __restrict__ v16, int* __restrict__ vwide) {
+  constexpr int PER = kBN * CPR / 256;  // chunks per thread
   const int jt = blockIdx.x, b = blockIdx.y, kvh = blockIdx.z;
   const int cap = max_blocks * 16;
   const int q_len = cu_q[b + 1] - cu_q[b];
@@ -753,31 +802,41 @@ __global__ void __launch_bounds__(256)
   if (ctx < q_len || ctx > cap) ctx = ctx < q_len ? q_len : cap;
   const int n_pages = (ctx + 15) / 16;
   if (jt * 8 >= n_pages) return;
-  const int n = kBN * chunks_per_row;
+  uint4 x[PER];
   uint32_t mx = 0;
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    const int tok = i / chunks_per_row, c = i - tok * chunks_per_row;
+#pragma unroll
+  for (int u = 0; u < PER; ++u) {
+    const int i = threadIdx.x + 256 * u;
+    const int tok = i / CPR, c = i % CPR;
     const int page = jt * 8 + (tok >> 4), slot = tok & 15;
     int phys = -1;
-    if (page < n_pages) {
+    if (jt * kBN + tok < ctx) {
       phys = __ldg(block_table + size_t(b) * max_blocks + page);
       if (phys >= num_blocks) phys = -1;
     }
-    uint4 x = make_uint4(0u, 0u, 0u, 0u);
-    if (phys >= 0) x = vc[((size_t(phys) * 16 + slot) * h_kv + kvh) * chunks_per_row + c];
+    x[u] = make_uint4(0u, 0u, 0u, 0u);
+    if (phys >= 0) x[u] = vc[((size_t(phys) * 16 + slot) * h_kv + kvh) * CPR + c];
     uint32_t m2;
-    asm("max.u16x2 %0, %1, %2;" : "=r"(m2) : "r"(x.x & 0x7fff7fffu), "r"(x.y & 0x7fff7fffu));
-    asm("max.u16x2 %0, %0, %1;" : "+r"(m2) : "r"(x.z & 0x7fff7fffu));
-    asm("max.u16x2 %0, %0, %1;" : "+r"(m2) : "r"(x.w & 0x7fff7fffu));
+    asm("max.u16x2 %0, %1, %2;" : "=r"(m2) : "r"(x[u].x & 0x7fff7fffu), "r"(x[u].y & 0x7fff7fffu));
+    asm("max.u16x2 %0, %0, %1;" : "+r"(m2) : "r"(x[u].z & 0x7fff7fffu));
+    asm("max.u16x2 %0, %0, %1;" : "+r"(m2) : "r"(x[u].w & 0x7fff7fffu));
     asm("max.u16x2 %0, %0, %1;" : "+r"(mx) : "r"(m2));
-    uint4 y;
-    y.x = pack_f16x2(bf16lo(x.x), bf16hi(x.x));
-    y.y = pack_f16x2(bf16lo(x.y), bf16hi(x.y));
-    y.z = pack_f16x2(bf16lo(x.z), bf16hi(x.z));
-    y.w = pack_f16x2(bf16lo(x.w), bf16hi(x.w));
-    v16[((size_t(b) * max_tiles * kBN + size_t(jt) * kBN + tok) * h_kv + kvh) * chunks_per_row + c] = y;
   }
+  // bf16 bits 0x4780 = 2^16: the first magnitude fp16 cannot hold.
   const int wide = __syncthreads_or((mx & 0xffffu) >= 0x4780u || (mx >> 16) >= 0x4780u);
+#pragma unroll
+  for (int u = 0; u < PER; ++u) {
+    const int i = threadIdx.x + 256 * u;
+    const int tok = i / CPR, c = i % CPR;
+    uint4 y = x[u];
+    if (!wide) {
+      y.x = pack_f16x2(bf16lo(x[u].x), bf16hi(x[u].x));
+      y.y = pack_f16x2(bf16lo(x[u].y), bf16hi(x[u].y));
+      y.z = pack_f16x2(bf16lo(x[u].z), bf16hi(x[u].z));
+      y.w = pack_f16x2(bf16lo(x[u].w), bf16hi(x[u].w));
+    }
+    v16[((size_t(b) * max_tiles * kBN + size_t(jt) * kBN + tok) * h_kv + kvh) * CPR + c] = y;
+  }
   if (threadIdx.x == 0) vwide[(size_t(b) * h_kv + kvh) * max_tiles + jt] = wide;
 }
 
@@ -811,7 +870,7 @@ cudaError_t launch(const void* q, const void* k, const void* v, const void* v16,
                           CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  auto kern = prefill_bf16_kernel<D, NQ, NSK, NSV, false>;
+  auto kern = prefill_bf16_kernel<D, NQ, NSK, NSV, false, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   const int n_qblk = (T + kBM - 1) / kBM;
@@ -886,16 +945,17 @@ cudaError_t launch_paged(const PagedPrefill& a, cudaStream_t stream) {
     if (encode_tensor_map(&tv16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, a.v16, dims, strides, box,
                           CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
-    paged_v_to_f16_kernel<<<dim3(max_tiles, a.B, a.h_kv), 256, 0, stream>>>(
+    paged_v_to_f16_kernel<D / 8><<<dim3(max_tiles, a.B, a.h_kv), 256, 0, stream>>>(
         static_cast<const uint4*>(a.v_cache), a.block_table, a.cu_q, a.seq_lens, a.max_blocks,
-        a.num_blocks, a.h_kv, D / 8, max_tiles, static_cast<uint4*>(a.v16), a.vwide);
+        a.num_blocks, a.h_kv, max_tiles, static_cast<uint4*>(a.v16), a.vwide);
     const cudaError_t e0 = cudaGetLastError();
     if (e0 != cudaSuccess) return e0;
   }
   paged_tiles_kernel<<<1, 32, 0, stream>>>(a.cu_q, a.B, a.max_q_len, a.max_blocks, a.tile_off);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  auto kern = prefill_bf16_kernel<D, NQ, NSK, NSV, true>;
+  auto kern = a.v16 ? prefill_bf16_kernel<D, NQ, NSK, NSV, true, true>
+                    : prefill_bf16_kernel<D, NQ, NSK, NSV, true, false>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   // At most one partial tile per row beyond ceil(total_q / 128), and no row

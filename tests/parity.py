@@ -12,10 +12,17 @@ Tolerances (stated once, used by every parity test):
   * LSE (fp32): |lse_gpu - lse_ref| <= 1e-4; an empty row must give -inf
     exactly on both sides.
 
+    Inputs far outside N(0, 1): the kernels' weights carry a relative error
+    (2^-12 for fp16 P, 2^-16 for the two-term bf16 P), so the error of an
+    output grows with the attention-weighted |v|, sum_j p_j |v_j| / l. Tests
+    with values of 1e5 in V pass that weighted magnitude (the oracle applied
+    to |V|) as ``mag``; the 2e-3 then scales with max(1, mag).
+
 Every check also records how much of the slack it used: the raw max-abs
-error, how many elements exceed the bare 2e-3, the largest error in bf16 ulps
-of the reference, and how many elements equal the reference rounded to bf16.
-``STATS`` collects them; the test session prints a summary at its end.
+error, how many elements exceed the bare 2e-3, the largest error left after
+taking away the half ulp of rounding (the part the 2e-3 must cover), and how
+many elements equal the reference rounded to bf16. ``STATS`` collects them;
+the test session prints a summary at its end.
 """
 from __future__ import annotations
 
@@ -36,9 +43,10 @@ def ulp_bf16(x: np.ndarray) -> np.ndarray:
     return np.exp2(e - 7)
 
 
-def bf16_tol(r: np.ndarray) -> np.ndarray:
+def bf16_tol(r: np.ndarray, mag=None) -> np.ndarray:
     """Element-wise bound for a bf16 output whose exact value is r."""
-    return BF16_ABS + 0.5 * ulp_bf16(np.abs(r) + BF16_ABS)
+    a = BF16_ABS if mag is None else BF16_ABS * np.maximum(1.0, np.asarray(mag, np.float64))
+    return a + 0.5 * ulp_bf16(np.abs(r) + a)
 
 
 def to_np(t) -> np.ndarray:
@@ -59,24 +67,25 @@ def _record(what: str, dtype, o: np.ndarray, r: np.ndarray, err: np.ndarray):
            "max_abs": float(err.max()) if err.size else 0.0}
     if dtype == torch.bfloat16 and err.size:
         rec["above_2e-3"] = int((err > BF16_ABS).sum())
-        rec["max_ulp"] = float((err / ulp_bf16(r)).max())
+        # error beyond half an ulp of rounding: what the 2e-3 has to cover
+        rec["excess"] = float(np.maximum(err - 0.5 * ulp_bf16(np.abs(r) + BF16_ABS), 0.0).max())
         rec["rounded_ref"] = float((o == _bf16_round(r)).mean())
     STATS.append(rec)
     extra = ""
-    if "max_ulp" in rec:
-        extra = (f" above_2e-3={rec['above_2e-3']} max_ulp={rec['max_ulp']:.2f}"
+    if "excess" in rec:
+        extra = (f" above_2e-3={rec['above_2e-3']} excess={rec['excess']:.3e}"
                  f" equal_to_bf16(ref)={rec['rounded_ref']:.4f}")
     print(f"parity {what}: n={rec['n']} max_abs={rec['max_abs']:.3e}{extra}")
     return rec
 
 
-def check_out(out, ref, dtype, what="o"):
+def check_out(out, ref, dtype, what="o", mag=None):
     o = to_np(out)
     r = np.asarray(ref, dtype=np.float64)
     assert o.shape == r.shape, (o.shape, r.shape)
     assert np.all(np.isfinite(o)), f"{what}: non-finite output"
     err = np.abs(o - r)
-    tol = bf16_tol(r) if dtype == torch.bfloat16 else np.full_like(r, F32_ABS)
+    tol = bf16_tol(r, mag) if dtype == torch.bfloat16 else np.full_like(r, F32_ABS)
     bad = err > tol
     if bad.any():
         i = np.unravel_index(np.argmax(err - tol), err.shape)
@@ -108,14 +117,15 @@ def summary_lines() -> list[str]:
         return []
     outs = [s for s in STATS if not s.get("lse")]
     lses = [s for s in STATS if s.get("lse")]
-    bf = [s for s in outs if "max_ulp" in s]
+    bf = [s for s in outs if "excess" in s]
     lines = [f"parity summary (passing checks): {len(outs)} outputs ({sum(s['n'] for s in outs)} elements), "
              f"{len(lses)} LSE"]
     if bf:
         w = max(bf, key=lambda s: s["max_abs"])
+        x = max(bf, key=lambda s: s["excess"])
         lines.append(f"  bf16: worst max_abs {w['max_abs']:.3e} ({w['what']}), "
                      f"elements above the bare 2e-3: {sum(s['above_2e-3'] for s in bf)}, "
-                     f"worst {max(s['max_ulp'] for s in bf):.2f} ulp")
+                     f"worst error beyond rounding {x['excess']:.3e} ({x['what']})")
     if lses:
         w = max(lses, key=lambda s: s["max_abs"])
         lines.append(f"  lse: worst max_abs {w['max_abs']:.3e} ({w['what']})")
@@ -127,5 +137,48 @@ def summary_lines() -> list[str]:
         lines.append(f"  {name}: n={sum(s['n'] for s in ss)} "
                      f"max_abs={max(s['max_abs'] for s in ss):.3e} "
                      f"above_2e-3={sum(s['above_2e-3'] for s in ss)} "
-                     f"max_ulp={max(s['max_ulp'] for s in ss):.2f}")
+                     f"excess={max(s['excess'] for s in ss):.3e} "
+                     f"equal_to_bf16(ref)={min(s['rounded_ref'] for s in ss):.4f}")
     return lines
+
+
+def check_nonfinite(out, ref, dtype, what="o", extra=None):
+    """Outputs for inputs holding NaN or inf, against the oracle (IEEE
+    arithmetic on the definition over each row's allowed keys):
+      * where the oracle is NaN the output must be NaN;
+      * where it is +-inf, NaN or that same infinity: the kernels form p * v
+        from two bf16 terms p_hi + p_lo, and 0 * inf is NaN when p_lo is 0,
+        so which of the two is not promised;
+      * where it is finite, finite and within the usual tolerance, except on
+        the elements of ``extra`` (a boolean mask): there a stated exception
+        makes the output NaN, and it must be NaN.
+    Returns the number of non-finite elements the oracle predicts."""
+    o = to_np(out)
+    r = np.asarray(ref, dtype=np.float64)
+    assert o.shape == r.shape, (o.shape, r.shape)
+    nan_r, inf_r, fin_r = np.isnan(r), np.isinf(r), np.isfinite(r)
+    assert np.isnan(o[nan_r]).all(), f"{what}: {int((~np.isnan(o[nan_r])).sum())} NaN of the oracle not NaN"
+    oi, ri = o[inf_r], r[inf_r]
+    assert (np.isnan(oi) | (oi == ri)).all(), f"{what}: an infinity of the oracle came out finite or flipped"
+    ex = np.zeros(r.shape, bool) if extra is None else np.asarray(extra, bool)
+    assert np.isnan(o[ex & fin_r]).all(), f"{what}: the stated exception did not give NaN"
+    keep = fin_r & ~ex
+    assert np.isfinite(o[keep]).all(), f"{what}: {int((~np.isfinite(o[keep])).sum())} finite oracle values came out non-finite"
+    err = np.abs(o[keep] - r[keep])
+    tol = bf16_tol(r[keep]) if dtype == torch.bfloat16 else np.full(err.shape, F32_ABS)
+    assert (err <= tol).all(), f"{what}: {int((err > tol).sum())} finite elements out of tolerance"
+    return int((~fin_r).sum())
+
+
+def check_lse_nonfinite(out, ref, what="lse"):
+    """LSE of rows with non-finite inputs: NaN where the oracle is NaN,
+    -inf exactly where it is -inf, within 1e-4 elsewhere."""
+    o = to_np(out)
+    r = np.asarray(ref, dtype=np.float64)
+    assert o.shape == r.shape
+    assert np.isnan(o[np.isnan(r)]).all(), f"{what}: NaN of the oracle not NaN"
+    assert np.array_equal(np.isneginf(o), np.isneginf(r)), f"{what}: -inf pattern differs"
+    fin = np.isfinite(r)
+    assert np.isfinite(o[fin]).all(), f"{what}: finite oracle values came out non-finite"
+    if fin.any():
+        assert np.abs(o[fin] - r[fin]).max() <= LSE_ABS, f"{what}: out of tolerance"

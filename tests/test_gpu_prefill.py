@@ -100,8 +100,9 @@ def test_bf16_wide_values_keep_exact_path(d):
     v[1, 300, 7] = -7.0e4    # key tile 2 of KV head 1
     v[1, 20, 0] = 65280.0    # largest bf16 below 2^16 (fits fp16): tile 0 stays fp16
     O_ref, L_ref = oracle.attention_ref(q, k, v, shape.scale, True)
+    mag, _ = oracle.attention_ref(q, k, v.abs(), shape.scale, True)  # weighted |v|
     o, lse = run(q, k, v, True, shape.scale)
-    check_out(o, O_ref, torch.bfloat16)
+    check_out(o, O_ref, torch.bfloat16, mag=mag)
     check_lse(lse, L_ref)
 
 

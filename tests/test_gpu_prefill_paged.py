@@ -96,8 +96,10 @@ def v16_layout(B, max_blocks, h_kv, d):
 
 def test_fp16_copy_layout_and_flags():
     """The workspace's fp16 copy holds each row's keys token-contiguously
-    (row b's key t at token b * tiles * 128 + t), zeros from the row's last page
-    to the end of its last 128-key tile, and a zero flag for tiles fp16 holds."""
+    (row b's key t at token b * tiles * 128 + t), zeros from the row's last key
+    to the end of its last 128-key tile (the slots of the last page past the
+    row's length included, whatever the cache holds there), and a zero flag
+    for tiles fp16 holds."""
     h, h_kv, d = 4, 2, 64
     q_lens, ctx = [5, 40, 1], [300, 40, 129]
     q, kc, vc, table, cu, seq = paged_batch(q_lens, ctx, h, h_kv, d, 6)
@@ -115,9 +117,9 @@ def test_fp16_copy_layout_and_flags():
         pages = -(-ctx[b] // 16)
         used_tiles = -(-pages // 8)
         assert (flags[b, :, :used_tiles] == 0).all()
-        keys = torch.stack([vc[table[b, t // 16], t % 16] for t in range(pages * 16)])
-        assert torch.equal(v16[b, :pages * 16], keys.to(torch.float16))
-        assert (v16[b, pages * 16:used_tiles * 128] == 0).all()
+        keys = torch.stack([vc[table[b, t // 16], t % 16] for t in range(ctx[b])])
+        assert torch.equal(v16[b, :ctx[b]], keys.to(torch.float16))
+        assert (v16[b, ctx[b]:used_tiles * 128] == 0).all()
 
 
 @pytest.mark.parametrize("causal", [True, False])
@@ -146,7 +148,8 @@ def test_wide_v_tiles_match_oracle(causal):
             if flags[b, k, t] != 0}
     assert wide == {(0, 1, 0), (1, 0, 2)}
     O_ref, L_ref = oracle.prefill_paged_ref(q, kc, vc, table, cu, seq, scale, causal)
-    check_out(o, O_ref, torch.bfloat16)
+    mag, _ = oracle.prefill_paged_ref(q, kc, vc.abs(), table, cu, seq, scale, causal)  # weighted |v|
+    check_out(o, O_ref, torch.bfloat16, mag=mag)
     check_lse(lse, L_ref)
 
 
