@@ -24,9 +24,9 @@
  *     memory) unless a parameter says otherwise; the caller owns every buffer.
  *     The library never allocates memory, frees or synchronises: each call
  *     only enqueues work on `stream` (a cudaStream_t; NULL = legacy default
- *     stream) and returns. The one exception is attn_prefill_host, whose
- *     first call on a device creates two copy streams and an event pool that
- *     it keeps (no memory allocation).
+ *     stream) and returns. The one exception is attn_prefill_host called
+ *     without a pipe of the caller's: its first call on a device creates two
+ *     copy streams and five events that it keeps (no memory allocation).
  *   - Tensors are dense, row-major, with the shapes given below. Tensor base
  *     pointers must be 16-byte aligned (TMA and 128-bit vector loads);
  *     `workspace` must be 256-byte aligned.
@@ -147,19 +147,41 @@ attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o,
  *                     stream continues only after the last output copy; the
  *                     host buffers may be read after that work completes
  *                     (e.g. cudaStreamSynchronize). Returns once queued.
- * Two copy streams and an event pool per device are created on the first
- * call (which therefore must not be inside a stream capture) and kept;
- * later calls, including captured ones, create nothing. Calls from several
- * host threads are serialised while they queue work.
+ *   pipe              NULL, or the caller's two copy streams and five events
+ *                     (attn_host_pipe_t below): with them the call creates
+ *                     nothing. With NULL the library creates such a pipe per
+ *                     device on the first call without one (that first call
+ *                     must therefore not be inside a stream capture) and
+ *                     keeps it; calls on one device then hold a per-device
+ *                     lock while they queue work.
+ * Pageable host buffers work, but a copy from or to pageable memory blocks
+ * the calling thread until it completes, so the groups do not overlap and
+ * the call returns only after the last output copy (holding the device's
+ * lock when pipe is NULL).
  * Errors: as attn_prefill, plus INVALID_ARG for n_chunks < 0, n_chunks > 64,
  * h_kv % n_chunks != 0, a NULL or misaligned scratch or one that is too
- * small; ATTN_ERR_CUDA if a copy, event or launch fails.
+ * small, a pipe with a NULL member, with copy_in == copy_out or with either
+ * equal to `stream`; UNSUPPORTED for more than 65535 query tiles of 128 on
+ * the bf16 path (T > 8388480). All of these are found before anything is
+ * queued. ATTN_ERR_CUDA if a copy, event or launch fails; the caller's
+ * stream is then still joined to both copy streams, so nothing queued by the
+ * call can touch the host buffers after the stream's later work starts.
  */
+#define ATTN_HOST_PIPE_EVENTS 5
+typedef struct attn_host_pipe {
+  void* copy_in;   /* cudaStream_t for host-to-device copies                  */
+  void* copy_out;  /* cudaStream_t for device-to-host copies                  */
+  void* events[ATTN_HOST_PIPE_EVENTS]; /* cudaEvent_t each, e.g. created with
+                                          cudaEventDisableTiming; re-recorded
+                                          by every call (one call at a time
+                                          per pipe)                          */
+} attn_host_pipe_t;
 size_t attn_prefill_host_scratch_bytes(int T, int h, int h_kv, int d_h, attn_dtype_t dtype);
 attn_status_t attn_prefill_host(const void* q, const void* k, const void* v, void* o, float* lse,
                                 int T, int h, int h_kv, int d_h, int causal, float scale,
                                 attn_dtype_t dtype, int n_chunks, void* scratch,
-                                size_t scratch_bytes, void* stream);
+                                size_t scratch_bytes, const attn_host_pipe_t* pipe,
+                                void* stream);
 
 /*
  * attn_prefill_paged -- exact attention for a batch of variable-length query
@@ -379,8 +401,10 @@ attn_status_t attn_decode_paged_deterministic(const void* q, const void* k_cache
  *     ATTN_ERR_INVALID_ARG before anything is launched (use fewer splits, a
  *     smaller batch, or attn_decode_paged);
  *   - the first call on each device looks up the array's device address with
- *     cudaGetSymbolAddress (with that device current) and caches it; make that
- *     first call on a device before any stream capture;
+ *     cudaGetSymbolAddress (with that device current) and keeps it for that
+ *     device's context; a later call in a new context (after
+ *     cudaDeviceReset) looks it up again. Make the first call on a device
+ *     (and the first after a reset) before any stream capture;
  *   - every call on a device shares the one array, which keeps the last
  *     call's partials. Nothing in it needs to start at zero. Calls whose
  *     kernels can overlap on the GPU (different streams with no ordering

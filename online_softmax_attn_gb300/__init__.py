@@ -69,7 +69,7 @@ def library() -> ctypes.CDLL:
     lib.attn_selftest_wait_timeout.restype = I
     lib.attn_prefill_host_scratch_bytes.argtypes = [I, I, I, I, I]
     lib.attn_prefill_host_scratch_bytes.restype = S
-    lib.attn_prefill_host.argtypes = [P, P, P, P, P, I, I, I, I, I, F, I, I, P, S, P]
+    lib.attn_prefill_host.argtypes = [P, P, P, P, P, I, I, I, I, I, F, I, I, P, S, P, P]
     lib.attn_prefill_host.restype = I
     lib.attn_prefill_paged_workspace_bytes.argtypes = [I]
     lib.attn_prefill_paged_workspace_bytes.restype = S
@@ -183,12 +183,39 @@ def attn_prefill_host_scratch_bytes(T: int, h: int, h_kv: int, d_h: int, dtype=t
     return int(n)
 
 
+ATTN_HOST_PIPE_EVENTS = 5
+
+
+class HostPipe(ctypes.Structure):
+    """attn_host_pipe_t: the caller's two copy streams and five events."""
+    _fields_ = [("copy_in", ctypes.c_void_p), ("copy_out", ctypes.c_void_p),
+                ("events", ctypes.c_void_p * ATTN_HOST_PIPE_EVENTS)]
+
+
+def make_host_pipe(copy_in, copy_out, events):
+    """A HostPipe from two torch.cuda.Stream and five torch.cuda.Event
+    (created without timing). The events are recorded once here, which makes
+    torch create them; keep the torch objects alive while the pipe is used."""
+    _need(len(events) == ATTN_HOST_PIPE_EVENTS, f"need {ATTN_HOST_PIPE_EVENTS} events")
+    for e in events:
+        e.record(copy_in)
+    hp = HostPipe()
+    hp.copy_in = copy_in.cuda_stream
+    hp.copy_out = copy_out.cuda_stream
+    for i, e in enumerate(events):
+        hp.events[i] = e.cuda_event
+    hp._keep = (copy_in, copy_out, tuple(events))
+    return hp
+
+
 def attn_prefill_host(q, k, v, causal: bool, scale: float | None = None, o=None, lse=None,
-                      return_lse: bool = True, scratch=None, n_chunks: int = 0, stream=None):
+                      return_lse: bool = True, scratch=None, n_chunks: int = 0, stream=None,
+                      pipe: HostPipe | None = None):
     """attn_prefill on host tensors: q [h,T,d], k/v [h_kv,T,d] (bf16 or fp32,
     CPU, contiguous; pinned memory lets the copies overlap the compute). The
     copies in and out run inside the call, pipelined over groups of KV heads
-    on the current CUDA device. Returns host (o, lse); they are complete once
+    on the current CUDA device, on the copy streams of ``pipe`` (a HostPipe;
+    None: the library's own). Returns host (o, lse); they are complete once
     ``stream`` (default: the current stream) has run the queued work."""
     for t in (q, k, v):
         _need(t.device.type == "cpu" and t.is_contiguous(), "q, k, v must be contiguous CPU tensors")
@@ -213,7 +240,8 @@ def attn_prefill_host(q, k, v, causal: bool, scale: float | None = None, o=None,
     dt = ATTN_DTYPE_BF16 if q.dtype == torch.bfloat16 else ATTN_DTYPE_F32
     st = library().attn_prefill_host(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), T, h, h_kv, d,
                                      int(bool(causal)), scale, dt, int(n_chunks), _ptr(scratch),
-                                     scratch.numel(), _stream(stream))
+                                     scratch.numel(), None if pipe is None else ctypes.byref(pipe),
+                                     _stream(stream))
     _check("attn_prefill_host", st)
     return o, lse
 

@@ -13,9 +13,12 @@
 // module loader reserves it on every GPU that loads this library, and it
 // stays reserved until the process exits. In host code the name
 // g_decode_static_scratch is only a host-side stand-in for the symbol, not a
-// device address; the real address is looked up with cudaGetSymbolAddress
-// once per device, with that device current, the first time this entry point
-// runs there.
+// device address; the real address is looked up with cudaGetSymbolAddress,
+// with the device current, the first time this entry point runs on a device,
+// and again whenever that device's context has changed since (after a
+// cudaDeviceReset the module is loaded anew and the array can move).
+#include <cudaTypedefs.h>
+
 #include <cmath>
 #include <mutex>
 
@@ -30,9 +33,38 @@ static __device__ __align__(256) unsigned char g_decode_static_scratch[ATTN_DECO
 
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mutex;
-void* g_scratch_ptr[kMaxDevices] = {};
+struct ScratchAddr {
+  void* ptr = nullptr;
+  unsigned long long ctx_id = 0;  // unique id of the context the address belongs to
+};
+ScratchAddr g_scratch[kMaxDevices];
 
-// Device address of this device's copy of the scratch array (nullptr on error).
+// Unique id of the calling thread's current context (0 when it cannot be
+// read, in which case the address is looked up on every call).
+unsigned long long current_context_id() {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current == nullptr || get_id == nullptr || get_current(&ctx) != CUDA_SUCCESS ||
+      ctx == nullptr || get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// Device address of the current device's copy of the scratch array (nullptr
+// on error, with the CUDA error in *err).
 void* scratch_for_current_device(cudaError_t* err) {
   int dev = -1;
   *err = cudaGetDevice(&dev);
@@ -41,14 +73,20 @@ void* scratch_for_current_device(cudaError_t* err) {
     *err = cudaErrorInvalidDevice;
     return nullptr;
   }
+  // Before the device's first runtime call no context is current and the id
+  // reads 0; the symbol lookup then creates the context, and its id is read
+  // again for the next call.
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (g_scratch_ptr[dev] == nullptr) {
+  ScratchAddr& a = g_scratch[dev];
+  const unsigned long long id = current_context_id();
+  if (a.ptr == nullptr || id == 0 || id != a.ctx_id) {
     void* p = nullptr;
     *err = cudaGetSymbolAddress(&p, g_decode_static_scratch);
     if (*err != cudaSuccess) return nullptr;
-    g_scratch_ptr[dev] = p;
+    a.ptr = p;
+    a.ctx_id = id != 0 ? id : current_context_id();
   }
-  return g_scratch_ptr[dev];
+  return a.ptr;
 }
 
 bool aligned_to(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }

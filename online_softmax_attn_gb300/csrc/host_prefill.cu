@@ -5,9 +5,10 @@
 // The layer is cut into groups of KV heads, each with its query heads (heads
 // are the outermost dimension, so a group is one contiguous slice of every
 // tensor). Group c+1's inputs copy in while group c computes and group c-1's
-// outputs copy out: the copies run on two library-owned streams, the
-// attention on the caller's stream, ordered by events (fork from and join
-// back to the caller's stream, which CUDA graph capture follows). Each group
+// outputs copy out: the copies run on two copy streams (the caller's, or a
+// pair the library creates on first use), the attention on the caller's
+// stream, ordered by events (fork from and join back to the caller's stream,
+// which CUDA graph capture follows). Each group
 // is an independent prefill over its heads ("Naive attention and the online
 // softmax": every query row's recurrence reads only its own head's Q and its
 // KV head's K, V), so results are bitwise those of attn_prefill.
@@ -25,41 +26,45 @@ constexpr int kMaxDevices = 64;
 
 bool aligned_to(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// Per device: an inbound and an outbound copy stream and an event pool,
-// created on the first call and kept for the life of the process.
-struct HostPipe {
+// The streams and events one call orders its work with. An event is re-recorded
+// once the wait on its previous record has been enqueued: a stream wait binds
+// to the record that precedes it, so five events serve any number of groups.
+struct Pipe {
   cudaStream_t in = nullptr, out = nullptr;
-  cudaEvent_t ev[2 * kMaxChunks + 2] = {};
-  bool ready = false;
+  cudaEvent_t ev[ATTN_HOST_PIPE_EVENTS] = {};
 };
-std::mutex g_pipe_mu;  // guards creation and the enqueue sequence (shared events)
-HostPipe g_pipes[kMaxDevices];
+enum { kEvStart = 0, kEvIn = 1, kEvCmp = 2, kEvInDone = 3, kEvOutDone = 4 };
 
-void destroy_pipe(HostPipe& p) {
+// Library-owned pipes, one per device, created on the first call that passes
+// no pipe of its own, and kept for the life of the process. Each has its own
+// lock, held while a call enqueues on it.
+struct OwnedPipe {
+  Pipe p;
+  bool ready = false;
+  std::mutex mu;
+};
+OwnedPipe g_pipes[kMaxDevices];
+
+void destroy_pipe(Pipe& p) {
   for (cudaEvent_t& e : p.ev)
     if (e) (void)cudaEventDestroy(e), e = nullptr;
   if (p.in) (void)cudaStreamDestroy(p.in), p.in = nullptr;
   if (p.out) (void)cudaStreamDestroy(p.out), p.out = nullptr;
 }
 
-cudaError_t pipe_for_current_device(HostPipe** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  HostPipe& p = g_pipes[dev];
-  if (!p.ready) {
-    e = cudaStreamCreateWithFlags(&p.in, cudaStreamNonBlocking);
-    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p.out, cudaStreamNonBlocking);
-    for (int i = 0; e == cudaSuccess && i < 2 * kMaxChunks + 2; ++i)
-      e = cudaEventCreateWithFlags(&p.ev[i], cudaEventDisableTiming);
-    if (e != cudaSuccess) {
-      destroy_pipe(p);
-      return e;
-    }
-    p.ready = true;
+// Called with the device's lock held.
+cudaError_t ensure_owned_pipe(OwnedPipe& op) {
+  if (op.ready) return cudaSuccess;
+  Pipe& p = op.p;
+  cudaError_t e = cudaStreamCreateWithFlags(&p.in, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p.out, cudaStreamNonBlocking);
+  for (int i = 0; e == cudaSuccess && i < ATTN_HOST_PIPE_EVENTS; ++i)
+    e = cudaEventCreateWithFlags(&p.ev[i], cudaEventDisableTiming);
+  if (e != cudaSuccess) {
+    destroy_pipe(p);
+    return e;
   }
-  *out = &p;
+  op.ready = true;
   return cudaSuccess;
 }
 
@@ -125,7 +130,8 @@ size_t attn_prefill_host_scratch_bytes(int T, int h, int h_kv, int d_h, attn_dty
 attn_status_t attn_prefill_host(const void* q, const void* k, const void* v, void* o, float* lse,
                                 int T, int h, int h_kv, int d_h, int causal, float scale,
                                 attn_dtype_t dtype, int n_chunks, void* scratch,
-                                size_t scratch_bytes, void* stream) {
+                                size_t scratch_bytes, const attn_host_pipe_t* pipe,
+                                void* stream) {
   if (T < 0 || h < 1 || h_kv < 1 || h % h_kv != 0 || h > 65535 || !std::isfinite(scale) ||
       !(scale > 0.f))
     return ATTN_ERR_INVALID_ARG;
@@ -138,6 +144,16 @@ attn_status_t attn_prefill_host(const void* q, const void* k, const void* v, voi
   if (!aligned_to(scratch, 256) ||
       scratch_bytes < attn_prefill_host_scratch_bytes(T, h, h_kv, d_h, dtype))
     return ATTN_ERR_INVALID_ARG;
+  if (pipe != nullptr) {
+    if (!pipe->copy_in || !pipe->copy_out || pipe->copy_in == pipe->copy_out ||
+        pipe->copy_in == stream || pipe->copy_out == stream)
+      return ATTN_ERR_INVALID_ARG;
+    for (int i = 0; i < ATTN_HOST_PIPE_EVENTS; ++i)
+      if (!pipe->events[i]) return ATTN_ERR_INVALID_ARG;
+  }
+  // The attention kernels' own limits, checked before anything is queued.
+  if (dtype == ATTN_DTYPE_BF16 && (static_cast<long long>(T) + 127) / 128 > 65535)
+    return ATTN_ERR_UNSUPPORTED;
   int sizes[kMaxChunks];
   const int chunks = chunk_plan(h_kv, n_chunks, sizes);
   const size_t elem = dtype == ATTN_DTYPE_F32 ? 4 : 2;
@@ -158,27 +174,36 @@ attn_status_t attn_prefill_host(const void* q, const void* k, const void* v, voi
   auto* hl = reinterpret_cast<uint8_t*>(lse);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-  std::lock_guard<std::mutex> lock(g_pipe_mu);
-  HostPipe* P = nullptr;
-  cudaError_t e = pipe_for_current_device(&P);
-  if (e != cudaSuccess) return ATTN_ERR_CUDA;
-  cudaEvent_t ev_start = P->ev[0], ev_done = P->ev[1];
+  Pipe P;
+  std::unique_lock<std::mutex> lock;
+  if (pipe != nullptr) {
+    P.in = static_cast<cudaStream_t>(pipe->copy_in);
+    P.out = static_cast<cudaStream_t>(pipe->copy_out);
+    for (int i = 0; i < ATTN_HOST_PIPE_EVENTS; ++i)
+      P.ev[i] = static_cast<cudaEvent_t>(pipe->events[i]);
+  } else {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+    lock = std::unique_lock<std::mutex>(g_pipes[dev].mu);
+    if (ensure_owned_pipe(g_pipes[dev]) != cudaSuccess) return ATTN_ERR_CUDA;
+    P = g_pipes[dev].p;
+  }
   // Both copy streams start after the work already queued on the caller's
   // stream (which may still be using the scratch).
-  e = cudaEventRecord(ev_start, s);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(P->in, ev_start, 0);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(P->out, ev_start, 0);
+  cudaError_t e = cudaEventRecord(P.ev[kEvStart], s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(P.in, P.ev[kEvStart], 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(P.out, P.ev[kEvStart], 0);
   for (int c = 0, kv0 = 0; e == cudaSuccess && c < chunks; kv0 += sizes[c], ++c) {
-    cudaEvent_t ev_in = P->ev[2 + c], ev_cmp = P->ev[2 + kMaxChunks + c];
+    cudaEvent_t ev_in = P.ev[kEvIn], ev_cmp = P.ev[kEvCmp];
     const int kvc = sizes[c], hc = kvc * g;
     const size_t oq = size_t(kv0) * g * q_head, okv = size_t(kv0) * q_head;
     const size_t ol = size_t(kv0) * g * l_head;
     const size_t q_bytes = size_t(hc) * q_head, kv_bytes = size_t(kvc) * q_head;
     const size_t l_bytes = size_t(hc) * l_head;
-    e = cudaMemcpyAsync(dk + okv, hk + okv, kv_bytes, cudaMemcpyHostToDevice, P->in);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(dv + okv, hv + okv, kv_bytes, cudaMemcpyHostToDevice, P->in);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(dq + oq, hq + oq, q_bytes, cudaMemcpyHostToDevice, P->in);
-    if (e == cudaSuccess) e = cudaEventRecord(ev_in, P->in);
+    e = cudaMemcpyAsync(dk + okv, hk + okv, kv_bytes, cudaMemcpyHostToDevice, P.in);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dv + okv, hv + okv, kv_bytes, cudaMemcpyHostToDevice, P.in);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dq + oq, hq + oq, q_bytes, cudaMemcpyHostToDevice, P.in);
+    if (e == cudaSuccess) e = cudaEventRecord(ev_in, P.in);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ev_in, 0);
     if (e == cudaSuccess) {
       if (dtype == ATTN_DTYPE_F32)
@@ -194,16 +219,19 @@ attn_status_t attn_prefill_host(const void* q, const void* k, const void* v, voi
                                 hc, kvc, d_h, causal != 0, scale, dws, s);
     }
     if (e == cudaSuccess) e = cudaEventRecord(ev_cmp, s);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(P->out, ev_cmp, 0);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(ho + oq, dO + oq, q_bytes, cudaMemcpyDeviceToHost, P->out);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(P.out, ev_cmp, 0);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(ho + oq, dO + oq, q_bytes, cudaMemcpyDeviceToHost, P.out);
     if (e == cudaSuccess && hl)
       e = cudaMemcpyAsync(hl + ol, reinterpret_cast<uint8_t*>(dl) + ol, l_bytes,
-                          cudaMemcpyDeviceToHost, P->out);
+                          cudaMemcpyDeviceToHost, P.out);
   }
-  // Join: the caller's stream continues after the last output copy. Done
-  // even after an error, so both copy streams are joined back.
-  cudaError_t ej = cudaEventRecord(ev_done, P->out);
-  if (ej == cudaSuccess) ej = cudaStreamWaitEvent(s, ev_done, 0);
+  // Join: the caller's stream continues after the last copy of both copy
+  // streams. Done even after an error, so that nothing queued on them can
+  // still read or write the caller's buffers once the stream moves on.
+  cudaError_t ej = cudaEventRecord(P.ev[kEvInDone], P.in);
+  if (ej == cudaSuccess) ej = cudaStreamWaitEvent(s, P.ev[kEvInDone], 0);
+  if (ej == cudaSuccess) ej = cudaEventRecord(P.ev[kEvOutDone], P.out);
+  if (ej == cudaSuccess) ej = cudaStreamWaitEvent(s, P.ev[kEvOutDone], 0);
   if (e == cudaSuccess) e = ej;
   if (e == cudaErrorNotSupported) return ATTN_ERR_UNSUPPORTED;
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;

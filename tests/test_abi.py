@@ -273,3 +273,31 @@ def test_selftest_wait_timeout_arguments(lib):
 def test_version(lib):
     lib.attn_version.restype = ctypes.c_int
     assert lib.attn_version() == 202
+
+
+def test_prefill_host_checks_limits_before_queueing(lib):
+    """attn_prefill_host refuses a bf16 layer with more than 65535 query tiles
+    of 128, and a pipe with a missing member, before it touches any pointer or
+    queues anything: the pointers here are placeholders no GPU could use, and
+    no GPU is needed."""
+    P, I, F, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    f = lib.attn_prefill_host
+    f.argtypes = [P, P, P, P, P, I, I, I, I, I, F, I, I, P, S, P, P]
+    f.restype = I
+    fake = ctypes.c_void_p(4096)
+    big_T = 65536 * 128
+    st = f(fake, fake, fake, fake, None, big_T, 1, 1, 64, 1, 0.125, attn.ATTN_DTYPE_BF16, 1, fake,
+           ctypes.c_size_t(-1).value, None, None)
+    assert st == attn.ATTN_ERR_UNSUPPORTED
+    pipe = attn.HostPipe()
+    pipe.copy_in, pipe.copy_out = 4096, 8192
+    for i in range(attn.ATTN_HOST_PIPE_EVENTS - 1):
+        pipe.events[i] = 4096 * (i + 3)
+    st = f(fake, fake, fake, fake, None, 256, 1, 1, 64, 1, 0.125, attn.ATTN_DTYPE_BF16, 1, fake,
+           ctypes.c_size_t(-1).value, ctypes.byref(pipe), None)
+    assert st == attn.ATTN_ERR_INVALID_ARG
+    pipe.copy_out = pipe.copy_in
+    pipe.events[attn.ATTN_HOST_PIPE_EVENTS - 1] = 4096 * 99
+    st = f(fake, fake, fake, fake, None, 256, 1, 1, 64, 1, 0.125, attn.ATTN_DTYPE_BF16, 1, fake,
+           ctypes.c_size_t(-1).value, ctypes.byref(pipe), None)
+    assert st == attn.ATTN_ERR_INVALID_ARG

@@ -101,3 +101,48 @@ def test_bad_chunk_count_is_rejected():
     q, k, v = W.prefill_inputs(W.PrefillShape("host_bad", 8, 4, 64, 64, torch.bfloat16, True), 1)
     with pytest.raises(RuntimeError):
         attn.attn_prefill_host(q, k, v, True, n_chunks=3)
+
+
+def _caller_pipe():
+    ins, outs = torch.cuda.Stream(), torch.cuda.Stream()
+    evs = [torch.cuda.Event() for _ in range(attn.ATTN_HOST_PIPE_EVENTS)]
+    return attn.make_host_pipe(ins, outs, evs)
+
+
+@pytest.mark.parametrize("n_chunks", [0, 8])
+def test_caller_pipe_bitwise(n_chunks):
+    """The caller's copy streams and events: the library creates nothing, the
+    five events are reused across the groups (8 groups here), and the result
+    is bitwise that of attn_prefill."""
+    shape = W.PrefillShape("host_pipe", 16, 8, 128, 333, torch.bfloat16, True)
+    q, k, v = W.prefill_inputs(shape, 8)
+    hq, hk, hv = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    pipe = _caller_pipe()
+    o, lse = attn.attn_prefill_host(hq, hk, hv, True, shape.scale, n_chunks=n_chunks, pipe=pipe)
+    torch.cuda.synchronize()
+    o_ref, l_ref = device_result(q, k, v, True, shape.scale)
+    assert torch.equal(o, o_ref) and torch.equal(lse, l_ref)
+
+
+def test_caller_pipe_captured_without_a_prior_call():
+    """With the caller's pipe nothing is created inside the call, so its very
+    first call may be inside a stream capture."""
+    shape = W.PrefillShape("host_pipe_graph", 8, 4, 64, 200, torch.bfloat16, False)
+    q, k, v = W.prefill_inputs(shape, 9)
+    hq, hk, hv = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    ho = torch.empty_like(hq).pin_memory()
+    hl = torch.empty((8, 200), dtype=torch.float32).pin_memory()
+    scratch = torch.empty(attn.attn_prefill_host_scratch_bytes(200, 8, 4, 64), dtype=torch.uint8,
+                          device="cuda")
+    pipe = _caller_pipe()
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            attn.attn_prefill_host(hq, hk, hv, False, shape.scale, o=ho, lse=hl, scratch=scratch,
+                                   pipe=pipe)
+    g.replay()
+    torch.cuda.synchronize()
+    o_ref, l_ref = device_result(q, k, v, False, shape.scale)
+    assert torch.equal(ho, o_ref) and torch.equal(hl, l_ref)

@@ -5,8 +5,9 @@ It serves callers that cannot allocate device memory where they call decode
 hot loop that must not call cudaMalloc). It keeps the split partials in a
 fixed array inside the library instead of a caller workspace. These tests
 call it through the C ABI and compare it with attn_decode_paged on the same
-inputs, for two calls in a row with different batches (the array keeps the
-previous call's contents, which must not leak into the next result).
+inputs, and both with the float64 oracle, for two calls in a row with
+different batches (the array keeps the previous call's contents, which must
+not leak into the next result).
 """
 import ctypes
 
@@ -14,6 +15,7 @@ import pytest
 import torch
 
 import online_softmax_attn_gb300 as attn
+import oracle
 import workloads as W
 from parity import check_lse, check_out, to_np
 
@@ -59,6 +61,10 @@ def test_static_scratch_matches_workspace_entry_point_twice(lib):
         torch.cuda.synchronize()
         check_out(o, to_np(o_ref), torch.bfloat16, f"static o (seed {seed})")
         check_lse(lse, to_np(lse_ref), f"static lse (seed {seed})")
+        O_or, L_or = oracle.decode_paged_ref(q.cpu(), kc.cpu(), vc.cpu(), table.cpu(), seq.cpu(),
+                                             shape.scale)
+        check_out(o, O_or, torch.bfloat16, f"static o vs oracle (seed {seed})")
+        check_lse(lse, L_or, f"static lse vs oracle (seed {seed})")
     assert attn.attn_get_device_error() == 0
 
 
