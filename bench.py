@@ -40,8 +40,8 @@ METRIC = "prefill attention TFLOP/s; paged decode KV GB/s (fraction of GB300 roo
 PREFILL = W.GQA_T8192_CAUSAL
 DECODE = W.DECODE_PAGED_B64
 
-# DRAM traffic per launch from one ncu capture of the kernel (see profiles/),
-# valid only for the kernel source it was taken on (hash of its files).
+# DRAM traffic per launch from one ncu capture of the kernel, valid only for
+# the kernel source it was taken on (hash of its files).
 KERNEL_FILES = {
     "prefill": ["online_softmax_attn_gb300/csrc/prefill_tc.cu", "online_softmax_attn_gb300/csrc/tc.cuh",
                 "online_softmax_attn_gb300/csrc/common.cuh", "online_softmax_attn_gb300/csrc/pdl.cuh"],
@@ -53,13 +53,15 @@ KERNEL_FILES["merge_pair"] = ["online_softmax_attn_gb300/csrc/merge.cu", "online
                               "online_softmax_attn_gb300/csrc/pdl.cuh"]
 NCU_TRAFFIC = {
     # kind: (dram read + write bytes per launch, sha256[:16] of the kernel's files)
-    "prefill": (135.65e6, "54c8b6f9626d119d"),  # profiles/prefill_bf16_T8192_causal.md
-    "prefill_paged": (465.07e6, "54c8b6f9626d119d"),  # profiles/prefill_paged_B8_q1024_ctx8192.md
-    # decode: 16-row capture (303.7 MB for 299.5 MB algorithmic) scaled by KV bytes to the
-    # 66-row batch (profiles/decode_split_paged_B16.md)
+    # prefill_bf16_kernel, causal T=8192 layer, full-size capture
+    "prefill": (135.65e6, "54c8b6f9626d119d"),
+    # prefill_bf16_kernel (paged), 8 rows x 1024 queries over 8192 keys, full-size capture
+    "prefill_paged": (465.07e6, "54c8b6f9626d119d"),
+    # decode_split_kernel: a 16-row capture (303.7 MB for 299.5 MB algorithmic) scaled by
+    # the KV bytes to the 66-row batch
     "decode": (2.1496e9, "c43dc21389d4e5ce"),
-    # merge_pair: full-size capture; reads are the compulsory 136.3 MB, writes 38.2 MB of the
-    # 68.2 MB output (the rest still in L2 at exit) (profiles/merge_pair_262144x128.md)
+    # merge_pair_kernel, 262144 rows x 128 bf16, full-size capture: reads are the compulsory
+    # 136.3 MB, writes 38.2 MB of the 68.2 MB output (the rest still in L2 at exit)
     "merge_pair": (174.55e6, "054155b75fe86019"),
 }
 
@@ -170,6 +172,72 @@ class ClockSampler:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
                 "samples": len(sm)}
+
+
+class NvmlClockSampler:
+    """SM clock, power and clock-event reasons of this process's GPU, read
+    through NVML (read-only queries) every ``period_s`` on a background thread
+    while the timed region runs. NVML identifies the GPU by its UUID."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown"}
+
+    def __init__(self, dev, period_s: float = 0.002):
+        import ctypes
+        import threading
+
+        self.period = period_s
+        self.samples = []
+        self._stop = threading.Event()
+        self._thread = None
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.lib, self.ct = lib, ctypes
+        self.h = ctypes.c_void_p()
+        uuid = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
+        if uuid is None or lib.nvmlDeviceGetHandleByUUID(f"GPU-{uuid}".encode(),
+                                                         ctypes.byref(self.h)) != 0:
+            raise OSError("no NVML handle for this GPU")
+        mx = ctypes.c_uint()
+        lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx))  # 1 = SM clock
+        self.max_mhz = float(mx.value)
+        self._reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def _loop(self):
+        ct, lib = self.ct, self.lib
+        c, r, pw = ct.c_uint(), ct.c_ulonglong(), ct.c_uint()
+        while not self._stop.is_set():
+            if lib.nvmlDeviceGetClockInfo(self.h, 1, ct.byref(c)) == 0:
+                self._reasons(self.h, ct.byref(r))
+                lib.nvmlDeviceGetPowerUsage(self.h, ct.byref(pw))
+                self.samples.append((float(c.value), int(r.value), pw.value / 1000.0))
+            self._stop.wait(self.period)
+
+    def start(self):
+        import threading
+
+        self._thread = threading.Thread(target=self._loop, daemon=True)
+        self._thread.start()
+
+    def stop(self):
+        self._stop.set()
+        if self._thread is not None:
+            self._thread.join(timeout=5)
+        if not self.samples:
+            return None
+        reasons = sorted({name for _, r, _ in self.samples for bit, name in self.REASONS.items()
+                          if r & bit})
+        return {"sm_mhz": statistics.median(c for c, _, _ in self.samples),
+                "sm_max_mhz": self.max_mhz, "reasons": reasons, "samples": len(self.samples),
+                "power_w_max": max(p for _, _, p in self.samples), "via": "nvml"}
+
+
+def make_clock_sampler(dev, local, out_dir):
+    try:
+        return NvmlClockSampler(dev)
+    except (OSError, AttributeError):
+        return ClockSampler(local, out_dir)
 
 
 def dist_setup():
@@ -342,7 +410,7 @@ def run_gpu(args, world, rank, local):
     if attn.attn_get_device_error() != 0:
         raise RuntimeError("device error during warm-up")
 
-    clocks = ClockSampler(local, args.clocks_dir)
+    clocks = make_clock_sampler(dev, local, args.clocks_dir)
     clocks.start()
     barrier(world)
     torch.cuda.synchronize()
@@ -486,6 +554,7 @@ def run_gpu(args, world, rank, local):
     # ---- CPU oracle baseline (rank 0, N = 1 only) ----
     cpu = None
     dec_cpu = None
+    cpu_rows_n = 0
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         torch.set_num_threads(cpu_cores())
         qc, kc_, vc_ = q.cpu(), k.cpu(), v.cpu()
@@ -495,6 +564,7 @@ def run_gpu(args, world, rank, local):
             t_tot += dt
             f_tot += fl
             n += 1
+        cpu_rows_n = n
         cpu = {"value": f_tot / t_tot / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
                "sample": f"{n} x 64 causal query rows of one head at T=8192 (float64 materialised softmax)"}
         order = np.argsort(lens)
@@ -511,53 +581,75 @@ def run_gpu(args, world, rank, local):
 
     if rank != 0:
         return
+    detail = {
+        "prefill": {"ms": pre_avg, "flops": pf, "T": PREFILL.T, "h": PREFILL.h, "h_kv": PREFILL.h_kv,
+                    "d_h": PREFILL.d_h, "causal": True, "e2e": e2e, "cpu_baseline": cpu},
+        "decode": {"value": dec_value, "unit": "GB/s", "ms": dec_avg, "B": B, "num_splits": S,
+                   "kv_tokens": sum(lens), "bytes": db, "traffic": traffic_for("decode"),
+                   "e2e": dec_e2e, "cpu_baseline": dec_cpu, "deterministic": det,
+                   "adaptive": adaptive},
+        "merge_pair": merge_pair, "decode_batch1": decode_b1, "prefill_T2048": prefill_2048,
+        "prefill_paged": prefill_paged, "clocks": clk,
+    }
+    # The full record goes to stderr; stdout carries one short line.
+    print("bench detail: " + json.dumps(detail), file=sys.stderr, flush=True)
+
+    def g4(x):
+        return None if x is None else float(f"{x:.4g}")
+
+    extras = {"decode_ms": g4(dec_avg)}
+    if dec_e2e:
+        extras["decode_e2e_gbs"] = g4(dec_e2e["value"])
+    if det:
+        extras["det_gbs"] = g4(det["value"])
+    if adaptive:
+        extras["adaptive_gbs"] = g4(adaptive["value"])
+    if prefill_2048:
+        extras["t2048_tflops"] = g4(prefill_2048["value"])
+        extras["t2048_frac"] = g4(prefill_2048["roofline"]["frac"])
+    if prefill_paged:
+        extras["paged_prefill_tflops"] = g4(prefill_paged["value"])
+        extras["paged_prefill_frac"] = g4(prefill_paged["roofline"]["frac"])
+    if merge_pair:
+        extras["merge_pair_gbs"] = g4(merge_pair["value"])
+    if decode_b1:
+        for key, short in ((W.DECODE_S32K.name, "b1_h32"), (W.DECODE_70B_TP8.name, "b1_70b_tp8")):
+            if key in decode_b1:
+                extras[f"{short}_us"] = g4(decode_b1[key]["us_per_call"])
+                extras[f"{short}_frac"] = g4(decode_b1[key]["frac_of_hbm"])
     line = {
         "metric": METRIC,
-        "value": value,
+        "value": g4(value),
         "unit": "TFLOP/s",
+        "decode_gbs": g4(dec_value),
+        "decode_frac": g4(dec_achieved / hbm_peak),
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": step_ms,
+        "ms_per_step": g4(step_ms),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
         "config": {
-            "workload": "causal GQA prefill T=8192 (h=32, h_kv=8, d_h=128, Q,K x3) + paged split-KV "
-                        "decode (64 rows U[1,16384] + 2 empty, 16-token pages)",
-            "prefill": {"h": PREFILL.h, "h_kv": PREFILL.h_kv, "d_h": PREFILL.d_h, "T": PREFILL.T,
-                        "causal": True, "flops": pf},
-            "decode": {"B": B, "h": DECODE.h, "h_kv": DECODE.h_kv, "d_h": DECODE.d_h, "page": 16,
-                       "num_splits": S, "kv_tokens": sum(lens), "bytes": db},
-            "l2": "flushed (512 MiB write) before each prefill; decode cache 2.15 GB > L2",
+            "workload": "causal GQA prefill T8192 h32 kv8 d128 + paged decode 66 rows",
+            "decode_splits": S,
+            "l2": "flush 512MiB; decode KV 2.1GB>L2",
             "parallelism": f"replicas x{world}",
         },
-        "roofline": {"bound": "tensor", "achieved": pre_achieved, "peak": tc_peak, "unit": "TFLOP/s",
-                     "frac": pre_achieved / tc_peak, "traffic": traffic_for("prefill"),
-                     "kernel": "prefill_bf16_kernel", "peak_source": f"{peak_kind} bf16 burst"},
-        "decode": {
-            "value": dec_value, "unit": "GB/s", "ms": dec_avg,
-            "roofline": {"bound": "hbm", "achieved": dec_achieved, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": dec_achieved / hbm_peak, "traffic": traffic_for("decode"),
-                         "kernel": "decode_split_kernel + merge_states_kernel",
-                         "peak_source": f"{peak_kind} copy bandwidth"},
-            "e2e": dec_e2e,
-            "cpu_baseline": dec_cpu,
-            "deterministic": det,
-            "adaptive": adaptive,
-        },
-        "merge_pair": merge_pair,
-        "decode_batch1": decode_b1,
-        "prefill_T2048": prefill_2048,
-        "prefill_paged": prefill_paged,
-        "prefill_ms": pre_avg,
-        "e2e": e2e,
-        "cpu_baseline": cpu,
+        "roofline": {"bound": "tensor", "achieved": g4(pre_achieved), "peak": tc_peak, "unit": "TFLOP/s",
+                     "frac": g4(pre_achieved / tc_peak), "traffic": traffic_for("prefill")},
+        "e2e": None if e2e is None else {k: (g4(v) if isinstance(v, float) else v)
+                                         for k, v in e2e.items() if k != "ms"},
+        "cpu_baseline": None if cpu is None else {
+            "value": g4(cpu["value"]), "unit": cpu["unit"], "cores": cpu["cores"], "kind": "oracle",
+            "sample": f"{cpu_rows_n}x64 rows of one T8192 head"},
         # prefill: V-to-fp16 pass + attention kernel; decode: split kernel + merge
         "gpu_launches": (2 * int(do_pre) + 2 * int(do_dec)) * args.steps,
-        "clocks": clk,
+        "clocks": None if clk is None else {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"],
+                                            "reasons": clk["reasons"], "samples": clk["samples"]},
+        "x": extras,
     }
     print(json.dumps(line), flush=True)
 
