@@ -497,6 +497,22 @@ attn_status_t attn_get_last_device_error(void* stream);
  */
 attn_status_t attn_selftest_wait_timeout(unsigned int limit_us, void* stream);
 
+/*
+ * attn_selftest_delayed_copy -- test aid for the decode kernels' reads before
+ * their dependency wait. The split-KV decode kernel reads seq_lens and the
+ * block table before it waits for the previous kernel on its stream (to warm
+ * L2 with its first pages), and again after the wait for the values it
+ * uses. A stale early read only happens when the kernel before it lets it
+ * start early and then writes those arrays; this call is such a kernel: one
+ * CTA that lets the next kernel on `stream` start at once, waits delay_us
+ * microseconds (a bounded spin), then copies n int32 from src to dst (device
+ * pointers). n == 0 is a no-op. Errors: INVALID_ARG for n < 0, delay_us >
+ * 1000, NULL or misaligned pointers with n > 0; ATTN_ERR_CUDA if the launch
+ * fails.
+ */
+attn_status_t attn_selftest_delayed_copy(int32_t* dst, const int32_t* src, int n,
+                                         unsigned int delay_us, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

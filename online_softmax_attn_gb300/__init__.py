@@ -96,6 +96,8 @@ def library() -> ctypes.CDLL:
     lib.attn_merge_states.restype = I
     lib.attn_merge_lse_pair.argtypes = [P, P, P, P, I, I, I, P, P, I, P]
     lib.attn_merge_lse_pair.restype = I
+    lib.attn_selftest_delayed_copy.argtypes = [P, P, I, ctypes.c_uint, P]
+    lib.attn_selftest_delayed_copy.restype = I
     lib.attn_get_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint)]
     lib.attn_get_device_error.restype = I
     lib.attn_get_last_device_error.argtypes = [P]
@@ -484,6 +486,16 @@ def attn_selftest_wait_timeout(limit_us: int = 1000, stream=None) -> None:
     barrier) after ``limit_us`` microseconds: it raises the wait-timeout bit
     of the device error word and returns. For failure-detection tests."""
     _check("attn_selftest_wait_timeout", library().attn_selftest_wait_timeout(int(limit_us), _stream(stream)))
+
+
+def attn_selftest_delayed_copy(dst, src, delay_us: int = 20, stream=None) -> None:
+    """Test aid: let the next kernel on the stream start at once, then after
+    delay_us copy src into dst (int32 CUDA tensors of the same size)."""
+    _need(dst.is_cuda and src.is_cuda and dst.dtype == src.dtype == torch.int32, "int32 CUDA tensors")
+    _need(dst.is_contiguous() and src.is_contiguous() and dst.numel() == src.numel(), "same-size contiguous")
+    _check("attn_selftest_delayed_copy",
+           library().attn_selftest_delayed_copy(_ptr(dst), _ptr(src), dst.numel(), int(delay_us),
+                                                _stream(stream)))
 
 
 def attn_get_device_error(stream=None) -> int:

@@ -368,6 +368,16 @@ attn_status_t attn_selftest_wait_timeout(unsigned int limit_us, void* stream) {
                                                 static_cast<cudaStream_t>(stream)));
 }
 
+attn_status_t attn_selftest_delayed_copy(int32_t* dst, const int32_t* src, int n,
+                                         unsigned int delay_us, void* stream) {
+  if (n < 0 || delay_us > 1000 || (n > 0 && (!dst || !src)) || !aligned(dst, 4) ||
+      !aligned(src, 4))
+    return ATTN_ERR_INVALID_ARG;
+  if (n == 0) return ATTN_OK;
+  return from_cuda(launch_delayed_copy(dst, src, n, uint64_t(delay_us) * 1000ull,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
 attn_status_t attn_get_device_error(void* stream, unsigned int* bits) {
   if (bits == nullptr) return ATTN_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

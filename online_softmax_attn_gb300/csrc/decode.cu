@@ -130,26 +130,29 @@ __global__ void __launch_bounds__(NW * 32, 1)
   // TMA prefetch lands nothing in this SM). The seq_len, split plan and table
   // entries read here only steer the prefetch: were an earlier kernel still
   // writing them, some other page would be warmed, and the loads after the
-  // wait read the right ones (L2 is the point of coherence). Only the first
-  // wave of CTAs (one per SM) can start before the previous kernel ends; the
-  // later ones would only request their first pages twice.
+  // wait read the right ones (L2 is the point of coherence). Every read of
+  // seq_lens, the split plan and the table in this kernel goes to L2
+  // (ld.global.cg): a line cached in L1 by an early read would otherwise
+  // serve a later one the old value. Only the first wave of CTAs (one per
+  // SM) can start before the previous kernel ends; the later ones would only
+  // request their first pages twice.
   uint32_t n_sm;
   asm("mov.u32 %0, %%nsmid;" : "=r"(n_sm));
   const uint32_t cta = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
   if (lane == 0 && cta < n_sm) {
-    const int sl = min(max(seq_lens[b], 0), max_blocks * kPage);
+    const int sl = min(max(__ldcg(seq_lens + b), 0), max_blocks * kPage);
     const int np = (sl + kPage - 1) / kPage;  // 0 .. max_blocks
     // Pages per split as the plan takes them. A value read this early may be
     // anything (the plan kernel may not have written it yet), so it is
     // bounded before use and every table index stays in [0, np).
-    const int fp = pps_dev ? *pps_dev : fixed_pps;
+    const int fp = pps_dev ? __ldcg(pps_dev) : fixed_pps;
     const int pps0 = fp > 0 ? min(fp, max(np, 1)) : (np + num_splits - 1) / num_splits;
     if (pps0 >= 1 && static_cast<long long>(split) * pps0 < np) {
       const int lo = split * pps0, hi = min(lo + pps0, np);
       for (int i = 0; i < NST; ++i) {
         const int p = lo + warp + NW * i;
         if (p >= hi) break;
-        const int phys = block_table[size_t(b) * max_blocks + p];
+        const int phys = __ldcg(block_table + size_t(b) * max_blocks + p);
         if (phys < 0 || phys >= num_blocks) continue;
 #pragma unroll
         for (int hf = 0; hf < D / 64; ++hf) {
@@ -176,10 +179,10 @@ __global__ void __launch_bounds__(NW * 32, 1)
     }
   }
 
-  const int seq_len = clamp_seq_len(seq_lens[b], max_blocks * kPage, &g_decode_err);
+  const int seq_len = clamp_seq_len(__ldcg(seq_lens + b), max_blocks * kPage, &g_decode_err);
   int pps = 0;
   const int n_act =
-      split_plan_fixed(seq_len, kPage, num_splits, pps_dev ? *pps_dev : fixed_pps, &pps);
+      split_plan_fixed(seq_len, kPage, num_splits, pps_dev ? __ldcg(pps_dev) : fixed_pps, &pps);
   if (split >= n_act) return;  // surplus split of a short (or empty) row
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -210,7 +213,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
 
   // Block-table entries for this warp's pages, 32 at a time (lane i holds
   // local page 32*chunk + i).
-  int bt_reg = lane < nloc ? bt_row[p_begin + warp + NW * lane] : -1;
+  int bt_reg = lane < nloc ? __ldcg(bt_row + p_begin + warp + NW * lane) : -1;
 
   auto issue = [&](int i, int phys) {
     const int st = i % NST;
@@ -338,7 +341,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
     const int inext = i + NST;
     if (inext < nloc) {
       if ((inext & 31) == 0)
-        bt_reg = (inext + lane < nloc) ? bt_row[p_begin + warp + NW * (inext + lane)] : -1;
+        bt_reg = (inext + lane < nloc) ? __ldcg(bt_row + p_begin + warp + NW * (inext + lane)) : -1;
       const int phys = __shfl_sync(0xffffffffu, bt_reg, inext & 31);
       if (lane == 0) {
         fence_proxy_async_smem();
@@ -495,6 +498,28 @@ __global__ void wait_timeout_selftest_kernel(uint64_t limit_ns) {
 
 cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, cudaStream_t stream) {
   wait_timeout_selftest_kernel<<<1, 1, 0, stream>>>(limit_ns);
+  return cudaGetLastError();
+}
+
+// Self-test of the reads before the dependency wait: the next kernel on the
+// stream (a programmatic dependent) may start at once, and after delay_ns this
+// grid copies n int32 from src to dst, so that the next kernel's reads before
+// its dependency wait see the old values. The delay is a bounded spin.
+__global__ void delayed_copy_kernel(int32_t* __restrict__ dst, const int32_t* __restrict__ src,
+                                    int n, uint64_t delay_ns) {
+  pdl_trigger();
+  if (threadIdx.x == 0) {
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < delay_ns) {
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += blockDim.x) dst[i] = src[i];
+}
+
+cudaError_t launch_delayed_copy(int32_t* dst, const int32_t* src, int n, uint64_t delay_ns,
+                                cudaStream_t stream) {
+  delayed_copy_kernel<<<1, 256, 0, stream>>>(dst, src, n, delay_ns);
   return cudaGetLastError();
 }
 

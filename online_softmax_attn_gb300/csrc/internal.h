@@ -65,6 +65,9 @@ cudaError_t launch_decode_plan(const int32_t* seq_lens, int B, int h_kv, int max
 cudaError_t launch_decode_split(const DecodeArgs& a, cudaStream_t stream);
 unsigned int decode_read_and_clear_error(cudaStream_t stream, cudaError_t* st);
 cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, cudaStream_t stream);
+// One CTA: lets the next kernel start, waits delay_ns, copies n int32.
+cudaError_t launch_delayed_copy(int32_t* dst, const int32_t* src, int n, uint64_t delay_ns,
+                                cudaStream_t stream);
 
 // prefill_simt.cu ----------------------------------------------------------
 cudaError_t launch_prefill_f32(const float* q, const float* k, const float* v, float* o,
