@@ -364,6 +364,12 @@ def run_gpu(args, world, rank, local):
         if rank == 0:
             print(json.dumps({"only": "decode_batch1", "decode_batch1": res}), flush=True)
         return
+    if args.only == "mixed":
+        flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+        res = measure_mixed(dev, flush, hbm_peak, tc_peak, peak_kind)
+        if rank == 0:
+            print(json.dumps({"only": "mixed", "mixed": res}), flush=True)
+        return
     if args.only == "merge_pair":
         # The pairwise merge measurement alone (profiler captures).
         flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
@@ -440,6 +446,15 @@ def run_gpu(args, world, rank, local):
     dec_value = world * db / (dec_avg * 1e-3) / 1e9
     pre_achieved = pf / (pre_avg * 1e-3) / 1e12
     dec_achieved = db / (dec_avg * 1e-3) / 1e9
+
+    if args.only in ("prefill", "decode"):
+        # One half of the step alone (profiler captures): not a bench line.
+        if rank == 0:
+            half = ({"prefill_tflops": value, "prefill_ms": pre_avg} if args.only == "prefill" else
+                    {"decode_gbs": dec_value, "decode_ms": dec_avg, "decode_frac": dec_achieved / hbm_peak,
+                     "rows": B, "num_splits": S})
+            print(json.dumps({"only": args.only, **half}), flush=True)
+        return
 
     # ---- end to end through the public API, host buffers ----
     e2e = None
@@ -550,6 +565,7 @@ def run_gpu(args, world, rank, local):
     decode_b1 = measure_decode_batch1(dev, hbm_peak, peak_kind) if extras else None
     prefill_2048 = measure_prefill_t2048(dev, flush, tc_peak, peak_kind) if extras else None
     prefill_paged = measure_prefill_paged(dev, flush, tc_peak, peak_kind) if extras else None
+    mixed = measure_mixed(dev, flush, hbm_peak, tc_peak, peak_kind) if extras else None
 
     # ---- CPU oracle baseline (rank 0, N = 1 only) ----
     cpu = None
@@ -589,7 +605,7 @@ def run_gpu(args, world, rank, local):
                    "e2e": dec_e2e, "cpu_baseline": dec_cpu, "deterministic": det,
                    "adaptive": adaptive},
         "merge_pair": merge_pair, "decode_batch1": decode_b1, "prefill_T2048": prefill_2048,
-        "prefill_paged": prefill_paged, "clocks": clk,
+        "prefill_paged": prefill_paged, "mixed": mixed, "clocks": clk,
     }
     # The full record goes to stderr; stdout carries one short line.
     print("bench detail: " + json.dumps(detail), file=sys.stderr, flush=True)
@@ -612,6 +628,10 @@ def run_gpu(args, world, rank, local):
         extras["paged_prefill_frac"] = g4(prefill_paged["roofline"]["frac"])
     if merge_pair:
         extras["merge_pair_gbs"] = g4(merge_pair["value"])
+    if mixed:
+        extras["mixed_prefill_tflops"] = g4(mixed["prefill_tflops"])
+        extras["mixed_decode_gbs"] = g4(mixed["decode_rows_gbs"])
+        extras["mixed_decode_alone_gbs"] = g4(mixed["decode_alone_gbs"])
     if decode_b1:
         for key, short in ((W.DECODE_S32K.name, "b1_h32"), (W.DECODE_70B_TP8.name, "b1_70b_tp8")):
             if key in decode_b1:
@@ -699,6 +719,83 @@ def measure_prefill_paged(dev, flush, tc_peak, peak_kind, iters=10):
                          "frac": tf / tc_peak, "traffic": traffic_for("prefill_paged"),
                          "kernel": "prefill_bf16_kernel (paged)",
                          "peak_source": f"{peak_kind} bf16 burst"}}
+
+
+def measure_mixed(dev, flush, hbm_peak, tc_peak, peak_kind, iters=10):
+    """A mixed serving step through attn_prefill_paged: 4 chunked-prefill rows
+    (the last 1024 of 8192 positions each, causal) and 64 decode rows over
+    seeded lengths U[4096, 16384], h=32, h_kv=8, d_h=128, bf16, the decode
+    rows routed to the split-KV decode (at most 32 splits). Timed with events
+    after an L2 flush: the mixed call, the 4 prefill rows alone, and
+    attn_decode_paged on the 64 decode rows alone. The decode rows' GB/s is
+    their KV bytes over (mixed - prefill alone)."""
+    import online_softmax_attn_gb300 as attn
+
+    h, h_kv, d, P = PREFILL.h, PREFILL.h_kv, PREFILL.d_h, W.PAGE_SIZE
+    n_pre, qn, ctx = 4, 1024, PREFILL.T
+    g = torch.Generator().manual_seed(41)
+    dec_lens = torch.randint(4096, 16385, (64,), generator=g).tolist()
+    lens = [ctx] * n_pre + dec_lens
+    q_lens = [qn] * n_pre + [1] * 64
+    table, nblk = W.paged_layout(lens, seed=43)
+    kc = W.normal((nblk, P, h_kv, d), 44, torch.bfloat16, dev)
+    vc = W.normal((nblk, P, h_kv, d), 45, torch.bfloat16, dev)
+    total_q = sum(q_lens)
+    q = W.normal((total_q, h, d), 46, torch.bfloat16, dev)
+    cu = torch.tensor([0] + list(np.cumsum(q_lens)), dtype=torch.int32, device=dev)
+    seq = torch.tensor(lens, dtype=torch.int32, device=dev)
+    table = table.to(dev)
+    B, mb = len(lens), table.shape[1]
+    o = torch.empty_like(q)
+    lse = torch.empty((total_q, h), dtype=torch.float32, device=dev)
+    dsplit = 32
+    ws = torch.empty(attn.attn_prefill_paged_decode_workspace_bytes(B, h, d, dsplit) +
+                     attn.attn_prefill_paged_workspace_bytes(B, mb, h_kv, d, v16=True),
+                     dtype=torch.uint8, device=dev)
+    # the prefill rows alone
+    pq = q[:n_pre * qn]
+    po, pl = torch.empty_like(pq), torch.empty((n_pre * qn, h), dtype=torch.float32, device=dev)
+    pws = torch.empty(attn.attn_prefill_paged_workspace_bytes(n_pre, mb, h_kv, d, v16=True),
+                      dtype=torch.uint8, device=dev)
+    pcu, pseq, ptab = cu[:n_pre + 1].contiguous(), seq[:n_pre].contiguous(), table[:n_pre].contiguous()
+    # the decode rows alone
+    dq = q[n_pre * qn:].contiguous()
+    dseq, dtab = seq[n_pre:].contiguous(), table[n_pre:].contiguous()
+    S = attn.attn_recommended_splits(64, h_kv, max(dec_lens), sum(dec_lens))
+    dws = torch.empty(attn.attn_decode_workspace_bytes(64, h, d, S), dtype=torch.uint8, device=dev)
+    do, dl = torch.empty_like(dq), torch.empty((64, h), dtype=torch.float32, device=dev)
+    calls = {
+        "mixed": lambda: attn.attn_prefill_paged(q, kc, vc, table, cu, seq, qn, True, PREFILL.scale,
+                                                 workspace=ws, o=o, lse=lse, decode_splits=dsplit),
+        "prefill": lambda: attn.attn_prefill_paged(pq, kc, vc, ptab, pcu, pseq, qn, True, PREFILL.scale,
+                                                   workspace=pws, o=po, lse=pl),
+        "decode": lambda: attn.attn_decode_paged(dq, kc, vc, dtab, dseq, S, PREFILL.scale,
+                                                 workspace=dws, o=do, lse=dl),
+    }
+    t = {}
+    for name, fn in calls.items():
+        for _ in range(3):
+            fn()
+        ms = []
+        for _ in range(iters):
+            flush.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            ms.append(a.elapsed_time(b))
+        t[name] = statistics.median(ms)
+    pairs = n_pre * sum(ctx - qn + i + 1 for i in range(qn))
+    pf = 4.0 * h * d * pairs
+    db = decode_bytes(dec_lens, DECODE)
+    dec_ms = max(t["mixed"] - t["prefill"], 1e-6)
+    return {"ms": t["mixed"], "prefill_alone_ms": t["prefill"], "decode_alone_ms": t["decode"],
+            "prefill_tflops": pf / (t["prefill"] * 1e-3) / 1e12,
+            "decode_rows_gbs": db / (dec_ms * 1e-3) / 1e9,
+            "decode_alone_gbs": db / (t["decode"] * 1e-3) / 1e9, "decode_alone_splits": S,
+            "rows": {"prefill": f"{n_pre} x {qn} queries over {ctx} keys", "decode": "64 x U[4096, 16384]"},
+            "hbm_peak": hbm_peak, "tc_peak": tc_peak, "peak_source": peak_kind}
 
 
 def measure_prefill_t2048(dev, flush, tc_peak, peak_kind, iters=15):
@@ -897,7 +994,8 @@ def main():
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the measurements outside the step (deterministic / adaptive decode, "
                          "pair merge, paged prefill), e.g. for a launch list of the step alone")
-    ap.add_argument("--only", choices=["prefill", "decode", "prefill_paged", "merge_pair", "decode_batch1"],
+    ap.add_argument("--only", choices=["prefill", "decode", "prefill_paged", "merge_pair", "decode_batch1",
+                                       "mixed"],
                     default=None,
                     help="run one half of the step, or the paged prefill or pair merge measurement "
                          "alone (profiler captures; not a bench line)")

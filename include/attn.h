@@ -200,7 +200,16 @@ attn_status_t attn_prefill_host(const void* q, const void* k, const void* v, voi
  * (attn_prefill_paged_v16_workspace_bytes) a pre-pass copies the pages each
  * row uses into an fp16 buffer in the workspace, row by row, and a 128-key
  * tile that converts exactly takes an fp16 P against it (one MMA instead of
- * two); a tile holding |v| >= 2^16, inf or NaN keeps the bf16 path.
+ * two); a tile holding |v| >= 2^16, inf or NaN keeps the bf16 path (read
+ * from the copy too, where it is stored as bf16).
+ * Rows of one query (decode rows of a mixed batch): with decode_splits > 0
+ * they get no query tile; after the prefill kernel the call runs the
+ * split-KV decode of attn_decode_paged_adaptive over those rows alone
+ * ([DEC] "Where GQA enters": one query in a 128-row tile leaves the rest of
+ * the tile idle and the row's keys on one CTA), with at most decode_splits
+ * splits per row planned on the device from their lengths, and writes their
+ * outputs at token cu_seqlens_q[b]. With decode_splits == 0 they run as
+ * 1-row query tiles.
  *
  *   q            [total_q, h, d_h] bf16, rows packed back to back    (read)
  *   k_cache,
@@ -211,12 +220,17 @@ attn_status_t attn_prefill_host(const void* q, const void* k, const void* v, voi
  *   seq_lens     [B] int32, q_len_b <= seq_lens[b] <= max_blocks_per_seq *
  *                page_size                                              (read)
  *   max_q_len    host bound on every q_len_b (sizes the grid)
- *   workspace    at least attn_prefill_paged_workspace_bytes(B) bytes
- *                (per-row tile offsets); with at least
+ *   decode_splits 0, or the most splits a decode row may take
+ *                (1 .. ATTN_MAX_SPLITS); see above
+ *   workspace    256-byte aligned device memory, overwritten by the call:
+ *                first attn_prefill_paged_decode_workspace_bytes(B, h, d_h,
+ *                decode_splits) bytes (0 when decode_splits is 0) for the
+ *                decode rows, then the prefill's own part: at least
+ *                attn_prefill_paged_workspace_bytes(B) bytes (per-row tile
+ *                offsets), or, for the fp16 V form, at least
  *                attn_prefill_paged_v16_workspace_bytes(B,
- *                max_blocks_per_seq, h_kv, d_h) bytes (when that is nonzero)
- *                the fp16 V form is used. 256-byte aligned, device memory,
- *                overwritten by the call
+ *                max_blocks_per_seq, h_kv, d_h) bytes (when that is nonzero;
+ *                the form is chosen by the size given)
  *   o            [total_q, h, d_h] bf16                                 (written)
  *   lse          [total_q, h] fp32, natural log, may be NULL             (written)
  * All tensor arguments are device pointers. Device-side problems set bits in
@@ -229,10 +243,12 @@ attn_status_t attn_prefill_host(const void* q, const void* k, const void* v, voi
  * Errors: INVALID_ARG for NULL or misaligned pointers (16 bytes for q, the
  * caches and o; 4 for the int32 arrays and lse), B < 0, total_q < 0,
  * max_q_len < 1 with total_q > 0, h < 1, h > 65535, h % h_kv != 0,
- * num_blocks < 1, max_blocks_per_seq < 1, scale not finite and > 0, a small
- * workspace; UNSUPPORTED for d_h other than 64 / 128, page_size != 16, or
- * more than 65535 query tiles in the launch (min(ceil(total_q / 128) + B,
- * B * ceil(max_q_len / 128))). B == 0 or total_q == 0 is a no-op.
+ * num_blocks < 1, max_blocks_per_seq < 1, scale not finite and > 0,
+ * decode_splits outside [0, ATTN_MAX_SPLITS], a small workspace;
+ * UNSUPPORTED for d_h other than 64 / 128, page_size != 16, g = h / h_kv
+ * not in {1, 2, 4, 8} with decode_splits > 0, or more than 65535 query
+ * tiles in the launch (min(ceil(total_q / 128) + B, B * ceil(max_q_len /
+ * 128))). B == 0 or total_q == 0 is a no-op.
  */
 size_t attn_prefill_paged_workspace_bytes(int B);
 /*
@@ -247,12 +263,21 @@ size_t attn_prefill_paged_workspace_bytes(int B);
  * copy's token index must fit int32); the small workspace then still works.
  */
 size_t attn_prefill_paged_v16_workspace_bytes(int B, int max_blocks_per_seq, int h_kv, int d_h);
+/*
+ * attn_prefill_paged_decode_workspace_bytes -- bytes at the front of
+ * attn_prefill_paged's workspace for its decode rows: split partials
+ * (attn_decode_workspace_bytes(B, h, d_h, decode_splits)) and 256 bytes for
+ * the device split plan. 0 when decode_splits is 0, and on invalid arguments.
+ * Host-only, pure.
+ */
+size_t attn_prefill_paged_decode_workspace_bytes(int B, int h, int d_h, int decode_splits);
 attn_status_t attn_prefill_paged(const void* q, const void* k_cache, const void* v_cache,
                                  const int32_t* block_table, const int32_t* cu_seqlens_q,
                                  const int32_t* seq_lens, int B, int total_q, int h, int h_kv,
                                  int d_h, int page_size, int num_blocks, int max_blocks_per_seq,
-                                 int max_q_len, int causal, float scale, void* workspace,
-                                 size_t workspace_bytes, void* o, float* lse, void* stream);
+                                 int max_q_len, int causal, float scale, int decode_splits,
+                                 void* workspace, size_t workspace_bytes, void* o, float* lse,
+                                 void* stream);
 
 /*
  * attn_decode_split_plan -- how one row's keys are cut into splits.

@@ -75,7 +75,10 @@ def library() -> ctypes.CDLL:
     lib.attn_prefill_paged_workspace_bytes.restype = S
     lib.attn_prefill_paged_v16_workspace_bytes.argtypes = [I, I, I, I]
     lib.attn_prefill_paged_v16_workspace_bytes.restype = S
-    lib.attn_prefill_paged.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, F, P, S, P, P, P]
+    lib.attn_prefill_paged_decode_workspace_bytes.argtypes = [I, I, I, I]
+    lib.attn_prefill_paged_decode_workspace_bytes.restype = S
+    lib.attn_prefill_paged.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, F, I, P, S, P, P,
+                                       P]
     lib.attn_prefill_paged.restype = I
     lib.attn_decode_split_plan.argtypes = [I, I, I, ctypes.POINTER(I)]
     lib.attn_decode_split_plan.restype = I
@@ -258,15 +261,24 @@ def attn_prefill_paged_workspace_bytes(B: int, max_blocks: int = 0, h_kv: int = 
     return int(library().attn_prefill_paged_workspace_bytes(B))
 
 
+def attn_prefill_paged_decode_workspace_bytes(B: int, h: int, d_h: int, decode_splits: int) -> int:
+    """Bytes at the front of attn_prefill_paged's workspace for its decode rows."""
+    return int(library().attn_prefill_paged_decode_workspace_bytes(B, h, d_h, decode_splits))
+
+
 def attn_prefill_paged(q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens, max_q_len: int,
                        causal: bool = True, scale: float | None = None, workspace="auto", o=None,
-                       lse=None, return_lse: bool = True, stream=None):
+                       lse=None, return_lse: bool = True, stream=None, decode_splits=None):
     """Variable-length query rows over a paged cache. q [total_q, h, d] bf16
     (rows packed back to back), caches [num_blocks, 16, h_kv, d] bf16,
     block_table [B, max_blocks] int32, cu_seqlens_q [B+1] int32, seq_lens [B]
     int32 (all CUDA). Row b's queries are its last q_len_b key positions.
+    ``decode_splits``: rows of one query go to the split-KV decode with at
+    most this many splits (0: they run as 1-row query tiles); None means 32
+    when the workspace is allocated here and 0 for a caller's workspace.
     ``workspace``: "auto" allocates the fp16-V form when it is available,
-    None the small form (all V tiles bf16), or a caller's uint8 CUDA tensor.
+    None the small form (all V tiles bf16), or a caller's uint8 CUDA tensor
+    (the decode part first, then the prefill's).
     Returns (o [total_q, h, d] bf16, lse [total_q, h] fp32 or None)."""
     for t in (q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens):
         _need(t.is_cuda and t.is_contiguous(), "tensors must be contiguous CUDA tensors")
@@ -280,14 +292,17 @@ def attn_prefill_paged(q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens,
     _need(cu_seqlens_q.shape == (B + 1,) and block_table.dim() == 2 and block_table.shape[0] == B,
           "cu_seqlens_q [B+1], block_table [B, max_blocks] and seq_lens [B] expected")
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if decode_splits is None:
+        decode_splits = 0 if isinstance(workspace, torch.Tensor) else 32
+    dec = attn_prefill_paged_decode_workspace_bytes(B, h, d, decode_splits)
     if isinstance(workspace, str):
         _need(workspace == "auto", 'workspace must be "auto", None or a tensor')
         n = attn_prefill_paged_workspace_bytes(B, block_table.shape[1], h_kv, d, v16=True)
         if n == 0:
             n = attn_prefill_paged_workspace_bytes(B)
-        workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=q.device)
+        workspace = torch.empty(max(dec + n, 256), dtype=torch.uint8, device=q.device)
     elif workspace is None:
-        workspace = torch.empty(max(attn_prefill_paged_workspace_bytes(B), 256),
+        workspace = torch.empty(max(dec + attn_prefill_paged_workspace_bytes(B), 256),
                                 dtype=torch.uint8, device=q.device)
     if o is None:
         o = torch.empty_like(q)
@@ -296,8 +311,8 @@ def attn_prefill_paged(q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens,
     st = library().attn_prefill_paged(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(cu_seqlens_q), _ptr(seq_lens),
         B, total_q, h, h_kv, d, page, nb, block_table.shape[1], int(max_q_len), int(bool(causal)),
-        scale, _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(o), _ptr(lse),
-        _stream(stream))
+        scale, int(decode_splits), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(o), _ptr(lse), _stream(stream))
     _check("attn_prefill_paged", st)
     return o, lse
 

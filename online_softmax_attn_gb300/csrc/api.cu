@@ -146,6 +146,7 @@ attn_status_t decode_paged_impl(const void* q, const void* k_cache, const void* 
       !aligned(workspace, 256))
     return ATTN_ERR_INVALID_ARG;
   const long long rows = static_cast<long long>(B) * h;
+  if (rows > 0x7fffffffll) return ATTN_ERR_INVALID_ARG;  // rows index an int grid
   const PartialLayout L = partial_layout(rows, num_splits, d_h);
   if (workspace_bytes < L.total + (adaptive ? 256u : 0u)) return ATTN_ERR_INVALID_ARG;
 
@@ -178,8 +179,8 @@ attn_status_t decode_paged_impl(const void* q, const void* k_cache, const void* 
     e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess)
-      e = launch_decode_plan(seq_lens, B, h_kv, max_blocks_per_seq * page_size, sms, num_splits,
-                             pps_dev, s);
+      e = launch_decode_plan(seq_lens, nullptr, B, h_kv, max_blocks_per_seq * page_size, sms,
+                             num_splits, pps_dev, s);
     if (e != cudaSuccess) return ATTN_ERR_CUDA;
   }
   e = launch_decode_split(a, s);
@@ -223,16 +224,30 @@ size_t attn_prefill_paged_v16_workspace_bytes(int B, int max_blocks_per_seq, int
   return paged_v16_layout(B, max_blocks_per_seq, h_kv, d_h).total;
 }
 
+size_t attn_prefill_paged_decode_workspace_bytes(int B, int h, int d_h, int decode_splits) {
+  if (B < 0 || h < 1 || d_h < 1 || decode_splits < 0 || decode_splits > ATTN_MAX_SPLITS) return 0;
+  if (decode_splits == 0) return 0;
+  // The adaptive decode's partials, then 256 bytes for its device plan.
+  return partial_layout(static_cast<long long>(B) * h, decode_splits, d_h).total + 256;
+}
+
 attn_status_t attn_prefill_paged(const void* q, const void* k_cache, const void* v_cache,
                                  const int32_t* block_table, const int32_t* cu_seqlens_q,
                                  const int32_t* seq_lens, int B, int total_q, int h, int h_kv,
                                  int d_h, int page_size, int num_blocks, int max_blocks_per_seq,
-                                 int max_q_len, int causal, float scale, void* workspace,
-                                 size_t workspace_bytes, void* o, float* lse, void* stream) {
+                                 int max_q_len, int causal, float scale, int decode_splits,
+                                 void* workspace, size_t workspace_bytes, void* o, float* lse,
+                                 void* stream) {
   if (B < 0 || total_q < 0 || h < 1 || h > 65535 || h_kv < 1 || h % h_kv != 0 ||
-      num_blocks < 1 || max_blocks_per_seq < 1 || !std::isfinite(scale) || !(scale > 0.f))
+      num_blocks < 1 || max_blocks_per_seq < 1 || !std::isfinite(scale) || !(scale > 0.f) ||
+      decode_splits < 0 || decode_splits > ATTN_MAX_SPLITS)
     return ATTN_ERR_INVALID_ARG;
   if ((d_h != 64 && d_h != 128) || page_size != 16) return ATTN_ERR_UNSUPPORTED;
+  if (decode_splits > 0) {
+    const int g = h / h_kv;
+    if (g != 1 && g != 2 && g != 4 && g != 8) return ATTN_ERR_UNSUPPORTED;
+    if (B > 65535 || static_cast<long long>(B) * h > 0x7fffffffll) return ATTN_ERR_INVALID_ARG;
+  }
   if (static_cast<long long>(max_blocks_per_seq) * page_size > (1ll << 30))
     return ATTN_ERR_INVALID_ARG;
   if (B == 0 || total_q == 0) return ATTN_OK;
@@ -243,7 +258,14 @@ attn_status_t attn_prefill_paged(const void* q, const void* k_cache, const void*
       !aligned(block_table, 4) || !aligned(cu_seqlens_q, 4) || !aligned(seq_lens, 4) ||
       !aligned(lse, 4) || !aligned(workspace, 256))
     return ATTN_ERR_INVALID_ARG;
-  if (workspace_bytes < attn_prefill_paged_workspace_bytes(B)) return ATTN_ERR_INVALID_ARG;
+  // Workspace: the decode rows' partials first (decode_splits > 0), then the
+  // prefill's own layout, small or with the fp16 V copy.
+  const size_t dec_bytes = attn_prefill_paged_decode_workspace_bytes(B, h, d_h, decode_splits);
+  if (workspace_bytes < dec_bytes + attn_prefill_paged_workspace_bytes(B))
+    return ATTN_ERR_INVALID_ARG;
+  uint8_t* const dec_ws = static_cast<uint8_t*>(workspace);
+  workspace = dec_ws + dec_bytes;
+  workspace_bytes -= dec_bytes;
   PagedPrefill a;
   a.q = q;
   a.k_cache = k_cache;
@@ -271,8 +293,49 @@ attn_status_t attn_prefill_paged(const void* q, const void* k_cache, const void*
   a.scale = scale;
   a.o = o;
   a.lse = lse;
-  const cudaError_t e = launch_prefill_paged(a, static_cast<cudaStream_t>(stream));
+  a.decode_rows_apart = decode_splits > 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_prefill_paged(a, s);
   if (e == cudaErrorNotSupported) return ATTN_ERR_UNSUPPORTED;
+  if (e != cudaSuccess || decode_splits == 0) return from_cuda(e);
+  // Rows of one query: the split-KV decode ([DEC] "Where GQA enters": a
+  // single query row as one row of a 128-row tile wastes the rest; split the
+  // key axis instead), with its split count planned on the device from those
+  // rows' lengths under a grid of decode_splits, their queries and outputs at
+  // token cu_seqlens_q[b].
+  const PartialLayout PL = partial_layout(static_cast<long long>(B) * h, decode_splits, d_h);
+  int* pps_dev = reinterpret_cast<int*>(dec_ws + PL.total);
+  DecodeArgs da;
+  da.q = q;
+  da.k_cache = k_cache;
+  da.v_cache = v_cache;
+  da.block_table = block_table;
+  da.seq_lens = seq_lens;
+  da.B = B;
+  da.h = h;
+  da.h_kv = h_kv;
+  da.d_h = d_h;
+  da.page_size = page_size;
+  da.num_blocks = num_blocks;
+  da.max_blocks_per_seq = max_blocks_per_seq;
+  da.num_splits = decode_splits;
+  da.scale = scale;
+  da.pps_dev = pps_dev;
+  da.q_rows = cu_seqlens_q;
+  da.o_part = reinterpret_cast<float*>(dec_ws + PL.o_off);
+  da.m_part = reinterpret_cast<float*>(dec_ws + PL.m_off);
+  da.l_part = reinterpret_cast<float*>(dec_ws + PL.l_off);
+  int dev = 0, sms = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess)
+    e = launch_decode_plan(seq_lens, cu_seqlens_q, B, h_kv, max_blocks_per_seq * page_size, sms,
+                           decode_splits, pps_dev, s);
+  if (e == cudaSuccess) e = launch_decode_split(da, s);
+  if (e == cudaSuccess)
+    e = launch_merge(da.o_part, da.m_part, da.l_part, nullptr, seq_lens, h, page_size,
+                     max_blocks_per_seq * page_size, static_cast<int>(static_cast<long long>(B) * h),
+                     decode_splits, d_h, o, lse, ATTN_DTYPE_BF16, s, 0, pps_dev, cu_seqlens_q);
   return from_cuda(e);
 }
 

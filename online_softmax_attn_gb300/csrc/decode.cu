@@ -111,8 +111,9 @@ __global__ void __launch_bounds__(NW * 32, 1)
                         const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ block_table,
                         const int32_t* __restrict__ seq_lens, int h, int max_blocks, int num_blocks,
                         int num_splits, int fixed_pps, const int* __restrict__ pps_dev,
-                        float qscale, float* __restrict__ o_part,
-                        float* __restrict__ m_part, float* __restrict__ l_part) {
+                        const int32_t* __restrict__ q_rows, float qscale,
+                        float* __restrict__ o_part, float* __restrict__ m_part,
+                        float* __restrict__ l_part) {
   using C = DecodeCfg<D, G, NW, NST>;
   constexpr int KS = D / 16;  // k-steps of S = q K^T
   constexpr int ND = D / 8;   // n-tiles of O~ += P V
@@ -139,7 +140,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
   uint32_t n_sm;
   asm("mov.u32 %0, %%nsmid;" : "=r"(n_sm));
   const uint32_t cta = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
-  if (lane == 0 && cta < n_sm) {
+  if (lane == 0 && cta < n_sm && q_rows == nullptr) {
     const int sl = min(max(__ldcg(seq_lens + b), 0), max_blocks * kPage);
     const int np = (sl + kPage - 1) / kPage;  // 0 .. max_blocks
     // Pages per split as the plan takes them. A value read this early may be
@@ -165,11 +166,20 @@ __global__ void __launch_bounds__(NW * 32, 1)
   pdl_wait();     // q, seq_lens, the split plan and the partials' buffers are the previous kernel's
   pdl_trigger();  // the merge may be scheduled once every split CTA is running
 
+  // A mixed batch (q_rows = its cu_seqlens_q): only the rows with one query
+  // are decoded here, their query at token q_rows[b]; the others return.
+  size_t q_tok = b;
+  if (q_rows != nullptr) {
+    const int r0 = __ldcg(q_rows + b), r1 = __ldcg(q_rows + b + 1);
+    if (r1 - r0 != 1) return;
+    q_tok = r0;
+  }
+
   // q fragments first: they do not depend on the row length. A-operand
   // layout of m16n8k16: a0 = (row gid, k 2tq..2tq+1), a2 = (row gid, k+8).
   uint32_t qa0[KS], qa2[KS];
   {
-    const __nv_bfloat16* qr = q + (size_t(b) * h + kvh * G + min(gid, G - 1)) * D + 2 * tq;
+    const __nv_bfloat16* qr = q + (q_tok * h + kvh * G + min(gid, G - 1)) * D + 2 * tq;
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
       const uint32_t x0 = __ldg(reinterpret_cast<const uint32_t*>(qr + 16 * ks));
@@ -408,7 +418,7 @@ cudaError_t launch_cfg(const DecodeArgs& a, const CUtensorMap& tk, const CUtenso
   return launch_pdl(kern, grid, dim3(NW * 32), C::SMEM, stream, tk, tv,
                     static_cast<const __nv_bfloat16*>(a.q), a.block_table, a.seq_lens, a.h,
                     a.max_blocks_per_seq, a.num_blocks, a.num_splits, a.fixed_pps, a.pps_dev,
-                    qscale, a.o_part, a.m_part, a.l_part);
+                    a.q_rows, qscale, a.o_part, a.m_part, a.l_part);
 }
 
 template <int D>
@@ -427,31 +437,37 @@ cudaError_t launch_d(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorM
 // On-device split plan of the adaptive decode: the batch's longest and total
 // (clamped) length, splits_rule, then pages per split of the longest row. The
 // split kernel and the merge read the result, so the launch geometry (a grid
-// of max_splits) never depends on the lengths.
+// of max_splits) never depends on the lengths. With q_rows (a mixed batch's
+// cu_seqlens_q) only the rows with one query count.
 __global__ void __launch_bounds__(256)
-    decode_plan_kernel(const int32_t* __restrict__ seq_lens, int B, int h_kv, int max_len,
-                       int num_sms, int max_splits, int* __restrict__ pps_out) {
+    decode_plan_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ q_rows,
+                       int B, int h_kv, int max_len, int num_sms, int max_splits,
+                       int* __restrict__ pps_out) {
   __shared__ long long s_tot[256];
-  __shared__ int s_max[256];
+  __shared__ int s_max[256], s_cnt[256];
   long long tot = 0;
-  int mx = 0;
+  int mx = 0, cnt = 0;
   for (int b = threadIdx.x; b < B; b += blockDim.x) {
+    if (q_rows != nullptr && q_rows[b + 1] - q_rows[b] != 1) continue;
     const int len = clamp_seq_len(seq_lens[b], max_len, &g_decode_err);
     tot += len;
     mx = max(mx, len);
+    ++cnt;
   }
   s_tot[threadIdx.x] = tot;
   s_max[threadIdx.x] = mx;
+  s_cnt[threadIdx.x] = cnt;
   __syncthreads();
   for (int off = blockDim.x / 2; off > 0; off >>= 1) {
     if (threadIdx.x < off) {
       s_tot[threadIdx.x] += s_tot[threadIdx.x + off];
       s_max[threadIdx.x] = max(s_max[threadIdx.x], s_max[threadIdx.x + off]);
+      s_cnt[threadIdx.x] += s_cnt[threadIdx.x + off];
     }
     __syncthreads();
   }
   if (threadIdx.x == 0) {
-    const int s = splits_rule(B, h_kv, s_max[0], s_tot[0], num_sms, max_splits);
+    const int s = splits_rule(max(s_cnt[0], 1), h_kv, s_max[0], s_tot[0], num_sms, max_splits);
     const int max_pages = (s_max[0] + kPage - 1) / kPage;
     *pps_out = max(1, (max_pages + s - 1) / s);
   }
@@ -459,10 +475,11 @@ __global__ void __launch_bounds__(256)
 
 }  // namespace
 
-cudaError_t launch_decode_plan(const int32_t* seq_lens, int B, int h_kv, int max_len,
-                               int num_sms, int max_splits, int* pps_out, cudaStream_t stream) {
-  decode_plan_kernel<<<1, 256, 0, stream>>>(seq_lens, B, h_kv, max_len, num_sms, max_splits,
-                                            pps_out);
+cudaError_t launch_decode_plan(const int32_t* seq_lens, const int32_t* q_rows, int B, int h_kv,
+                               int max_len, int num_sms, int max_splits, int* pps_out,
+                               cudaStream_t stream) {
+  decode_plan_kernel<<<1, 256, 0, stream>>>(seq_lens, q_rows, B, h_kv, max_len, num_sms,
+                                            max_splits, pps_out);
   return cudaGetLastError();
 }
 

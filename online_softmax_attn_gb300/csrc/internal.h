@@ -32,11 +32,13 @@ inline PartialLayout partial_layout(long long rows, int num_splits, int d_h) {
 // seq_lens != nullptr: n_active(row) = split_plan(seq_lens[row / heads_per_seq]),
 // with the length clamped into [0, max_len] exactly as the decode kernel does.
 // fixed_pps as in split_plan_fixed (0: pages per split from num_splits).
+// q_rows != nullptr (a mixed batch's cu_seqlens_q): only rows of sequences
+// with one query are merged, each written at token q_rows[row / heads_per_seq].
 cudaError_t launch_merge(const float* o_part, const float* m_part, const float* l_part,
                          const int32_t* n_active, const int32_t* seq_lens, int heads_per_seq,
                          int page_size, int max_len, int rows, int num_splits, int d_h, void* o, float* lse,
                          attn_dtype_t out_dtype, cudaStream_t stream, int fixed_pps = 0,
-                         const int* pps_dev = nullptr);
+                         const int* pps_dev = nullptr, const int32_t* q_rows = nullptr);
 unsigned int merge_read_and_clear_error(cudaStream_t stream, cudaError_t* st);
 // Pairwise (O, LSE) merge; arguments validated by the caller.
 cudaError_t launch_merge_pair(const void* o_a, const float* lse_a, const void* o_b,
@@ -57,11 +59,15 @@ struct DecodeArgs {
   float* l_part;
   int fixed_pps = 0;  // > 0: fixed pages per split (split_plan_fixed)
   const int* pps_dev = nullptr;  // non-null: pages per split read from device memory
+  // Non-null (a mixed batch's cu_seqlens_q [B + 1]): only rows with one query
+  // are decoded, their query and output at token q_rows[b].
+  const int32_t* q_rows = nullptr;
 };
 // One CTA: the batch's split count by splits_rule, as pages per split of the
 // longest row, written to *pps_out (adaptive decode).
-cudaError_t launch_decode_plan(const int32_t* seq_lens, int B, int h_kv, int max_len,
-                               int num_sms, int max_splits, int* pps_out, cudaStream_t stream);
+cudaError_t launch_decode_plan(const int32_t* seq_lens, const int32_t* q_rows, int B, int h_kv,
+                               int max_len, int num_sms, int max_splits, int* pps_out,
+                               cudaStream_t stream);
 cudaError_t launch_decode_split(const DecodeArgs& a, cudaStream_t stream);
 unsigned int decode_read_and_clear_error(cudaStream_t stream, cudaError_t* st);
 cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, cudaStream_t stream);
@@ -100,6 +106,7 @@ struct PagedPrefill {
   float scale;
   void* o;                     // [total_q, h, d_h] bf16
   float* lse;                  // [total_q, h] or nullptr
+  int decode_rows_apart = 0;   // nonzero: rows of one query get no query tiles
 };
 cudaError_t launch_prefill_paged(const PagedPrefill& a, cudaStream_t stream);
 unsigned int prefill_read_and_clear_error(cudaStream_t stream, cudaError_t* st);

@@ -35,7 +35,8 @@ __global__ void __launch_bounds__(WPR > 8 ? WPR * 32 : 256)
                         const float* __restrict__ l_part, const int32_t* __restrict__ n_active,
                         const int32_t* __restrict__ seq_lens, int heads_per_seq, int page_size,
                         int max_len, int rows, int S, void* __restrict__ o_out, float* __restrict__ lse_out,
-                        int fixed_pps, const int* __restrict__ pps_dev) {
+                        int fixed_pps, const int* __restrict__ pps_dev,
+                        const int32_t* __restrict__ q_rows) {
   constexpr int VEC = D / 32;
   static_assert(VEC == 2 || VEC == 4, "d_h must be 64 or 128");
   constexpr int RPC = WPR > 8 ? 1 : 8 / WPR;  // rows per CTA (8 warps, or WPR warps for one row)
@@ -52,7 +53,17 @@ __global__ void __launch_bounds__(WPR > 8 ? WPR * 32 : 256)
   pdl_wait();  // the partials are the previous kernel's output
   pdl_trigger();
   if (WPR == 1 && row >= rows) return;
-  const bool live = row < rows;  // WPR > 1: one row per CTA, always live
+  bool live = row < rows;  // WPR > 1: one row per CTA
+  // Where the row is written: the row itself, or in a mixed batch the token
+  // of its sequence's one query (rows of longer sequences are not merged).
+  size_t out_row = row;
+  if (q_rows != nullptr && live) {
+    const int b = row / heads_per_seq;
+    const int r0 = q_rows[b], r1 = q_rows[b + 1];
+    live = r1 - r0 == 1;
+    out_row = size_t(r0) * heads_per_seq + row % heads_per_seq;
+  }
+  if (WPR == 1 && !live) return;
 
   const float* mrow = m_part + size_t(row) * S;
   const float* lrow = l_part + size_t(row) * S;
@@ -162,7 +173,7 @@ __global__ void __launch_bounds__(WPR > 8 ? WPR * 32 : 256)
 
   if constexpr (kOutBf16) {
     uint32_t* dst = reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(o_out) +
-                                                size_t(row) * D + lane * VEC);
+                                                out_row * D + lane * VEC);
     if constexpr (VEC == 4) {
       uint2 pk;
       pk.x = pack_bf16x2(acc[0], acc[1]);
@@ -172,7 +183,7 @@ __global__ void __launch_bounds__(WPR > 8 ? WPR * 32 : 256)
       dst[0] = pack_bf16x2(acc[0], acc[1]);
     }
   } else {
-    float* dst = static_cast<float*>(o_out) + size_t(row) * D + lane * VEC;
+    float* dst = static_cast<float*>(o_out) + out_row * D + lane * VEC;
     if constexpr (VEC == 4) {
       *reinterpret_cast<float4*>(dst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
     } else {
@@ -180,14 +191,14 @@ __global__ void __launch_bounds__(WPR > 8 ? WPR * 32 : 256)
     }
   }
   // M is in exp2 units here; the partials' m and the LSE are natural-log.
-  if (lse_out != nullptr && lane == 0) lse_out[row] = empty ? -INFINITY : M * kLn2 + logf(L);
+  if (lse_out != nullptr && lane == 0) lse_out[out_row] = empty ? -INFINITY : M * kLn2 + logf(L);
 }
 
 cudaError_t launch_merge(const float* o_part, const float* m_part, const float* l_part,
                          const int32_t* n_active, const int32_t* seq_lens, int heads_per_seq,
                          int page_size, int max_len, int rows, int num_splits, int d_h, void* o, float* lse,
                          attn_dtype_t out_dtype, cudaStream_t stream, int fixed_pps,
-                         const int* pps_dev) {
+                         const int* pps_dev, const int32_t* q_rows) {
   if (rows <= 0) return cudaSuccess;
   // Few rows and many splits: spread each row's splits over 8 warps, or over
   // 32 (one 1024-thread CTA per row) when there are more than 64 splits and
@@ -204,7 +215,7 @@ cudaError_t launch_merge(const float* o_part, const float* m_part, const float* 
 #define ATTN_MERGE_LAUNCH(D, BF, W)                                                               \
   e = launch_pdl(merge_states_kernel<D, BF, W>, grid, block, 0, stream, o_part, m_part, l_part, \
                  n_active, seq_lens, heads_per_seq, page_size, max_len, rows, num_splits, o, lse, \
-                 fixed_pps, pps_dev)
+                 fixed_pps, pps_dev, q_rows)
   if (d_h == 128) {
     if (bf) {
       if (wider) ATTN_MERGE_LAUNCH(128, true, 32);

@@ -792,12 +792,12 @@ __global__ void __launch_bounds__(256)
     paged_v_to_f16_kernel(const uint4* __restrict__ vc, const int32_t* __restrict__ block_table,
                           const int32_t* __restrict__ cu_q, const int32_t* __restrict__ seq_lens,
                           int max_blocks, int num_blocks, int h_kv, int max_tiles,
-                          uint4* __restrict__ v16, int* __restrict__ vwide) {
+                          int skip_single, uint4* __restrict__ v16, int* __restrict__ vwide) {
   constexpr int PER = kBN * CPR / 256;  // chunks per thread
   const int jt = blockIdx.x, b = blockIdx.y, kvh = blockIdx.z;
   const int cap = max_blocks * 16;
   const int q_len = cu_q[b + 1] - cu_q[b];
-  if (q_len < 0 || q_len > cap) return;
+  if (q_len < 0 || q_len > cap || (skip_single && q_len == 1)) return;
   int ctx = seq_lens[b];
   if (ctx < q_len || ctx > cap) ctx = ctx < q_len ? q_len : cap;
   const int n_pages = (ctx + 15) / 16;
@@ -891,9 +891,10 @@ cudaError_t launch(const void* q, const void* k, const void* v, const void* v16,
 
 // Row b's query tiles: tile_off[b+1] = tile_off[b] + ceil(q_len_b / 128). A
 // query count below 0 or above max_q_len (the grid's bound) is an error:
-// that row gets no tiles and its outputs are not written.
+// that row gets no tiles and its outputs are not written. With skip_single,
+// rows of one query get no tiles either (the split-KV decode takes them).
 __global__ void paged_tiles_kernel(const int32_t* __restrict__ cu_q, int B, int max_q_len,
-                                   int max_blocks, int32_t* __restrict__ tile_off) {
+                                   int max_blocks, int skip_single, int32_t* __restrict__ tile_off) {
   if (threadIdx.x != 0) return;
   int acc = 0;
   tile_off[0] = 0;
@@ -903,6 +904,7 @@ __global__ void paged_tiles_kernel(const int32_t* __restrict__ cu_q, int B, int 
       atomicOr(&g_prefill_err, ATTN_DEVERR_BAD_SEQ_LEN);
       n = 0;
     }
+    if (skip_single && n == 1) n = 0;  // a decode row, handled by the split-KV decode
     acc += (n + kBM - 1) / kBM;
     tile_off[b + 1] = acc;
   }
@@ -947,11 +949,12 @@ cudaError_t launch_paged(const PagedPrefill& a, cudaStream_t stream) {
       return cudaErrorInvalidValue;
     paged_v_to_f16_kernel<D / 8><<<dim3(max_tiles, a.B, a.h_kv), 256, 0, stream>>>(
         static_cast<const uint4*>(a.v_cache), a.block_table, a.cu_q, a.seq_lens, a.max_blocks,
-        a.num_blocks, a.h_kv, max_tiles, static_cast<uint4*>(a.v16), a.vwide);
+        a.num_blocks, a.h_kv, max_tiles, a.decode_rows_apart, static_cast<uint4*>(a.v16), a.vwide);
     const cudaError_t e0 = cudaGetLastError();
     if (e0 != cudaSuccess) return e0;
   }
-  paged_tiles_kernel<<<1, 32, 0, stream>>>(a.cu_q, a.B, a.max_q_len, a.max_blocks, a.tile_off);
+  paged_tiles_kernel<<<1, 32, 0, stream>>>(a.cu_q, a.B, a.max_q_len, a.max_blocks,
+                                           a.decode_rows_apart, a.tile_off);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   auto kern = a.v16 ? prefill_bf16_kernel<D, NQ, NSK, NSV, true, true>

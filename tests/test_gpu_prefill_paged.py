@@ -36,12 +36,19 @@ MIXED = ([1, 128, 200, 77, 5, 300, 1, 129],
 @pytest.mark.parametrize("h,h_kv,d", [(8, 2, 128), (6, 2, 128), (4, 2, 64)])
 @pytest.mark.parametrize("causal", [True, False])
 @pytest.mark.parametrize("workspace", ["auto", None], ids=["fp16V", "bf16V"])
-def test_mixed_batch_matches_oracle(h, h_kv, d, causal, workspace):
+@pytest.mark.parametrize("decode_splits", [0, 32], ids=["decode_rows_as_tiles", "decode_rows_split"])
+def test_mixed_batch_matches_oracle(h, h_kv, d, causal, workspace, decode_splits):
+    """Rows of 1, 5, 77-300 queries; the one-query rows either as 1-row query
+    tiles or through the split-KV decode (g = 3 has no decode kernel, so
+    h = 6 keeps the tiles)."""
+    if decode_splits and (h // h_kv) not in (1, 2, 4, 8):
+        decode_splits = 0
     q_lens, ctx = MIXED
     q, kc, vc, table, cu, seq = paged_batch(q_lens, ctx, h, h_kv, d, 3)
     scale = 1.0 / d ** 0.5
     o, lse = attn.attn_prefill_paged(q.cuda(), kc.cuda(), vc.cuda(), table.cuda(), cu.cuda(), seq.cuda(),
-                                     max(q_lens), causal, scale, workspace=workspace)
+                                     max(q_lens), causal, scale, workspace=workspace,
+                                     decode_splits=decode_splits)
     torch.cuda.synchronize()
     assert attn.attn_get_device_error() == 0
     O_ref, L_ref = oracle.prefill_paged_ref(q, kc, vc, table, cu, seq, scale, causal)
@@ -192,3 +199,48 @@ def test_widened_logits_mixed_batch(workspace):
     O_ref, L_ref = oracle.prefill_paged_ref(q, kc, vc, table, cu, seq, scale, True)
     check_out(o, O_ref, torch.bfloat16)
     check_lse(lse, L_ref)
+
+
+@pytest.mark.parametrize("decode_splits", [1, 5, 32])
+@pytest.mark.parametrize("workspace", ["auto", None], ids=["fp16V", "bf16V"])
+def test_decode_heavy_mixed_batch(decode_splits, workspace):
+    """The shape of a serving step: 3 chunked-prefill rows and 40 decode rows
+    over 1-5000 keys (lengths crossing page edges), every row against the
+    oracle, whatever the decode rows' split bound."""
+    h, h_kv, d = 32, 8, 128
+    g = torch.Generator().manual_seed(17)
+    dec_ctx = torch.randint(1, 5000, (40,), generator=g).tolist()
+    dec_ctx[:4] = [1, 15, 16, 17]
+    q_lens = [300, 128, 1] + [1] * 40
+    ctx = [1000, 128, 4097] + dec_ctx
+    q, kc, vc, table, cu, seq = paged_batch(q_lens, ctx, h, h_kv, d, 19)
+    scale = 1.0 / d ** 0.5
+    o, lse = attn.attn_prefill_paged(q.cuda(), kc.cuda(), vc.cuda(), table.cuda(), cu.cuda(), seq.cuda(),
+                                     max(q_lens), True, scale, workspace=workspace,
+                                     decode_splits=decode_splits)
+    torch.cuda.synchronize()
+    assert attn.attn_get_device_error() == 0
+    O_ref, L_ref = oracle.prefill_paged_ref(q, kc, vc, table, cu, seq, scale, True)
+    check_out(o, O_ref, torch.bfloat16, f"mixed decode_splits={decode_splits}")
+    check_lse(lse, L_ref)
+
+
+def test_caller_workspace_with_decode_part():
+    """A caller's workspace holding the decode part and the fp16-V form."""
+    h, h_kv, d = 8, 2, 128
+    q_lens, ctx = MIXED
+    q, kc, vc, table, cu, seq = paged_batch(q_lens, ctx, h, h_kv, d, 5)
+    B, mb = len(ctx), table.shape[1]
+    n = (attn.attn_prefill_paged_decode_workspace_bytes(B, h, d, 7) +
+         attn.attn_prefill_paged_workspace_bytes(B, mb, h_kv, d, v16=True))
+    ws = torch.full((n,), 0x7f, dtype=torch.uint8, device="cuda")
+    o, lse = attn.attn_prefill_paged(q.cuda(), kc.cuda(), vc.cuda(), table.cuda(), cu.cuda(), seq.cuda(),
+                                     max(q_lens), True, 1.0 / d ** 0.5, workspace=ws, decode_splits=7)
+    torch.cuda.synchronize()
+    O_ref, L_ref = oracle.prefill_paged_ref(q, kc, vc, table, cu, seq, 1.0 / d ** 0.5, True)
+    check_out(o, O_ref, torch.bfloat16, "caller workspace with decode part")
+    check_lse(lse, L_ref)
+    with pytest.raises(attn.AttnError):  # one byte short of the decode part plus the small form
+        small = attn.attn_prefill_paged_decode_workspace_bytes(B, h, d, 7) + attn.attn_prefill_paged_workspace_bytes(B)
+        attn.attn_prefill_paged(q.cuda(), kc.cuda(), vc.cuda(), table.cuda(), cu.cuda(), seq.cuda(),
+                                max(q_lens), True, workspace=ws[:small - 1], decode_splits=7)
