@@ -390,8 +390,8 @@ def run_gpu(args, world, rank, local):
     dq, kc, vc, table, seq = W.decode_inputs(DECODE, seed=rank, device=dev, seq_lens=lens)
     table, seq = table.to(dev), seq.to(dev)
     B = len(lens)
-    S = attn.attn_recommended_splits(B, DECODE.h_kv, max(lens), sum(lens))
-    ws = torch.empty(attn.attn_decode_workspace_bytes(B, DECODE.h, DECODE.d_h, S), dtype=torch.uint8, device=dev)
+    S = attn.attn_recommended_splits_ragged(B, DECODE.h_kv, max(lens), sum(lens))
+    ws = torch.empty(attn.attn_decode_workspace_bytes(B, DECODE.h, S, DECODE.d_h), dtype=torch.uint8, device=dev)
     do = torch.empty_like(dq)
     dlse = torch.empty((B, DECODE.h), dtype=torch.float32, device=dev)
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
@@ -517,7 +517,7 @@ def run_gpu(args, world, rank, local):
     if args.only is None and not args.no_extras:
         pps = 128
         det_splits = -(-table.shape[1] // pps)
-        det_ws = torch.empty(attn.attn_decode_workspace_bytes(B, DECODE.h, DECODE.d_h, det_splits),
+        det_ws = torch.empty(attn.attn_decode_workspace_bytes(B, DECODE.h, det_splits, DECODE.d_h),
                              dtype=torch.uint8, device=dev)
         for _ in range(3):
             attn.attn_decode_paged_deterministic(dq, kc, vc, table, seq, pps, DECODE.scale,
@@ -539,7 +539,7 @@ def run_gpu(args, world, rank, local):
     adaptive = None
     if args.only is None and not args.no_extras:
         amax = 32
-        ad_ws = torch.empty(attn.attn_decode_adaptive_workspace_bytes(B, DECODE.h, DECODE.d_h, amax),
+        ad_ws = torch.empty(attn.attn_decode_adaptive_workspace_bytes(B, DECODE.h, amax, DECODE.d_h),
                             dtype=torch.uint8, device=dev)
         for _ in range(3):
             attn.attn_decode_paged_adaptive(dq, kc, vc, table, seq, amax, DECODE.scale,
@@ -554,7 +554,7 @@ def run_gpu(args, world, rank, local):
             b_.synchronize()
             ams.append(a_.elapsed_time(b_))
         at = statistics.median(ams)
-        off = attn.attn_decode_workspace_bytes(B, DECODE.h, DECODE.d_h, amax)
+        off = attn.attn_decode_workspace_bytes(B, DECODE.h, amax, DECODE.d_h)
         adaptive = {"value": db / (at * 1e-3) / 1e9, "unit": "GB/s", "ms": at, "max_splits": amax,
                     "device_pages_per_split": int(ad_ws[off:off + 4].view(torch.int32).item()),
                     "frac_of_hbm": db / (at * 1e-3) / 1e9 / hbm_peak}
@@ -749,7 +749,7 @@ def measure_mixed(dev, flush, hbm_peak, tc_peak, peak_kind, iters=10):
     o = torch.empty_like(q)
     lse = torch.empty((total_q, h), dtype=torch.float32, device=dev)
     dsplit = 32
-    ws = torch.empty(attn.attn_prefill_paged_decode_workspace_bytes(B, h, d, dsplit) +
+    ws = torch.empty(attn.attn_prefill_paged_decode_workspace_bytes(B, h, dsplit, d) +
                      attn.attn_prefill_paged_workspace_bytes(B, mb, h_kv, d, v16=True),
                      dtype=torch.uint8, device=dev)
     # the prefill rows alone
@@ -761,8 +761,8 @@ def measure_mixed(dev, flush, hbm_peak, tc_peak, peak_kind, iters=10):
     # the decode rows alone
     dq = q[n_pre * qn:].contiguous()
     dseq, dtab = seq[n_pre:].contiguous(), table[n_pre:].contiguous()
-    S = attn.attn_recommended_splits(64, h_kv, max(dec_lens), sum(dec_lens))
-    dws = torch.empty(attn.attn_decode_workspace_bytes(64, h, d, S), dtype=torch.uint8, device=dev)
+    S = attn.attn_recommended_splits_ragged(64, h_kv, max(dec_lens), sum(dec_lens))
+    dws = torch.empty(attn.attn_decode_workspace_bytes(64, h, S, d), dtype=torch.uint8, device=dev)
     do, dl = torch.empty_like(dq), torch.empty((64, h), dtype=torch.float32, device=dev)
     calls = {
         "mixed": lambda: attn.attn_prefill_paged(q, kc, vc, table, cu, seq, qn, True, PREFILL.scale,
@@ -883,7 +883,7 @@ def measure_decode_batch1(dev, hbm_peak, peak_kind):
         kv = kc.numel() * kc.element_size() * 2
         copies = max(2, -(-2 * l2 // kv))
         caches = [(kc.clone(), vc.clone()) for _ in range(copies)]
-        ws = torch.empty(max(attn.attn_decode_workspace_bytes(1, shape.h, shape.d_h, splits), 256),
+        ws = torch.empty(max(attn.attn_decode_workspace_bytes(1, shape.h, splits, shape.d_h), 256),
                          dtype=torch.uint8, device=dev)
         o = torch.empty_like(q)
         lse = torch.empty((1, shape.h), dtype=torch.float32, device=dev)

@@ -34,6 +34,22 @@
  *   - LSE is the natural-log log-sum-exp m + ln(l) of the scaled logits, fp32.
  *   - A query row with no allowed key yields output 0 and LSE = -inf ([MRG],
  *     last paragraph: zero output is the extension chosen for empty rows).
+ *   - Signatures. The three core calls keep their minimal argument lists,
+ *     with these additions, each where the minimal form could not serve:
+ *       attn_prefill       workspace, workspace_bytes (after dtype): scratch
+ *                          for the fp16 copy of V with which P V runs as one
+ *                          fp16 tensor-core product per key tile instead of
+ *                          two bf16 ones (1.13x on the causal T = 8192
+ *                          layer); NULL keeps the no-scratch form.
+ *       attn_decode_paged  num_blocks (after page_size): the cache's page
+ *                          count, which the TMA tensor map over the cache
+ *                          needs, and against which table entries are
+ *                          checked (an entry outside the cache reads zeros
+ *                          and sets an error bit instead of reading past it).
+ *       attn_merge_states  none.
+ *     attn_decode_workspace_bytes and attn_recommended_splits keep theirs;
+ *     the ragged-batch split rule, which needs the batch's total length, is
+ *     attn_recommended_splits_ragged. Every other call is an addition.
  *   - Errors: arguments are validated on the host before anything is
  *     launched; an invalid call returns ATTN_ERR_INVALID_ARG (or
  *     ATTN_ERR_UNSUPPORTED for a well-formed but unbuilt shape) and enqueues
@@ -72,7 +88,7 @@ typedef enum { ATTN_DTYPE_F32 = 0, ATTN_DTYPE_BF16 = 1 } attn_dtype_t;
 /* Human-readable name of a status code; never NULL. */
 const char* attn_status_string(attn_status_t status);
 
-/* Library ABI version (major * 100 + minor). */
+/* Library ABI version (major * 100 + minor): 300. */
 int attn_version(void);
 
 /*
@@ -223,8 +239,8 @@ attn_status_t attn_prefill_host(const void* q, const void* k, const void* v, voi
  *   decode_splits 0, or the most splits a decode row may take
  *                (1 .. ATTN_MAX_SPLITS); see above
  *   workspace    256-byte aligned device memory, overwritten by the call:
- *                first attn_prefill_paged_decode_workspace_bytes(B, h, d_h,
- *                decode_splits) bytes (0 when decode_splits is 0) for the
+ *                first attn_prefill_paged_decode_workspace_bytes(B, h,
+ *                decode_splits, d_h) bytes (0 when decode_splits is 0) for the
  *                decode rows, then the prefill's own part: at least
  *                attn_prefill_paged_workspace_bytes(B) bytes (per-row tile
  *                offsets), or, for the fp16 V form, at least
@@ -266,11 +282,11 @@ size_t attn_prefill_paged_v16_workspace_bytes(int B, int max_blocks_per_seq, int
 /*
  * attn_prefill_paged_decode_workspace_bytes -- bytes at the front of
  * attn_prefill_paged's workspace for its decode rows: split partials
- * (attn_decode_workspace_bytes(B, h, d_h, decode_splits)) and 256 bytes for
+ * (attn_decode_workspace_bytes(B, h, decode_splits, d_h)) and 256 bytes for
  * the device split plan. 0 when decode_splits is 0, and on invalid arguments.
  * Host-only, pure.
  */
-size_t attn_prefill_paged_decode_workspace_bytes(int B, int h, int d_h, int decode_splits);
+size_t attn_prefill_paged_decode_workspace_bytes(int B, int h, int decode_splits, int d_h);
 attn_status_t attn_prefill_paged(const void* q, const void* k_cache, const void* v_cache,
                                  const int32_t* block_table, const int32_t* cu_seqlens_q,
                                  const int32_t* seq_lens, int B, int total_q, int h, int h_kv,
@@ -293,19 +309,27 @@ attn_status_t attn_prefill_paged(const void* q, const void* k_cache, const void*
 int attn_decode_split_plan(int seq_len, int page_size, int num_splits, int* pages_per_split);
 
 /*
- * attn_recommended_splits -- split count for a decode batch on a GPU with
- * num_sms SMs. Follows [DEC] "The grid" (fill the first wave:
- * S* = ceil(N_SM / G_2D) with G_2D = B * h_kv). For a ragged batch (the
- * longest row more than 1.25x the mean length, known from total_seq_len) the
- * splits are raised until the longest row's split is no larger than a
- * quarter of the mean work per CTA slot. Finally each split of the longest
- * row keeps at least 32 pages (so a CTA's start-up is amortised). Result in
- * [1, ATTN_MAX_SPLITS]. Host-only, pure; -1 on invalid arguments.
- * total_seq_len may be 0 when unknown (then the ragged rule is skipped).
+ * attn_recommended_splits -- split count for a decode batch on `device`.
+ * Follows [DEC] "The grid": fill the first wave, S* = ceil(N_SM / G_2D) with
+ * G_2D = B * h_kv and N_SM the device's SM count; then each split of the
+ * longest row keeps at least 32 pages (so a CTA's start-up is amortised).
+ * Result in [1, ATTN_MAX_SPLITS]. Host-only (it queries the device's SM
+ * count); -1 on invalid arguments or when the device cannot be queried.
  */
 #define ATTN_MAX_SPLITS 1024
-int attn_recommended_splits(int B, int h_kv, int max_seq_len, long long total_seq_len,
-                            int num_sms);
+int attn_recommended_splits(int B, int h_kv, int max_seq_len, int device);
+
+/*
+ * attn_recommended_splits_ragged -- attn_recommended_splits for a ragged
+ * batch, with the SM count given: when the longest row is more than 1.25x
+ * the mean length (known from total_seq_len), the splits are raised until
+ * the longest row's split is no larger than a quarter of the mean work per
+ * CTA slot, before the 32-page floor. total_seq_len may be 0 when unknown
+ * (the ragged rule is then skipped; the result is that of
+ * attn_recommended_splits). Host-only, pure; -1 on invalid arguments.
+ */
+int attn_recommended_splits_ragged(int B, int h_kv, int max_seq_len, long long total_seq_len,
+                                   int num_sms);
 
 /*
  * attn_decode_workspace_bytes -- bytes of scratch that attn_decode_paged needs
@@ -315,7 +339,7 @@ int attn_recommended_splits(int B, int h_kv, int max_seq_len, long long total_se
  *   l fp32 [B*h, num_splits], each region starting on a 256-byte boundary.
  * Host-only, pure; 0 on invalid arguments.
  */
-size_t attn_decode_workspace_bytes(int B, int h, int d_h, int num_splits);
+size_t attn_decode_workspace_bytes(int B, int h, int num_splits, int d_h);
 
 /*
  * attn_decode_paged -- split-KV (FlashDecoding) attention of one query token
@@ -334,7 +358,7 @@ size_t attn_decode_workspace_bytes(int B, int h, int d_h, int num_splits);
  *   block_table [B, max_blocks_per_seq]                  int32 (read); entries
  *               for pages >= ceil(seq_len/page_size) are never read
  *   seq_lens    [B]                                      int32 (read), >= 0
- *   workspace   attn_decode_workspace_bytes(B,h,d_h,num_splits) bytes (scratch)
+ *   workspace   attn_decode_workspace_bytes(B,h,num_splits,d_h) bytes (scratch)
  *   o           [B, h, d_h]                              bf16 (written)
  *   lse         [B, h]                 fp32, may be NULL (written)
  * page_size must be 16; d_h must be 128 or 64; g = h / h_kv in {1,2,4,8};
@@ -370,11 +394,11 @@ attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* 
  *
  * Arguments, layouts and errors are those of attn_decode_paged with
  * num_splits replaced by max_splits (1 .. ATTN_MAX_SPLITS), plus:
- *   workspace: attn_decode_adaptive_workspace_bytes(B, h, d_h, max_splits)
+ *   workspace: attn_decode_adaptive_workspace_bytes(B, h, max_splits, d_h)
  *     bytes; its last 256 bytes begin with the plan (int32 pages per split)
  *     written by the call.
  */
-size_t attn_decode_adaptive_workspace_bytes(int B, int h, int d_h, int max_splits);
+size_t attn_decode_adaptive_workspace_bytes(int B, int h, int max_splits, int d_h);
 attn_status_t attn_decode_paged_adaptive(const void* q, const void* k_cache, const void* v_cache,
                                          const int32_t* block_table, const int32_t* seq_lens,
                                          int B, int h, int h_kv, int d_h, int page_size,
@@ -421,7 +445,7 @@ attn_status_t attn_decode_paged_deterministic(const void* q, const void* k_cache
  * (ATTN_DECODE_STATIC_SCRATCH_BYTES on every GPU that loads the library, held
  * until the process exits). Arguments, layouts, results and errors are those
  * of attn_decode_paged, plus:
- *   - the partials, attn_decode_workspace_bytes(B, h, d_h, num_splits) bytes,
+ *   - the partials, attn_decode_workspace_bytes(B, h, num_splits, d_h) bytes,
  *     must fit in ATTN_DECODE_STATIC_SCRATCH_BYTES; a larger request returns
  *     ATTN_ERR_INVALID_ARG before anything is launched (use fewer splits, a
  *     smaller batch, or attn_decode_paged);

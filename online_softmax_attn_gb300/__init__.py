@@ -23,6 +23,7 @@ __all__ = [
     "attn_merge_states",
     "attn_decode_split_plan",
     "attn_recommended_splits",
+    "attn_recommended_splits_ragged",
     "attn_decode_workspace_bytes",
     "attn_get_device_error",
     "attn_get_last_device_error",
@@ -82,8 +83,10 @@ def library() -> ctypes.CDLL:
     lib.attn_prefill_paged.restype = I
     lib.attn_decode_split_plan.argtypes = [I, I, I, ctypes.POINTER(I)]
     lib.attn_decode_split_plan.restype = I
-    lib.attn_recommended_splits.argtypes = [I, I, I, Z, I]
+    lib.attn_recommended_splits.argtypes = [I, I, I, I]
     lib.attn_recommended_splits.restype = I
+    lib.attn_recommended_splits_ragged.argtypes = [I, I, I, Z, I]
+    lib.attn_recommended_splits_ragged.restype = I
     lib.attn_decode_workspace_bytes.argtypes = [I, I, I, I]
     lib.attn_decode_workspace_bytes.restype = S
     lib.attn_decode_paged.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, F, P, S, P, P, P]
@@ -261,9 +264,9 @@ def attn_prefill_paged_workspace_bytes(B: int, max_blocks: int = 0, h_kv: int = 
     return int(library().attn_prefill_paged_workspace_bytes(B))
 
 
-def attn_prefill_paged_decode_workspace_bytes(B: int, h: int, d_h: int, decode_splits: int) -> int:
+def attn_prefill_paged_decode_workspace_bytes(B: int, h: int, decode_splits: int, d_h: int) -> int:
     """Bytes at the front of attn_prefill_paged's workspace for its decode rows."""
-    return int(library().attn_prefill_paged_decode_workspace_bytes(B, h, d_h, decode_splits))
+    return int(library().attn_prefill_paged_decode_workspace_bytes(B, h, decode_splits, d_h))
 
 
 def attn_prefill_paged(q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens, max_q_len: int,
@@ -294,7 +297,7 @@ def attn_prefill_paged(q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens,
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     if decode_splits is None:
         decode_splits = 0 if isinstance(workspace, torch.Tensor) else 32
-    dec = attn_prefill_paged_decode_workspace_bytes(B, h, d, decode_splits)
+    dec = attn_prefill_paged_decode_workspace_bytes(B, h, decode_splits, d)
     if isinstance(workspace, str):
         _need(workspace == "auto", 'workspace must be "auto", None or a tensor')
         n = attn_prefill_paged_workspace_bytes(B, block_table.shape[1], h_kv, d, v16=True)
@@ -327,19 +330,30 @@ def attn_decode_split_plan(seq_len: int, num_splits: int, page_size: int = 16):
     return n, pps.value
 
 
-def attn_recommended_splits(B: int, h_kv: int, max_seq_len: int, total_seq_len: int = 0,
-                            num_sms: int | None = None) -> int:
-    if num_sms is None:
-        num_sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
-    s = library().attn_recommended_splits(int(B), int(h_kv), int(max_seq_len), int(total_seq_len),
-                                          int(num_sms))
+def attn_recommended_splits(B: int, h_kv: int, max_seq_len: int, device: int | None = None) -> int:
+    """Split count filling the first wave of `device` (default: the current one)."""
+    if device is None:
+        device = torch.cuda.current_device()
+    s = library().attn_recommended_splits(int(B), int(h_kv), int(max_seq_len), int(device))
     if s < 1:
         raise ValueError("invalid arguments to attn_recommended_splits")
     return s
 
 
-def attn_decode_workspace_bytes(B: int, h: int, d_h: int, num_splits: int) -> int:
-    return int(library().attn_decode_workspace_bytes(int(B), int(h), int(d_h), int(num_splits)))
+def attn_recommended_splits_ragged(B: int, h_kv: int, max_seq_len: int, total_seq_len: int,
+                                   num_sms: int | None = None) -> int:
+    """Split count for a ragged batch (total_seq_len known); pure host logic."""
+    if num_sms is None:
+        num_sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    s = library().attn_recommended_splits_ragged(int(B), int(h_kv), int(max_seq_len),
+                                                 int(total_seq_len), int(num_sms))
+    if s < 1:
+        raise ValueError("invalid arguments to attn_recommended_splits_ragged")
+    return s
+
+
+def attn_decode_workspace_bytes(B: int, h: int, num_splits: int, d_h: int) -> int:
+    return int(library().attn_decode_workspace_bytes(int(B), int(h), int(num_splits), int(d_h)))
 
 
 def attn_decode_paged(q, k_cache, v_cache, block_table, seq_lens, num_splits: int,
@@ -359,7 +373,7 @@ def attn_decode_paged(q, k_cache, v_cache, block_table, seq_lens, num_splits: in
     _need(block_table.dim() == 2 and block_table.shape[0] == B and seq_lens.shape == (B,),
           "block_table [B,max_blocks] and seq_lens [B] expected")
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    need = attn_decode_workspace_bytes(B, h, d, num_splits)
+    need = attn_decode_workspace_bytes(B, h, num_splits, d)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     if o is None:
@@ -374,9 +388,9 @@ def attn_decode_paged(q, k_cache, v_cache, block_table, seq_lens, num_splits: in
     return o, lse
 
 
-def attn_decode_adaptive_workspace_bytes(B: int, h: int, d_h: int, max_splits: int) -> int:
+def attn_decode_adaptive_workspace_bytes(B: int, h: int, max_splits: int, d_h: int) -> int:
     """Partials for max_splits plus 256 bytes for the on-device plan."""
-    return library().attn_decode_adaptive_workspace_bytes(B, h, d_h, max_splits)
+    return library().attn_decode_adaptive_workspace_bytes(B, h, max_splits, d_h)
 
 
 def attn_decode_paged_adaptive(q, k_cache, v_cache, block_table, seq_lens, max_splits: int,
@@ -395,7 +409,7 @@ def attn_decode_paged_adaptive(q, k_cache, v_cache, block_table, seq_lens, max_s
     _need(block_table.dim() == 2 and block_table.shape[0] == B and seq_lens.shape == (B,),
           "block_table [B,max_blocks] and seq_lens [B] expected")
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    need = attn_decode_adaptive_workspace_bytes(B, h, d, max_splits)
+    need = attn_decode_adaptive_workspace_bytes(B, h, max_splits, d)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     if o is None:
@@ -432,7 +446,7 @@ def attn_decode_paged_deterministic(q, k_cache, v_cache, block_table, seq_lens, 
     if num_splits is None:
         num_splits = -(-max_blocks // pages_per_split)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    need = attn_decode_workspace_bytes(B, h, d, num_splits)
+    need = attn_decode_workspace_bytes(B, h, num_splits, d)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     if o is None:

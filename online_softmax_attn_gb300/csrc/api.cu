@@ -64,20 +64,29 @@ const char* attn_status_string(attn_status_t status) {
   return "unknown status";
 }
 
-int attn_version(void) { return 202; }
+int attn_version(void) { return 300; }
 
 int attn_decode_split_plan(int seq_len, int page_size, int num_splits, int* pages_per_split) {
   if (seq_len < 0 || page_size < 1 || num_splits < 1) return -1;
   return split_plan(seq_len, page_size, num_splits, pages_per_split);
 }
 
-int attn_recommended_splits(int B, int h_kv, int max_seq_len, long long total_seq_len,
-                            int num_sms) {
+int attn_recommended_splits_ragged(int B, int h_kv, int max_seq_len, long long total_seq_len,
+                                   int num_sms) {
   if (B < 1 || h_kv < 1 || max_seq_len < 0 || total_seq_len < 0 || num_sms < 1) return -1;
   return splits_rule(B, h_kv, max_seq_len, total_seq_len, num_sms, ATTN_MAX_SPLITS);
 }
 
-size_t attn_decode_workspace_bytes(int B, int h, int d_h, int num_splits) {
+int attn_recommended_splits(int B, int h_kv, int max_seq_len, int device) {
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
+    (void)cudaGetLastError();  // leave no sticky error for the caller
+    return -1;
+  }
+  return attn_recommended_splits_ragged(B, h_kv, max_seq_len, 0, sms);
+}
+
+size_t attn_decode_workspace_bytes(int B, int h, int num_splits, int d_h) {
   if (B < 0 || h < 1 || d_h < 1 || num_splits < 1) return 0;
   return partial_layout(static_cast<long long>(B) * h, num_splits, d_h).total;
 }
@@ -224,7 +233,7 @@ size_t attn_prefill_paged_v16_workspace_bytes(int B, int max_blocks_per_seq, int
   return paged_v16_layout(B, max_blocks_per_seq, h_kv, d_h).total;
 }
 
-size_t attn_prefill_paged_decode_workspace_bytes(int B, int h, int d_h, int decode_splits) {
+size_t attn_prefill_paged_decode_workspace_bytes(int B, int h, int decode_splits, int d_h) {
   if (B < 0 || h < 1 || d_h < 1 || decode_splits < 0 || decode_splits > ATTN_MAX_SPLITS) return 0;
   if (decode_splits == 0) return 0;
   // The adaptive decode's partials, then 256 bytes for its device plan.
@@ -260,7 +269,7 @@ attn_status_t attn_prefill_paged(const void* q, const void* k_cache, const void*
     return ATTN_ERR_INVALID_ARG;
   // Workspace: the decode rows' partials first (decode_splits > 0), then the
   // prefill's own layout, small or with the fp16 V copy.
-  const size_t dec_bytes = attn_prefill_paged_decode_workspace_bytes(B, h, d_h, decode_splits);
+  const size_t dec_bytes = attn_prefill_paged_decode_workspace_bytes(B, h, decode_splits, d_h);
   if (workspace_bytes < dec_bytes + attn_prefill_paged_workspace_bytes(B))
     return ATTN_ERR_INVALID_ARG;
   uint8_t* const dec_ws = static_cast<uint8_t*>(workspace);
@@ -350,7 +359,7 @@ attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* 
                            workspace_bytes, o, lse, stream);
 }
 
-size_t attn_decode_adaptive_workspace_bytes(int B, int h, int d_h, int max_splits) {
+size_t attn_decode_adaptive_workspace_bytes(int B, int h, int max_splits, int d_h) {
   if (B < 0 || h < 1 || d_h < 1 || max_splits < 1) return 0;
   return partial_layout(static_cast<long long>(B) * h, max_splits, d_h).total + 256;
 }

@@ -62,9 +62,9 @@ def _bf16_round(r: np.ndarray) -> np.ndarray:
     return torch.from_numpy(np.ascontiguousarray(r)).to(torch.bfloat16).double().numpy()
 
 
-def _record(what: str, dtype, o: np.ndarray, r: np.ndarray, err: np.ndarray):
+def _record(what: str, dtype, o: np.ndarray, r: np.ndarray, err: np.ndarray, scaled: bool = False):
     rec = {"what": what, "n": int(err.size),
-           "max_abs": float(err.max()) if err.size else 0.0}
+           "max_abs": float(err.max()) if err.size else 0.0, "scaled": scaled}
     if dtype == torch.bfloat16 and err.size:
         rec["above_2e-3"] = int((err > BF16_ABS).sum())
         # error beyond half an ulp of rounding: what the 2e-3 has to cover
@@ -92,7 +92,7 @@ def check_out(out, ref, dtype, what="o", mag=None):
         raise AssertionError(
             f"{what}: {int(bad.sum())} of {err.size} elements out of tolerance; worst at {i}: "
             f"gpu={o[i]!r} ref={r[i]!r} err={err[i]:.3e} tol={tol[i]:.3e}")
-    _record(what, dtype, o, r, err)
+    _record(what, dtype, o, r, err, scaled=mag is not None)
     return float(err.max()) if err.size else 0.0
 
 
@@ -117,7 +117,8 @@ def summary_lines() -> list[str]:
         return []
     outs = [s for s in STATS if not s.get("lse")]
     lses = [s for s in STATS if s.get("lse")]
-    bf = [s for s in outs if "excess" in s]
+    scaled = [s for s in outs if s.get("scaled")]
+    bf = [s for s in outs if "excess" in s and not s.get("scaled")]
     lines = [f"parity summary (passing checks): {len(outs)} outputs ({sum(s['n'] for s in outs)} elements), "
              f"{len(lses)} LSE"]
     if bf:
@@ -126,6 +127,9 @@ def summary_lines() -> list[str]:
         lines.append(f"  bf16: worst max_abs {w['max_abs']:.3e} ({w['what']}), "
                      f"elements above the bare 2e-3: {sum(s['above_2e-3'] for s in bf)}, "
                      f"worst error beyond rounding {x['excess']:.3e} ({x['what']})")
+    if scaled:
+        lines.append(f"  {len(scaled)} checks with |v| up to 3e5 (bound scaled by the weighted |v|): "
+                     f"worst max_abs {max(s['max_abs'] for s in scaled):.3e}")
     if lses:
         w = max(lses, key=lambda s: s["max_abs"])
         lines.append(f"  lse: worst max_abs {w['max_abs']:.3e} ({w['what']})")

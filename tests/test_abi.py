@@ -82,21 +82,21 @@ def test_split_plan_covers_every_page_once():
 def test_workspace_bytes_match_pages():
     g = golden("split_sizing.json")
     p = g["partial_bytes_B1_h32"]
-    assert attn.attn_decode_workspace_bytes(p["B"], p["h"], p["d_h"], p["S"]) == p["bytes"]
+    assert attn.attn_decode_workspace_bytes(p["B"], p["h"], p["S"], p["d_h"]) == p["bytes"]
     per = g["partial_bytes_per_token_head"]
-    assert attn.attn_decode_workspace_bytes(1, 1, per["d_h"], per["S"]) >= per["bytes"]
-    assert attn.attn_decode_workspace_bytes(0, 1, 128, 1) == 0
+    assert attn.attn_decode_workspace_bytes(1, 1, per["S"], per["d_h"]) >= per["bytes"]
+    assert attn.attn_decode_workspace_bytes(0, 1, 1, 128) == 0
 
 
 def test_first_wave_split_count():
     g = golden("split_sizing.json")
     for case in g["first_wave_splits"]:
         # G_2D = B * h_kv at B = 1
-        assert attn.attn_recommended_splits(1, case["g2d"], 1 << 20, 0, case["n_sm"]) == case["splits"]
+        assert attn.attn_recommended_splits_ragged(1, case["g2d"], 1 << 20, 0, case["n_sm"]) == case["splits"]
 
 
 def test_recommended_splits_ragged_batch_balances():
-    s = attn.attn_recommended_splits(66, 8, 16384, 64 * 8192, 152)
+    s = attn.attn_recommended_splits_ragged(66, 8, 16384, 64 * 8192, 152)
     assert s >= 2
     # Longest row's split is at most a quarter of the mean work per SM.
     pages_max = 16384 // 16
@@ -203,12 +203,12 @@ def test_prefill_workspace_bytes(lib):
 def test_recommended_splits_uniform_rows_and_minimum_work():
     """Rows of one length take the first-wave count; no split of the longest
     row gets fewer than 32 pages; the ragged rule needs a row well above the mean."""
-    assert attn.attn_recommended_splits(1, 8, 32768, 32768, 152) == 19   # ceil(152 / 8)
-    assert attn.attn_recommended_splits(1, 1, 32768, 32768, 152) == 64   # 2048 pages / 32
-    assert attn.attn_recommended_splits(1, 8, 256, 256, 152) == 1        # 16 pages: one split
-    assert attn.attn_recommended_splits(4, 8, 8192, 4 * 8192, 152) == 5  # uniform batch: ceil(152 / 32)
+    assert attn.attn_recommended_splits_ragged(1, 8, 32768, 32768, 152) == 19   # ceil(152 / 8)
+    assert attn.attn_recommended_splits_ragged(1, 1, 32768, 32768, 152) == 64   # 2048 pages / 32
+    assert attn.attn_recommended_splits_ragged(1, 8, 256, 256, 152) == 1        # 16 pages: one split
+    assert attn.attn_recommended_splits_ragged(4, 8, 8192, 4 * 8192, 152) == 5  # uniform batch: ceil(152 / 32)
     # ragged: one long row among short ones raises the count above the first wave
-    assert attn.attn_recommended_splits(8, 8, 16384, 16384 + 7 * 512, 152) > 3
+    assert attn.attn_recommended_splits_ragged(8, 8, 16384, 16384 + 7 * 512, 152) > 3
 
 
 def test_merge_lse_pair_arguments(lib):
@@ -252,8 +252,8 @@ def test_decode_deterministic_arguments(lib):
 
 def test_decode_adaptive_workspace(lib):
     """The adaptive decode needs the partials for max_splits plus 256 bytes."""
-    need = attn.attn_decode_workspace_bytes(3, 32, 128, 16)
-    assert attn.attn_decode_adaptive_workspace_bytes(3, 32, 128, 16) == need + 256
+    need = attn.attn_decode_workspace_bytes(3, 32, 16, 128)
+    assert attn.attn_decode_adaptive_workspace_bytes(3, 32, 16, 128) == need + 256
     P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
     lib.attn_decode_paged_adaptive.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, F, P,
                                                ctypes.c_size_t, P, P, P]
@@ -272,7 +272,7 @@ def test_selftest_wait_timeout_arguments(lib):
 
 def test_version(lib):
     lib.attn_version.restype = ctypes.c_int
-    assert lib.attn_version() == 202
+    assert lib.attn_version() == 300
 
 
 def test_prefill_host_checks_limits_before_queueing(lib):
@@ -301,3 +301,54 @@ def test_prefill_host_checks_limits_before_queueing(lib):
     st = f(fake, fake, fake, fake, None, 256, 1, 1, 64, 1, 0.125, attn.ATTN_DTYPE_BF16, 1, fake,
            ctypes.c_size_t(-1).value, ctypes.byref(pipe), None)
     assert st == attn.ATTN_ERR_INVALID_ARG
+
+
+def declared_signatures():
+    """Parameter names of every function declared in include/*.h."""
+    sigs = {}
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if not f.endswith(".h"):
+            continue
+        src = open(os.path.join(ROOT, "include", f)).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        for name, params in re.findall(r"\b(attn_\w+)\s*\(([^)]*)\)\s*;", src):
+            names = [] if params.strip() in ("", "void") else \
+                [re.findall(r"(\w+)\s*$", p.strip())[0] for p in params.split(",")]
+            sigs[name] = names
+    return sigs
+
+
+# The core calls' minimal signatures, and what the header adds to them (each
+# addition explained in the header's "Signatures" note).
+MINIMAL = {
+    "attn_prefill": ["q", "k", "v", "o", "lse", "T", "h", "h_kv", "d_h", "causal", "scale", "dtype",
+                     "stream"],
+    "attn_decode_paged": ["q", "k_cache", "v_cache", "block_table", "seq_lens", "B", "h", "h_kv", "d_h",
+                          "page_size", "max_blocks_per_seq", "num_splits", "scale", "workspace",
+                          "workspace_bytes", "o", "lse", "stream"],
+    "attn_merge_states": ["o_part", "m_part", "l_part", "n_active", "rows", "num_splits", "d_h", "o", "lse",
+                          "out_dtype", "stream"],
+    "attn_decode_workspace_bytes": ["B", "h", "num_splits", "d_h"],
+    "attn_recommended_splits": ["B", "h_kv", "max_seq_len", "device"],
+    "attn_get_last_device_error": ["stream"],
+    "attn_status_string": ["status"],
+}
+ADDED = {"attn_prefill": ["workspace", "workspace_bytes"], "attn_decode_paged": ["num_blocks"]}
+
+
+def test_core_signatures_are_the_minimal_ones_plus_documented_additions():
+    sigs = declared_signatures()
+    for name, minimal in MINIMAL.items():
+        assert name in sigs, name
+        got = sigs[name]
+        extra = ADDED.get(name, [])
+        assert sorted(set(got) - set(minimal)) == sorted(extra), (name, got)
+        # the minimal parameters keep their order
+        assert [p for p in got if p not in extra] == minimal, (name, got)
+    # The header's note names exactly these additions, one entry per call:
+    # "<call>   <param>, <param> (after ...)".
+    note = open(os.path.join(ROOT, "include", "attn.h")).read().replace("\n *", " ")
+    for name, extra in ADDED.items():
+        m = re.search(rf"{name}\s+([\w, ]+?)\s*\(after", note)
+        assert m, name
+        assert [x.strip() for x in m.group(1).split(",")] == extra, (name, m.group(1))

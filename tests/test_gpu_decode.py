@@ -64,7 +64,7 @@ def test_decode_paged_batch_every_row(which):
     shape = W.DECODE_PAGED_B64
     q, kc, vc, table, seq = W.decode_inputs(shape, seed=0)
     lens = seq.tolist()
-    S = attn.attn_recommended_splits(len(lens), shape.h_kv, max(lens), sum(lens))
+    S = attn.attn_recommended_splits_ragged(len(lens), shape.h_kv, max(lens), sum(lens))
     if which == "other":
         S = S // 4 + 1
     o, lse = run_decode(q, kc, vc, table, seq, S)
@@ -82,7 +82,7 @@ def test_decode_paged_batch_full_size_sampled_rows():
     shape = W.DECODE_PAGED_B64
     q, kc, vc, table, seq = W.decode_inputs(shape, seed=0)
     lens = seq.tolist()
-    S = attn.attn_recommended_splits(len(lens), shape.h_kv, max(lens), sum(lens))
+    S = attn.attn_recommended_splits_ragged(len(lens), shape.h_kv, max(lens), sum(lens))
     o, lse = run_decode(q, kc, vc, table, seq, S)
     empty = [i for i, s in enumerate(lens) if s == 0]
     assert len(empty) == 2
@@ -158,3 +158,12 @@ def test_decode_max_split_count():
     assert attn.attn_get_device_error() == 0
     check_out(o, O_ref, torch.bfloat16)
     check_lse(lse, L_ref)
+
+
+def test_recommended_splits_reads_the_device():
+    """The device form equals the pure rule with that device's SM count and
+    no total length."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for B, h_kv, s in [(1, 8, 32768), (1, 1, 32768), (66, 8, 16384), (4, 8, 256)]:
+        assert attn.attn_recommended_splits(B, h_kv, s, 0) == \
+            attn.attn_recommended_splits_ragged(B, h_kv, s, 0, sms)

@@ -21,14 +21,14 @@ def _built():
 
 def expected_pps(lens, h_kv, max_splits):
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    s = attn.attn_recommended_splits(len(lens), h_kv, max(lens), sum(lens), sms)
+    s = attn.attn_recommended_splits_ragged(len(lens), h_kv, max(lens), sum(lens), sms)
     s = min(s, max_splits)
     max_pages = (max(lens) + 15) // 16
     return max(1, -(-max_pages // s))
 
 
 def plan_of(ws, B, h, d, max_splits):
-    off = attn.attn_decode_workspace_bytes(B, h, d, max_splits)
+    off = attn.attn_decode_workspace_bytes(B, h, max_splits, d)
     return int(ws[off:off + 4].view(torch.int32).item())
 
 
@@ -42,7 +42,7 @@ def test_adaptive_matches_oracle_and_host_rule(lens, max_splits):
     shape = W.DECODE_PAGED_B64
     q, kc, vc, table, seq = W.decode_inputs(shape, 8, seq_lens=lens)
     B = len(lens)
-    ws = torch.empty(attn.attn_decode_adaptive_workspace_bytes(B, shape.h, shape.d_h, max_splits),
+    ws = torch.empty(attn.attn_decode_adaptive_workspace_bytes(B, shape.h, max_splits, shape.d_h),
                      dtype=torch.uint8, device="cuda")
     o, lse = attn.attn_decode_paged_adaptive(q.cuda(), kc.cuda(), vc.cuda(), table.cuda(), seq.cuda(),
                                              max_splits, shape.scale, workspace=ws)
@@ -65,7 +65,7 @@ def test_graph_replay_adapts_to_new_lengths():
     B, S = len(lens_a), 48
     dq, dk, dv, dt = q.cuda(), kc.cuda(), vc.cuda(), table.cuda()
     seq = torch.tensor(lens_a, dtype=torch.int32, device="cuda")
-    ws = torch.empty(attn.attn_decode_adaptive_workspace_bytes(B, shape.h, shape.d_h, S),
+    ws = torch.empty(attn.attn_decode_adaptive_workspace_bytes(B, shape.h, S, shape.d_h),
                      dtype=torch.uint8, device="cuda")
     o = torch.empty_like(dq)
     lse = torch.empty(B, shape.h, device="cuda")

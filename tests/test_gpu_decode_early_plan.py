@@ -32,9 +32,9 @@ def decode_after_rewrite(q, kc, vc, table_dev, seq_dev, dst, src, S, scale, mode
     if mode == "deterministic":
         pps = 8
         n = -(-table_dev.shape[1] // pps)
-        ws = torch.empty(attn.attn_decode_workspace_bytes(B, h, d, n), dtype=torch.uint8, device="cuda")
+        ws = torch.empty(attn.attn_decode_workspace_bytes(B, h, n, d), dtype=torch.uint8, device="cuda")
     else:
-        ws = torch.empty(attn.attn_decode_workspace_bytes(B, h, d, S), dtype=torch.uint8, device="cuda")
+        ws = torch.empty(attn.attn_decode_workspace_bytes(B, h, S, d), dtype=torch.uint8, device="cuda")
     torch.cuda.synchronize()
     attn.attn_selftest_delayed_copy(dst, src, delay_us=50)
     if mode == "deterministic":

@@ -231,7 +231,7 @@ def test_caller_workspace_with_decode_part():
     q_lens, ctx = MIXED
     q, kc, vc, table, cu, seq = paged_batch(q_lens, ctx, h, h_kv, d, 5)
     B, mb = len(ctx), table.shape[1]
-    n = (attn.attn_prefill_paged_decode_workspace_bytes(B, h, d, 7) +
+    n = (attn.attn_prefill_paged_decode_workspace_bytes(B, h, 7, d) +
          attn.attn_prefill_paged_workspace_bytes(B, mb, h_kv, d, v16=True))
     ws = torch.full((n,), 0x7f, dtype=torch.uint8, device="cuda")
     o, lse = attn.attn_prefill_paged(q.cuda(), kc.cuda(), vc.cuda(), table.cuda(), cu.cuda(), seq.cuda(),
@@ -241,6 +241,6 @@ def test_caller_workspace_with_decode_part():
     check_out(o, O_ref, torch.bfloat16, "caller workspace with decode part")
     check_lse(lse, L_ref)
     with pytest.raises(attn.AttnError):  # one byte short of the decode part plus the small form
-        small = attn.attn_prefill_paged_decode_workspace_bytes(B, h, d, 7) + attn.attn_prefill_paged_workspace_bytes(B)
+        small = attn.attn_prefill_paged_decode_workspace_bytes(B, h, 7, d) + attn.attn_prefill_paged_workspace_bytes(B)
         attn.attn_prefill_paged(q.cuda(), kc.cuda(), vc.cuda(), table.cuda(), cu.cuda(), seq.cuda(),
                                 max(q_lens), True, workspace=ws[:small - 1], decode_splits=7)

@@ -53,7 +53,7 @@ def test_static_scratch_matches_workspace_entry_point_twice(lib):
     cases = [(0, [0, 1, 17, 300, 1000, 5000], 8), (1, [4000, 16, 0, 2500, 77], 3)]
     for seed, lens, S in cases:
         q, kc, vc, table, seq = (t.cuda() for t in W.decode_inputs(shape, seed=seed, seq_lens=lens))
-        assert attn.attn_decode_workspace_bytes(len(lens), shape.h, shape.d_h, S) <= SCRATCH_BYTES
+        assert attn.attn_decode_workspace_bytes(len(lens), shape.h, S, shape.d_h) <= SCRATCH_BYTES
         o_ref, lse_ref = attn.attn_decode_paged(q, kc, vc, table, seq, S, shape.scale)
         o = torch.full_like(q, float("nan"))
         lse = torch.full((len(lens), shape.h), float("nan"), device="cuda")
@@ -72,7 +72,7 @@ def test_static_scratch_refuses_oversized_request(lib):
     # 64 rows x 32 heads x 64 splits of partials need ~68 MB > 16 MiB: refused
     # on the host before any launch.
     B, h, h_kv, d, S = 64, 32, 8, 128, 64
-    assert attn.attn_decode_workspace_bytes(B, h, d, S) > SCRATCH_BYTES
+    assert attn.attn_decode_workspace_bytes(B, h, S, d) > SCRATCH_BYTES
     q = torch.zeros((B, h, d), dtype=torch.bfloat16, device="cuda")
     kc = torch.zeros((1, 16, h_kv, d), dtype=torch.bfloat16, device="cuda")
     table = torch.zeros((B, 1), dtype=torch.int32, device="cuda")
