@@ -49,20 +49,25 @@ KERNEL_FILES = {
                "online_softmax_attn_gb300/csrc/pdl.cuh"],
 }
 KERNEL_FILES["prefill_paged"] = KERNEL_FILES["prefill"]
+KERNEL_FILES["prefill_T2048"] = KERNEL_FILES["prefill"]
 KERNEL_FILES["merge_pair"] = ["online_softmax_attn_gb300/csrc/merge.cu", "online_softmax_attn_gb300/csrc/common.cuh",
                               "online_softmax_attn_gb300/csrc/pdl.cuh"]
 NCU_TRAFFIC = {
     # kind: (dram read + write bytes per launch, sha256[:16] of the kernel's files)
-    # prefill_bf16_kernel, causal T=8192 layer, full-size capture
-    "prefill": (135.65e6, "54c8b6f9626d119d"),
+    # prefill_bf16_kernel, causal T=8192 layer, full-size capture: 102.4 MB read
+    # (compulsory Q, K, fp16 V) + 33.6 MB of the 67.1 MB output written back by exit
+    "prefill": (136.06e6, "4b09c590f008c803"),
+    # prefill_bf16_kernel, causal T=2048 layer, full-size capture: the compulsory
+    # 25.2 MB read; the 16.8 MB output is still in L2 when the kernel exits
+    "prefill_T2048": (25.24e6, "4b09c590f008c803"),
     # prefill_bf16_kernel (paged), 8 rows x 1024 queries over 8192 keys, full-size capture
-    "prefill_paged": (465.07e6, "54c8b6f9626d119d"),
-    # decode_split_kernel: a 16-row capture (303.7 MB for 299.5 MB algorithmic) scaled by
+    "prefill_paged": (467.01e6, "4b09c590f008c803"),
+    # decode_split_kernel: a 16-row capture (303.9 MB for 299.5 MB algorithmic) scaled by
     # the KV bytes to the 66-row batch
-    "decode": (2.1496e9, "c43dc21389d4e5ce"),
+    "decode": (2.1517e9, "c7756d32f7037510"),
     # merge_pair_kernel, 262144 rows x 128 bf16, full-size capture: reads are the compulsory
-    # 136.3 MB, writes 38.2 MB of the 68.2 MB output (the rest still in L2 at exit)
-    "merge_pair": (174.55e6, "054155b75fe86019"),
+    # 136.3 MB, writes 37.4 MB of the 68.2 MB output (the rest still in L2 at exit)
+    "merge_pair": (173.73e6, "1d1116a09f523c2d"),
 }
 
 
@@ -363,6 +368,13 @@ def run_gpu(args, world, rank, local):
         res = measure_decode_batch1(dev, hbm_peak, peak_kind)
         if rank == 0:
             print(json.dumps({"only": "decode_batch1", "decode_batch1": res}), flush=True)
+        return
+    if args.only == "prefill_t2048":
+        # The T=2048 layer's measurement alone (profiler captures).
+        flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+        res = measure_prefill_t2048(dev, flush, tc_peak, peak_kind, iters=max(1, args.steps))
+        if rank == 0:
+            print(json.dumps({"only": "prefill_t2048", "prefill_T2048": res}), flush=True)
         return
     if args.only == "mixed":
         flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
@@ -861,7 +873,8 @@ def measure_prefill_t2048(dev, flush, tc_peak, peak_kind, iters=15):
             "timing": f"CUDA graph of {n} calls", "event_single_call_us": t_ev * 1e3,
             "event_single_call_tflops": flops / (t_ev * 1e-3) / 1e12,
             "roofline": {"bound": "tensor", "achieved": tf, "peak": tc_peak, "unit": "TFLOP/s",
-                         "frac": tf / tc_peak, "traffic": None, "kernel": "prefill_bf16_kernel",
+                         "frac": tf / tc_peak, "traffic": traffic_for("prefill_T2048"),
+                         "kernel": "prefill_bf16_kernel",
                          "peak_source": f"{peak_kind} bf16 burst"}}
 
 
@@ -995,7 +1008,7 @@ def main():
                     help="skip the measurements outside the step (deterministic / adaptive decode, "
                          "pair merge, paged prefill), e.g. for a launch list of the step alone")
     ap.add_argument("--only", choices=["prefill", "decode", "prefill_paged", "merge_pair", "decode_batch1",
-                                       "mixed"],
+                                       "mixed", "prefill_t2048"],
                     default=None,
                     help="run one half of the step, or the paged prefill or pair merge measurement "
                          "alone (profiler captures; not a bench line)")
