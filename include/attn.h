@@ -93,8 +93,9 @@ int attn_version(void);
 
 /*
  * attn_prefill_workspace_bytes -- scratch attn_prefill can use for the given
- * shape: an fp16 copy of V ([h_kv, T, d_h]) and one int per (KV head, 128-key
- * tile) saying whether that tile fits fp16. Host-only, pure. 0 for
+ * shape: an fp16 copy of V ([h_kv, T, d_h]), one int per (KV head, 128-key
+ * tile) saying whether that tile fits fp16, and 256 bytes holding the
+ * counter from which the attention kernel's CTAs claim work. Host-only, pure. 0 for
  * ATTN_DTYPE_F32 (the SIMT path needs none) and for T == 0; (size_t)-1 on
  * invalid arguments (T < 0, h_kv < 1, d_h not 64 or 128, unknown dtype).
  */

@@ -84,7 +84,7 @@ cudaError_t launch_prefill_f32(const float* q, const float* k, const float* v, f
 // Workspace carve-up: fp16 copy of V [h_kv, T, d_h], then one int flag per
 // (KV head, 128-key tile).
 struct PrefillLayout {
-  size_t v16_off, flags_off, total;
+  size_t v16_off, flags_off, sched_off, total;
 };
 PrefillLayout prefill_layout(int T, int h_kv, int d_h);
 // workspace == nullptr: every key tile takes the exact bf16 P_hi + P_lo path.

@@ -16,12 +16,14 @@
 // stored, in the registers S held. O = O~ / l and LSE are independent of the
 // reference.
 //
-// GB300 design (one CTA per (KV head, 128-query block, pair of query heads)):
+// GB300 design (work item: a 128-query block of a pair of query heads that
+// share a KV head; contiguous rows run a persistent grid of one CTA per SM,
+// paged rows one CTA per item):
 //   * softmax warpgroups (warps 0-3, 4-7), one per query head; thread = row
 //     (tensor-memory lane), so row sums and maxima need no shuffles. P is
 //     written over the first columns of its own S tile: fp16 for a V tile
 //     that converts to fp16 exactly, else bf16 P_hi and P_lo.
-//   * control warpgroup: warp 8 is the TMA producer (Q of both heads once,
+//   * control warpgroup: warp 8 is the TMA producer (Q of both heads per item,
 //     then K and V of the shared KV head through rings of their own, 128-byte
 //     swizzle, 64-element boxes); warp 9 allocates tensor memory and issues
 //     the MMAs as a whole warp (elect.sync picks the issuing lane):
@@ -32,10 +34,17 @@
 //     fp16 cannot carry; flagged tiles are read as bf16 and take P_hi + P_lo.
 //   The two heads ping-pong: while one warpgroup exponentiates its S tile,
 //   the tensor core runs the other head's P V and next Q K^T.
-//   Causal CTAs visit only key tiles up to the diagonal (the masked half of
-//   the FLOPs is skipped) and the grid runs the longest query blocks first.
+//   Causal items visit only key tiles up to the diagonal (the masked half of
+//   the FLOPs is skipped); the longest query blocks are handed out first.
+//   A persistent CTA claims its next item as it issues the current one's last
+//   loads, loads the next Q once the current item's last S MMA is done, and
+//   runs the next item's first S MMAs while its softmax warps store O (staged
+//   in two V stages, not in Q), so set-up and drain overlap work.
 //   Every mbarrier wait is bounded; on a timeout the CTA raises the error
 //   word, drains its copies and MMAs (bounded), frees tensor memory and exits.
+#include <climits>
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.h"
 #include "pdl.cuh"
@@ -71,10 +80,12 @@ struct PfCfg {
   static constexpr int V_OFF = K_OFF + NSK * KTILE;
   static constexpr int BAR_OFF = V_OFF + NSV * KTILE;
   // q_full, k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV], s_full[NQ],
-  // p_full[NQ], o_final[NQ], mma_done
-  static constexpr int NBAR = 1 + 2 * NSK + 2 * NSV + 3 * NQ + 1;
-  static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;  // tensor-memory slot, abort flag, tail tile
-  static constexpr int SMEM = MISC_OFF + 16 + 1024;    // + alignment slack
+  // p_full[NQ], o_final[NQ], mma_done, q_empty, stage_free[2], item_full[2]
+  static constexpr int NBAR = 1 + 2 * NSK + 2 * NSV + 3 * NQ + 1 + 5;
+  static_assert(NSV >= 3, "the epilogue stages O in two V stages the next item does not load first");
+  // tensor-memory slot, abort flag, tail tile (2 ints), item slots (2 ints)
+  static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
+  static constexpr int SMEM = MISC_OFF + 32 + 1024;  // + alignment slack
   static constexpr int TMEM_COLS = NQ == 1 ? 256 : 512;
   // NQ softmax warpgroups + one control warpgroup (TMA warp, MMA warp, two
   // idle warps: setmaxnreg moves registers per whole warpgroup).
@@ -82,12 +93,13 @@ struct PfCfg {
   static constexpr int PRODUCER_WARP = NQ * 4;
   static constexpr int MMA_WARP = NQ * 4 + 1;
   // Register split (NQ = 2): launched at 168/thread (384 x 168 = 64512);
-  // control warpgroup drops to 112, softmax warpgroups rise to 192:
-  // 2 x 128 x 192 + 128 x 112 = 63488 <= 64512. (With the O~ rescale after
-  // the P store the softmax fits 192; 88 registers spilled in the control
-  // warps.)
+  // control warpgroup drops to 120, softmax warpgroups rise to 192:
+  // 2 x 128 x 192 + 128 x 120 = 64512, the whole launch allocation. (With
+  // the O~ rescale after the P store the softmax fits 192; 88 registers
+  // spilled in the control warps, and 112 spilled a few words once the
+  // producer claimed items.)
   static constexpr int REG_LAUNCH = 168;
-  static constexpr int REG_CONTROL = 112;
+  static constexpr int REG_CONTROL = 120;
   static constexpr int REG_SOFTMAX = 192;
   static_assert(NQ != 2 || 2 * 128 * REG_SOFTMAX + 128 * REG_CONTROL <= THREADS * REG_LAUNCH,
                 "register split exceeds the launch allocation");
@@ -152,6 +164,18 @@ struct Bars {
     return base + 8 * (1 + 2 * nsk + 2 * nsv + 2 * nq + t);
   }
   __device__ uint32_t mma_done() const { return base + 8 * (1 + 2 * nsk + 2 * nsv + 3 * nq); }
+  // Q's shared memory is free: the item's last S MMA has completed.
+  __device__ uint32_t q_empty() const { return base + 8 * (2 + 2 * nsk + 2 * nsv + 3 * nq); }
+  // An item's O rows have left the V stages they were staged in; items
+  // alternate between the two barriers.
+  __device__ uint32_t stage_free(int i) const {
+    return base + 8 * (3 + 2 * nsk + 2 * nsv + 3 * nq + i);
+  }
+  // The producer has written the index of the CTA's next item (or -1: none
+  // left) into item slot i; items alternate between the two.
+  __device__ uint32_t item_full(int i) const {
+    return base + 8 * (5 + 2 * nsk + 2 * nsv + 3 * nq + i);
+  }
 };
 
 // Bounded wait that also gives up at once when another role has aborted.
@@ -186,6 +210,86 @@ struct PagedArgs {
   int max_tiles;  // 128-key tiles per row in the fp16 V copy: ceil(max_blocks / 8)
 };
 
+// One work item: a 128-query block of NQ query heads that share a KV head.
+struct Work {
+  int hq0;       // first query head
+  int kvh;       // their KV head
+  int qb;        // query block (paged rows: the block within row pb)
+  int nkv;       // key tiles the block visits
+  int n_kv_all;  // key tiles of the KV head (contiguous) or row (paged)
+  int pb, q_tok0, q_len, ctx, n_pages;  // paged rows only
+};
+
+// P of a key tile whose V stays bf16 (a value of magnitude 2^16 or more, an
+// inf or a NaN): P = P_hi + P_lo, both bf16, P_hi in columns 0-63 of the S
+// tile and P_lo in columns 64-127. Such tiles are rare, so this runs out of
+// line, which keeps the softmax loop's code small. It reads the S tile again
+// from tensor memory (the caller's registers hold it only up to the row max),
+// masks keys from lim on to -inf as the caller did, and returns the row sum of
+// the weights, added up in the same order as the fp16 path. Warp-collective.
+__device__ __noinline__ float softmax_p_two_term(uint32_t tS, int lim, float scale_log2,
+                                                 float bias) {
+  uint32_t sr[4][32];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) tc::ld32(tS + c * 32, sr[c]);
+  tc::wait_ld();
+  if (lim < kBN) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (c * 32 + i >= lim) sr[c][i] = __float_as_uint(-INFINITY);
+  }
+  const uint64_t c2 = f2(scale_log2, scale_log2);
+  const uint64_t nb2 = f2(-bias, -bias);
+  uint64_t sumA = f2(0.f, 0.f), sumB = f2(0.f, 0.f);
+  // P = P_hi + P_lo, both bf16. P_hi is p truncated to bf16 (its upper
+  // 16 bits), P_lo = bf16(p - P_hi) (the difference is exact in fp32),
+  // so the pair carries ~16 significant bits (a single bf16 P costs up
+  // to 2^-8 relative per weight, which rows dominated by a few keys do
+  // not average away). Within chunk c, sr[c][2i] is reused for the
+  // P_hi pair of keys (2i, 2i+1), sr[c][2i+1] for P_lo.
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float y0, y1;
+      unf2(fma2(f2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])), c2,
+                nb2),
+           y0, y1);
+      const float p0 = ex2_approx(y0);
+      const float p1 = ex2_approx(y1);
+      const uint64_t pp = f2(p0, p1);
+      if (i & 1) sumB = add2(sumB, pp); else sumA = add2(sumA, pp);
+      const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
+      uint32_t hi;
+      asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(hi) : "r"(u0), "r"(u1));
+      float d0, d1;
+      unf2(sub2(pp, f2(__uint_as_float(u0 & 0xffff0000u), __uint_as_float(u1 & 0xffff0000u))),
+           d0, d1);
+      sr[c][2 * i] = hi;
+      sr[c][2 * i + 1] = pack_bf16x2(d0, d1);
+    }
+  }
+  // P_hi fills columns 0-63 and P_lo columns 64-127.
+  uint32_t hi[32], lo[32];
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        hi[16 * c + i] = sr[2 * half + c][2 * i];
+        lo[16 * c + i] = sr[2 * half + c][2 * i + 1];
+      }
+    tc::st32(tS + 32 * half, hi);       // P_hi keys 64*half .. +63
+    tc::st32(tS + 64 + 32 * half, lo);  // P_lo keys 64*half .. +63
+  }
+  float sa0, sa1;
+  unf2(add2(sumA, sumB), sa0, sa1);
+  return sa0 + sa1;
+}
+
 // PAGED: variable-length rows over a paged cache. PCOPY (paged only): V is
 // read from the workspace copy that paged_v_to_f16_kernel made (fp16 bits
 // for normal tiles, bf16 bits for flagged ones), else from the cache itself.
@@ -196,7 +300,8 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
                         const __grid_constant__ CUtensorMap tmap_v,
                         const __grid_constant__ CUtensorMap tmap_v16,
                         const int* __restrict__ vwide, __nv_bfloat16* __restrict__ o, float* __restrict__ lse, int T, int h,
-                        int h_kv, int causal, float scale_log2, int n_qblk, const PagedArgs pa) {
+                        int h_kv, int causal, float scale_log2, int n_qblk,
+                        int* __restrict__ sched, const PagedArgs pa) {
   using C = PfCfg<D, NQ, NSK, NSV>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -210,16 +315,28 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
   // within the tile and the number of such slots up to the page's end. Kept
   // in shared memory so that no warp holds registers for it.
   int* tail_info = reinterpret_cast<int*>(smem + C::MISC_OFF + 8);
+  volatile int* item_slot = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 16);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // Grid (head pairs, query tiles): the block scheduler walks x fastest, so
-  // every head pair's longest query tile starts before any shorter one.
-  const int hq0 = blockIdx.x * NQ;
-  const int kvh = hq0 / (h / h_kv);
-  int qb, nkv, n_kv_all;
-  // Paged rows: the row, its first query token, query count and key count.
-  int pb = 0, q_tok0 = 0, q_len = 0, ctx = 0, n_pages = 0;
+  const int n_hp = h / NQ;
+  // Work items. Contiguous rows: the grid is persistent (one CTA per SM at
+  // most); item i is head group i % n_hp of the query block with the
+  // (i / n_hp)-th most key tiles (causal: the longest blocks first). CTA c
+  // starts with item c; the producer claims each next item from the counter
+  // *sched (the V pass zeroes it), which hands out G, G + 1, ... in order, so
+  // the CTA that runs out of work first takes the longest item left. Without
+  // a counter the CTA takes round r's item c (rounds of G = gridDim.x items)
+  // when r is even and item G - 1 - c when r is odd. The producer publishes
+  // each item in an item slot; the other roles read it there. Paged rows:
+  // one item, the CTA's own (grid: head groups x the rows' query tiles, each
+  // row's longest tile first).
+  const int G = PAGED ? 1 : int(gridDim.x);
+  const int n_items = PAGED ? 1 : n_hp * n_qblk;
+  auto item_of_round = [&](int rr) {
+    return rr * G + ((rr & 1) ? G - 1 - int(blockIdx.x) : int(blockIdx.x));
+  };
+  Work pw{};
   if constexpr (PAGED) {
     const int tile = int(blockIdx.y);
     if (tile >= pa.tile_off[pa.B]) return;  // surplus CTA of the fixed grid
@@ -228,44 +345,78 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
       const int mid = (lo + hi + 1) >> 1;
       if (pa.tile_off[mid] <= tile) lo = mid; else hi = mid - 1;
     }
-    pb = lo;
-    qb = pa.tile_off[pb + 1] - 1 - tile;  // longest tile of the row first
-    q_tok0 = pa.cu_q[pb];
-    q_len = pa.cu_q[pb + 1] - q_tok0;
-    ctx = pa.seq_lens[pb];
-    if (ctx < q_len || ctx > pa.max_blocks * 16) {
+    pw.hq0 = int(blockIdx.x) * NQ;
+    pw.kvh = pw.hq0 / (h / h_kv);
+    pw.pb = lo;
+    pw.qb = pa.tile_off[lo + 1] - 1 - tile;  // longest tile of the row first
+    pw.q_tok0 = pa.cu_q[lo];
+    pw.q_len = pa.cu_q[lo + 1] - pw.q_tok0;
+    int ctx = pa.seq_lens[lo];
+    if (ctx < pw.q_len || ctx > pa.max_blocks * 16) {
       if (threadIdx.x == 0) atomicOr(&g_prefill_err, ATTN_DEVERR_BAD_SEQ_LEN);
-      ctx = ctx < q_len ? q_len : pa.max_blocks * 16;
+      ctx = ctx < pw.q_len ? pw.q_len : pa.max_blocks * 16;
     }
-    n_pages = (ctx + 15) / 16;
-    const int q_hi = min(qb * kBM + kBM, q_len);  // end of this tile's queries
-    const int key_end = causal ? ctx - q_len + q_hi : ctx;
-    nkv = (key_end + kBN - 1) / kBN;
-    n_kv_all = nkv;
-  } else {
-    qb = causal ? (n_qblk - 1 - int(blockIdx.y)) : int(blockIdx.y);
-    n_kv_all = (T + kBN - 1) / kBN;
-    nkv = causal ? min(qb + 1, n_kv_all) : n_kv_all;
+    pw.ctx = ctx;
+    pw.n_pages = (ctx + 15) / 16;
+    const int q_hi = min(pw.qb * kBM + kBM, pw.q_len);  // end of this tile's queries
+    const int key_end = causal ? ctx - pw.q_len + q_hi : ctx;
+    pw.nkv = (key_end + kBN - 1) / kBN;
+    pw.n_kv_all = pw.nkv;
   }
-  // Per key tile of this KV head: nonzero -> V stays bf16 (exact P_hi + P_lo
+  auto work_at = [&](int i) -> Work {
+    if constexpr (PAGED) {
+      return pw;
+    } else {
+      Work w{};
+      const int hp = i % n_hp;
+      const int rank = i / n_hp;
+      w.hq0 = hp * NQ;
+      w.kvh = w.hq0 / (h / h_kv);
+      w.qb = causal ? (n_qblk - 1 - rank) : rank;
+      w.n_kv_all = (T + kBN - 1) / kBN;
+      w.nkv = causal ? min(w.qb + 1, w.n_kv_all) : w.n_kv_all;
+      return w;
+    }
+  };
+  // Per key tile of a KV head: nonzero -> V stays bf16 (exact P_hi + P_lo
   // product); zero -> V is read from its fp16 copy (fp16 P). No flags: all
   // tiles bf16. Paged rows: flags [B, h_kv, max_tiles].
-  const int* tile_wide =
-      !vwide ? nullptr
-             : vwide + (PAGED ? (size_t(pb) * h_kv + kvh) * pa.max_tiles : size_t(kvh) * n_kv_all);
-  auto is_wide = [&](int j) { return tile_wide ? (__ldg(tile_wide + j) != 0) : true; };
+  auto wide_flags = [&](const Work& w) -> const int* {
+    return !vwide ? nullptr
+                  : vwide + (PAGED ? (size_t(w.pb) * h_kv + w.kvh) * pa.max_tiles
+                                   : size_t(w.kvh) * w.n_kv_all);
+  };
+  auto is_wide = [&](const int* tile_wide, int j) {
+    return tile_wide ? (__ldg(tile_wide + j) != 0) : true;
+  };
+  // The flags of key tiles j0 .. j0 + 31 (below n) as one bit each, for a
+  // whole warp: one load per lane every 32 tiles instead of a load on every
+  // tile's path to its MMAs and exponentials. Warp-collective.
+  auto wide_bits = [&](const int* tile_wide, int j0, int n) -> uint32_t {
+    if (!tile_wide) return 0xffffffffu;
+    const int jj = j0 + (threadIdx.x & 31);
+    return __ballot_sync(0xffffffffu, jj < n && __ldg(tile_wide + jj) != 0);
+  };
+  // Whether any of key tiles 0 .. n-1 is wide. Warp-collective.
+  auto item_has_wide = [&](const int* tile_wide, int n) -> bool {
+    uint32_t any = 0;
+    for (int j0 = 0; j0 < n; j0 += 32) any |= wide_bits(tile_wide, j0, n);
+    return any != 0;
+  };
 
   if (threadIdx.x == 0) {
-    // p_full collects one arrival per softmax thread; the others take one.
+    // p_full collects one arrival per softmax thread, stage_free one per
+    // softmax warp; the others take one.
     for (int i = 0; i < C::NBAR; ++i) {
       const uint32_t bar = bars.base + 8 * i;
       const bool is_p = bar >= bars.p_full(0) && bar < bars.p_full(0) + 8 * NQ;
-      mbar_init(bar, is_p ? 128u : 1u);
+      const bool is_stage = bar == bars.stage_free(0) || bar == bars.stage_free(1);
+      mbar_init(bar, is_p ? 128u : is_stage ? uint32_t(NQ * 4) : 1u);
     }
     *abort_flag = 0;
     if constexpr (PAGED && !PCOPY) {
-      tail_info[0] = ctx % 16 != 0 ? ctx / kBN : -1;
-      tail_info[1] = (ctx % kBN) | ((16 - ctx % 16) << 8);
+      tail_info[0] = pw.ctx % 16 != 0 ? pw.ctx / kBN : -1;
+      tail_info[1] = (pw.ctx % kBN) | ((16 - pw.ctx % 16) << 8);
     }
     fence_barrier_init();
   }
@@ -274,6 +425,18 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Item it of this CTA as the producer published it: -1 when none is left,
+  // -2 on an abort. Warp-uniform (the wait's outcome is).
+  auto next_item = [&](int it) -> int {
+    if constexpr (PAGED) {
+      return it == 0 ? 0 : -1;
+    } else {
+      if (!__all_sync(0xffffffffu,
+                      wait_or_abort(bars.item_full(it & 1), (it >> 1) & 1, abort_flag)))
+        return -2;
+      return __shfl_sync(0xffffffffu, item_slot[it & 1], 0);
+    }
+  };
 
   // Register shares move per warpgroup: every warp of a warpgroup executes
   // the same setmaxnreg, at the top of its role's code.
@@ -285,88 +448,155 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
       prefetch_tmap(&tmap_q);
       prefetch_tmap(&tmap_k);
       prefetch_tmap(&tmap_v);
-      if (tile_wide) prefetch_tmap(&tmap_v16);
-      mbar_arrive_expect_tx(bars.q_full(), NQ * C::QTILE);
-      for (int t = 0; t < NQ; ++t)
-        for (int s = 0; s < C::SUBS; ++s) {
-          if constexpr (PAGED)
-            tma_load_3d(sbase + C::Q_OFF + t * C::QTILE + s * C::SUB_BYTES, &tmap_q, bars.q_full(),
-                        s * 64, hq0 + t, q_tok0 + qb * kBM);
-          else
-            tma_load_3d(sbase + C::Q_OFF + t * C::QTILE + s * C::SUB_BYTES, &tmap_q, bars.q_full(),
-                        s * 64, qb * kBM, hq0 + t);
+      if (vwide) prefetch_tmap(&tmap_v16);
+      // Loads issued so far (K and V tiles counted over all of this CTA's
+      // items: tile g uses stage g % NS, phase (g / NS) & 1).
+      int k_issued = 0, v_issued = 0, q_issued = 0;
+      // An item's epilogue stages O in the V stages of its last two tiles;
+      // the load of V tile (its last tile + 2) is the first to reuse one, so
+      // it waits for that item's stage_free. stage_waited items have been
+      // waited for; the last tiles of the (at most two) others are kept.
+      int stage_waited = 0, gl_even = 0, gl_odd = 0;
+      int g0 = 0, it = 0, rr = 0;
+      bool ok = true;
+      int cur = PAGED ? 0 : int(blockIdx.x);  // this item (grid size <= n_items)
+      for (;; ++it) {
+        if constexpr (!PAGED) {
+          // Q of the next item once the last S MMA of the previous one is
+          // done; that S also follows every role's read of item slot
+          // (it & 1) for item it - 2, so the slot can take item it.
+          if (it > 0 && !wait_or_abort(bars.q_empty(), (it - 1) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          item_slot[it & 1] = cur;
+          mbar_arrive(bars.item_full(it & 1));
         }
-      // Paged rows: the 8 pages of key tile j (a page past the row's end, or
-      // an invalid entry, is read at coordinate -1 and arrives as zeros).
-      int pg[8];
-      auto fetch_pages = [&](int j) {
-        if constexpr (PAGED) {
+        if (cur < 0) break;
+        const Work w = work_at(cur);
+        const int* tile_wide = wide_flags(w);
+        mbar_arrive_expect_tx(bars.q_full(), NQ * C::QTILE);
+        for (int t = 0; t < NQ; ++t)
+          for (int s = 0; s < C::SUBS; ++s) {
+            if constexpr (PAGED)
+              tma_load_3d(sbase + C::Q_OFF + t * C::QTILE + s * C::SUB_BYTES, &tmap_q,
+                          bars.q_full(), s * 64, w.hq0 + t, w.q_tok0 + w.qb * kBM);
+            else
+              tma_load_3d(sbase + C::Q_OFF + t * C::QTILE + s * C::SUB_BYTES, &tmap_q,
+                          bars.q_full(), s * 64, w.qb * kBM, w.hq0 + t);
+          }
+        q_issued = it + 1;
+        // Paged rows: the 8 pages of key tile j (a page past the row's end, or
+        // an invalid entry, is read at coordinate -1 and arrives as zeros).
+        int pg[8];
+        auto fetch_pages = [&](int j) {
+          if constexpr (PAGED) {
 #pragma unroll
-          for (int p = 0; p < 8; ++p) {
-            const int page = j * 8 + p;
-            int phys = -1;
-            if (page < n_pages) {
-              phys = pa.block_table[size_t(pb) * pa.max_blocks + page];
-              if (phys < 0 || phys >= pa.num_blocks) {
-                atomicOr(&g_prefill_err, ATTN_DEVERR_BAD_PAGE);
-                phys = -1;
+            for (int p = 0; p < 8; ++p) {
+              const int page = j * 8 + p;
+              int phys = -1;
+              if (page < w.n_pages) {
+                phys = pa.block_table[size_t(w.pb) * pa.max_blocks + page];
+                if (phys < 0 || phys >= pa.num_blocks) {
+                  atomicOr(&g_prefill_err, ATTN_DEVERR_BAD_PAGE);
+                  phys = -1;
+                }
               }
+              pg[p] = phys;
             }
-            pg[p] = phys;
+          }
+        };
+        auto load_tile = [&](uint32_t dst, const CUtensorMap* map, uint32_t bar, int j) {
+          if constexpr (PAGED) {
+#pragma unroll
+            for (int s = 0; s < C::SUBS; ++s)
+#pragma unroll
+              for (int p = 0; p < 8; ++p)
+                tma_load_4d(dst + s * C::SUB_BYTES + p * 16 * 128, map, bar, s * 64, w.kvh, 0,
+                            pg[p]);
+          } else {
+            for (int s = 0; s < C::SUBS; ++s)
+              tma_load_3d(dst + s * C::SUB_BYTES, map, bar, s * 64, j * kBN, w.kvh);
+          }
+        };
+        // K and V have rings of their own: a K stage frees as soon as the last
+        // head's S MMA on it completes, a V stage after the last P V MMA.
+        for (int j = 0; j < w.nkv; ++j) {
+          const int g = g0 + j;
+          const int sk = g % NSK, sv = g % NSV;
+          fetch_pages(j);
+          if (g >= NSK && !wait_or_abort(bars.k_empty(sk), ((g / NSK) - 1) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bars.k_full(sk), C::KTILE);
+          load_tile(sbase + C::K_OFF + sk * C::KTILE, &tmap_k, bars.k_full(sk), j);
+          k_issued = g + 1;
+          if (g >= NSV && !wait_or_abort(bars.v_empty(sv), ((g / NSV) - 1) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          while (!PAGED && ok && stage_waited < it &&
+                 ((stage_waited & 1) ? gl_odd : gl_even) + 2 <= g) {
+            ok = wait_or_abort(bars.stage_free(stage_waited & 1), (stage_waited >> 1) & 1,
+                               abort_flag);
+            ++stage_waited;
+          }
+          if (!ok) break;
+          // Q and K are older than the V pass, so they load before this wait;
+          // the fp16 V copy and the tile flags are the V pass's output.
+          if (g == 0) pdl_wait();
+          mbar_arrive_expect_tx(bars.v_full(sv), C::KTILE);
+          if (PAGED && PCOPY) {
+            // The row's copy is token-contiguous: one 128-token box per
+            // 64-element column block instead of one box per page. It holds
+            // fp16 bits, or bf16 bits for a flagged tile (a byte copy: the map's
+            // fp16 type only sets the element size).
+            const int tok = w.pb * pa.max_tiles * kBN + j * kBN;
+            for (int s = 0; s < C::SUBS; ++s)
+              tma_load_3d(sbase + C::V_OFF + sv * C::KTILE + s * C::SUB_BYTES, &tmap_v16,
+                          bars.v_full(sv), s * 64, w.kvh, tok);
+          } else {
+            load_tile(sbase + C::V_OFF + sv * C::KTILE,
+                      is_wide(tile_wide, j) ? &tmap_v : &tmap_v16, bars.v_full(sv), j);
+          }
+          v_issued = g + 1;
+        }
+        if (!ok) break;
+        if (it & 1) gl_odd = g0 + w.nkv - 1; else gl_even = g0 + w.nkv - 1;
+        g0 += w.nkv;
+        // The next item, claimed as this one's loads are all issued (a few
+        // key tiles before it ends); its Q and first K tile go to L2 now, so
+        // that its Q load, issued once this item's last S MMA is done, is
+        // served from there.
+        if constexpr (PAGED) {
+          cur = -1;
+        } else {
+          int nxt;
+          if (sched != nullptr) {
+            nxt = G + atomicAdd(sched, 1);
+          } else {
+            ++rr;
+            nxt = rr * G < n_items ? item_of_round(rr) : n_items;
+          }
+          cur = nxt < n_items ? nxt : -1;
+          if (cur >= 0) {
+            const Work wn = work_at(cur);
+            for (int t = 0; t < NQ; ++t)
+              for (int s = 0; s < C::SUBS; ++s)
+                tma_prefetch_l2_3d(&tmap_q, s * 64, wn.qb * kBM, wn.hq0 + t);
+            for (int s = 0; s < C::SUBS; ++s) tma_prefetch_l2_3d(&tmap_k, s * 64, 0, wn.kvh);
           }
         }
-      };
-      auto load_tile = [&](uint32_t dst, const CUtensorMap* map, uint32_t bar, int j) {
-        if constexpr (PAGED) {
-#pragma unroll
-          for (int s = 0; s < C::SUBS; ++s)
-#pragma unroll
-            for (int p = 0; p < 8; ++p)
-              tma_load_4d(dst + s * C::SUB_BYTES + p * 16 * 128, map, bar, s * 64, kvh, 0, pg[p]);
-        } else {
-          for (int s = 0; s < C::SUBS; ++s)
-            tma_load_3d(dst + s * C::SUB_BYTES, map, bar, s * 64, j * kBN, kvh);
-        }
-      };
-      // K and V have rings of their own: a K stage frees as soon as the last
-      // head's S MMA on it completes, a V stage after the last P V MMA.
-      int k_issued = 0, v_issued = 0;
-      for (int j = 0; j < nkv; ++j) {
-        const int sk = j % NSK, sv = j % NSV;
-        fetch_pages(j);
-        if (j >= NSK && !wait_or_abort(bars.k_empty(sk), ((j / NSK) - 1) & 1, abort_flag)) break;
-        mbar_arrive_expect_tx(bars.k_full(sk), C::KTILE);
-        load_tile(sbase + C::K_OFF + sk * C::KTILE, &tmap_k, bars.k_full(sk), j);
-        k_issued = j + 1;
-        if (j >= NSV && !wait_or_abort(bars.v_empty(sv), ((j / NSV) - 1) & 1, abort_flag)) break;
-        // Q and K are older than the V pass, so they load before this wait;
-        // the fp16 V copy and the tile flags are the V pass's output.
-        if (j == 0) pdl_wait();
-        mbar_arrive_expect_tx(bars.v_full(sv), C::KTILE);
-        const bool v_wide = is_wide(j);
-        if (PAGED && PCOPY) {
-          // The row's copy is token-contiguous: one 128-token box per
-          // 64-element column block instead of one box per page. It holds
-          // fp16 bits, or bf16 bits for a flagged tile (a byte copy: the map's
-          // fp16 type only sets the element size).
-          const int tok = pb * pa.max_tiles * kBN + j * kBN;
-          for (int s = 0; s < C::SUBS; ++s)
-            tma_load_3d(sbase + C::V_OFF + sv * C::KTILE + s * C::SUB_BYTES, &tmap_v16,
-                        bars.v_full(sv), s * 64, kvh, tok);
-        } else {
-          load_tile(sbase + C::V_OFF + sv * C::KTILE, v_wide ? &tmap_v : &tmap_v16, bars.v_full(sv),
-                    j);
-        }
-        v_issued = j + 1;
       }
       if (*abort_flag) {
         // Drain: the newest load of each stage is the only one that can still
         // be in flight. Bounded waits, error already recorded.
-        (void)mbar_wait(bars.q_full(), 0, &g_prefill_err);
-        for (int j = max(0, k_issued - NSK); j < k_issued; ++j)
-          (void)mbar_wait(bars.k_full(j % NSK), (j / NSK) & 1, &g_prefill_err);
-        for (int j = max(0, v_issued - NSV); j < v_issued; ++j)
-          (void)mbar_wait(bars.v_full(j % NSV), (j / NSV) & 1, &g_prefill_err);
+        if (q_issued > 0) (void)mbar_wait(bars.q_full(), (q_issued - 1) & 1, &g_prefill_err);
+        for (int g = max(0, k_issued - NSK); g < k_issued; ++g)
+          (void)mbar_wait(bars.k_full(g % NSK), (g / NSK) & 1, &g_prefill_err);
+        for (int g = max(0, v_issued - NSV); g < v_issued; ++g)
+          (void)mbar_wait(bars.v_full(g % NSV), (g / NSV) & 1, &g_prefill_err);
       }
     }
   } else if (warp == C::MMA_WARP) {
@@ -419,38 +649,65 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
       auto wait = [&](uint32_t bar, uint32_t parity) {
         return __all_sync(0xffffffffu, wait_or_abort(bar, parity, abort_flag));
       };
-      bool ok = wait(bars.q_full(), 0) && wait(bars.k_full(0), 0);
-      if (ok) {
-        tc::fence_after();
-        for (int t = 0; t < NQ; ++t) {
-          issue_s(t, 0);
-          tc::commit_elect(bars.s_full(t));
-        }
-        tc::commit_elect(bars.k_empty(0));
-      }
       // Order per key tile j: P_0 V_j, S_0(j+1), P_1 V_j, S_1(j+1): each head's
       // next QK^T follows its own P V (P aliases S in tensor memory), and the
-      // other head's softmax runs while these MMAs execute.
-      pdl_wait();  // the tile flags below are the V pass's output
-      for (int j = 0; ok && j < nkv; ++j) {
-        const int sv = j % NSV;
-        const int sk1 = (j + 1) % NSK;
-        const bool wide = is_wide(j);
-        for (int t = 0; t < NQ && ok; ++t) {
-          if (!wait(bars.p_full(t), j & 1)) { ok = false; break; }
-          if (t == 0 && !wait(bars.v_full(sv), (j / NSV) & 1)) { ok = false; break; }
-          tc::fence_after();
-          issue_pv(t, sv, j > 0, wide);
-          if (j == nkv - 1) tc::commit_elect(bars.o_final(t));
-          if (t == NQ - 1) tc::commit_elect(bars.v_empty(sv));
-          if (j + 1 < nkv) {
-            if (t == 0 && !wait(bars.k_full(sk1), ((j + 1) / NSK) & 1)) { ok = false; break; }
+      // other head's softmax runs while these MMAs execute. An item's first S
+      // MMAs follow the previous item's last P V, so they run while its
+      // softmax warps store O; its first P V waits for their first P, which
+      // they write after reading O out.
+      bool ok = true;
+      int g0 = 0;
+      for (int it = 0; ok; ++it) {
+        const int item = next_item(it);
+        if (item < 0) break;
+        const Work w = work_at(item);
+        const int* tile_wide = wide_flags(w);
+        ok = wait(bars.q_full(), it & 1) && wait(bars.k_full(g0 % NSK), (g0 / NSK) & 1);
+        if (!ok) break;
+        tc::fence_after();
+        for (int t = 0; t < NQ; ++t) {
+          issue_s(t, g0 % NSK);
+          tc::commit_elect(bars.s_full(t));
+        }
+        tc::commit_elect(bars.k_empty(g0 % NSK));
+        if (w.nkv == 1) tc::commit_elect(bars.q_empty());
+        if (it == 0) pdl_wait();  // the tile flags below are the V pass's output
+        // The loop is instantiated twice: for items without a wide tile (the
+        // common case) it has no per-tile format branch at all.
+        auto tiles = [&](auto any_wide) {
+        constexpr bool MAYBE_WIDE = decltype(any_wide)::value;
+        uint32_t wbits = 0;
+        for (int j = 0; ok && j < w.nkv; ++j) {
+          const int g = g0 + j;
+          const int sv = g % NSV;
+          const int sk1 = (g + 1) % NSK;
+          bool wide = false;
+          if constexpr (MAYBE_WIDE) {
+            if ((j & 31) == 0) wbits = wide_bits(tile_wide, j, w.nkv);
+            wide = (wbits >> (j & 31)) & 1u;
+          }
+          for (int t = 0; t < NQ && ok; ++t) {
+            if (!wait(bars.p_full(t), g & 1)) { ok = false; break; }
+            if (t == 0 && !wait(bars.v_full(sv), (g / NSV) & 1)) { ok = false; break; }
             tc::fence_after();
-            issue_s(t, sk1);
-            tc::commit_elect(bars.s_full(t));
-            if (t == NQ - 1) tc::commit_elect(bars.k_empty(sk1));
+            issue_pv(t, sv, j > 0, wide);
+            if (j == w.nkv - 1) tc::commit_elect(bars.o_final(t));
+            if (t == NQ - 1) tc::commit_elect(bars.v_empty(sv));
+            if (j + 1 < w.nkv) {
+              if (t == 0 && !wait(bars.k_full(sk1), ((g + 1) / NSK) & 1)) { ok = false; break; }
+              tc::fence_after();
+              issue_s(t, sk1);
+              tc::commit_elect(bars.s_full(t));
+              if (t == NQ - 1) {
+                tc::commit_elect(bars.k_empty(sk1));
+                if (j + 2 == w.nkv) tc::commit_elect(bars.q_empty());  // Q's last reader
+              }
+            }
           }
         }
+        };
+        if (item_has_wide(tile_wide, w.nkv)) tiles(std::true_type{}); else tiles(std::false_type{});
+        g0 += w.nkv;
       }
       // Everything issued has completed once mma_done flips.
       tc::commit_elect(bars.mma_done());
@@ -463,26 +720,43 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
     const int t = warp >> 2;
     const int wq = warp & 3;
     const int r = wq * 32 + lane;
-    const int row = qb * kBM + r;  // query index within the row (paged) or the sequence
-    const int hq = hq0 + t;
-    // Paged rows: keys [0, key_end) are visible to this query (none for the
-    // padding rows of a row's last tile).
-    const bool row_valid = PAGED ? row < q_len : row < T;
-    const int key_end = !PAGED ? 0 : (!row_valid ? 0 : (causal ? ctx - q_len + row + 1 : ctx));
     const uint32_t tS = tmem + (uint32_t(wq * 32) << 16) + t * 256;
     const uint32_t tO = tS + 128;
+    bool ok = true;
+    int g0 = 0;
+    pdl_wait();  // the tile flags are the V pass's output
+    for (int it = 0; ok; ++it) {
+    const int item = next_item(it);
+    if (item < 0) break;
+    const Work w = work_at(item);
+    const int* tile_wide = wide_flags(w);
+    const int row = w.qb * kBM + r;  // query index within the row (paged) or the sequence
+    const int hq = w.hq0 + t;
+    // Paged rows: keys [0, key_end) are visible to this query (none for the
+    // padding rows of a row's last tile).
+    const bool row_valid = PAGED ? row < w.q_len : row < T;
+    const int key_end =
+        !PAGED ? 0 : (!row_valid ? 0 : (causal ? w.ctx - w.q_len + row + 1 : w.ctx));
     // m_ref: exp2-domain reference that l, O~ and this tile's P are relative
     // to (the row max of some tile seen so far, within 2^15 of the running
     // max).
     float m_ref = -INFINITY;
     float l = 0.f;
-    bool ok = true;
-    pdl_wait();  // the tile flags are the V pass's output
-    for (int j = 0; j < nkv; ++j) {
+    // Instantiated twice, as the MMA warp's loop: without a wide tile in the
+    // item, no tile takes the format branch.
+    auto tiles = [&](auto any_wide) {
+    constexpr bool MAYBE_WIDE = decltype(any_wide)::value;
+    uint32_t wbits = 0;
+    for (int j = 0; j < w.nkv; ++j) {
+      const int g = g0 + j;
       // The format of P follows the format of this key tile's V.
-      const bool wide = is_wide(j);
+      bool wide = false;
+      if constexpr (MAYBE_WIDE) {
+        if ((j & 31) == 0) wbits = wide_bits(tile_wide, j, w.nkv);
+        wide = (wbits >> (j & 31)) & 1u;
+      }
       // Warp-uniform outcome: the tensor-memory loads below are warp-collective.
-      if (!__all_sync(0xffffffffu, wait_or_abort(bars.s_full(t), j & 1, abort_flag))) {
+      if (!__all_sync(0xffffffffu, wait_or_abort(bars.s_full(t), g & 1, abort_flag))) {
         ok = false;
         break;
       }
@@ -495,8 +769,8 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
           // workspace copy, when there is one, has them zeroed already). The tile's V phase cannot
           // move on before that P V, so the wait sees this tile's copy. Done
           // before the S tile is loaded, while few registers are live.
-          const int sv = j % NSV;
-          if (wait_or_abort(bars.v_full(sv), (j / NSV) & 1, abort_flag)) {
+          const int sv = g % NSV;
+          if (wait_or_abort(bars.v_full(sv), (g / NSV) & 1, abort_flag)) {
             // Thread r clears 16-byte chunk r % 8 of slot r / 8 past the last
             // key, in every 64-column block (16 slots x 8 chunks = 128 threads).
             if ((r >> 3) < (tail_info[1] >> 8)) {
@@ -518,7 +792,7 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
         lim = min(kBN, key_end - j * kBN);
       } else {
         if (j * kBN + kBN > T) lim = T - j * kBN;
-        if (causal && j == qb) lim = min(lim, r + 1);
+        if (causal && j == w.qb) lim = min(lim, r + 1);
       }
       const uint64_t c2 = f2(scale_log2, scale_log2);
       uint32_t sr[4][32];
@@ -564,8 +838,9 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
       const bool rescale = j > 0 && __any_sync(0xffffffffu, alpha != 1.f);
       const float bias = (m_ref == -INFINITY) ? 0.f : m_ref;
       const uint64_t nb2 = f2(-bias, -bias);
-      uint64_t sumA = f2(0.f, 0.f), sumB = f2(0.f, 0.f);
+      float psum;  // row sum of this tile's weights
       if (!wide) {
+        uint64_t sumA = f2(0.f, 0.f), sumB = f2(0.f, 0.f);
         // P in fp16 (11 significant bits). Key pair (2i, 2i+1) of chunk c
         // goes to P column 16c + i, i.e. the first 64 columns of the S tile
         // just read; sr[c][i] is reused to stage that pair (its S values
@@ -593,49 +868,11 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
             for (int i = 0; i < 16; ++i) pw[16 * c + i] = sr[2 * half + c][i];
           tc::st32(tS + 32 * half, pw);  // P keys 64*half .. +63
         }
+        float sa0, sa1;
+        unf2(add2(sumA, sumB), sa0, sa1);
+        psum = sa0 + sa1;
       } else {
-        // P = P_hi + P_lo, both bf16. P_hi is p truncated to bf16 (its upper
-        // 16 bits), P_lo = bf16(p - P_hi) (the difference is exact in fp32),
-        // so the pair carries ~16 significant bits (a single bf16 P costs up
-        // to 2^-8 relative per weight, which rows dominated by a few keys do
-        // not average away). Within chunk c, sr[c][2i] is reused for the
-        // P_hi pair of keys (2i, 2i+1), sr[c][2i+1] for P_lo.
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            float y0, y1;
-            unf2(fma2(f2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])), c2,
-                      nb2),
-                 y0, y1);
-            const float p0 = ex2_approx(y0);
-            const float p1 = ex2_approx(y1);
-            const uint64_t pp = f2(p0, p1);
-            if (i & 1) sumB = add2(sumB, pp); else sumA = add2(sumA, pp);
-            const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
-            uint32_t hi;
-            asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(hi) : "r"(u0), "r"(u1));
-            float d0, d1;
-            unf2(sub2(pp, f2(__uint_as_float(u0 & 0xffff0000u), __uint_as_float(u1 & 0xffff0000u))),
-                 d0, d1);
-            sr[c][2 * i] = hi;
-            sr[c][2 * i + 1] = pack_bf16x2(d0, d1);
-          }
-        }
-        // P_hi fills columns 0-63 and P_lo columns 64-127.
-        uint32_t hi[32], lo[32];
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-#pragma unroll
-          for (int c = 0; c < 2; ++c)
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              hi[16 * c + i] = sr[2 * half + c][2 * i];
-              lo[16 * c + i] = sr[2 * half + c][2 * i + 1];
-            }
-          tc::st32(tS + 32 * half, hi);       // P_hi keys 64*half .. +63
-          tc::st32(tS + 64 + 32 * half, lo);  // P_lo keys 64*half .. +63
-        }
+        psum = softmax_p_two_term(tS, lim, scale_log2, bias);
       }
       if (rescale) {
         // sr is free once P is stored (tcgen05.st reads its registers at
@@ -657,32 +894,47 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
           tc::st32(tO + c * 32, sr[c]);
         }
       }
-      float sa0, sa1;
-      unf2(add2(sumA, sumB), sa0, sa1);
-      l += sa0 + sa1;
+      l += psum;
       tc::wait_st();
       tc::fence_before();
       mbar_arrive(bars.p_full(t));
     }
-    if (ok) ok = __all_sync(0xffffffffu, wait_or_abort(bars.o_final(t), 0, abort_flag));
-    if (ok) {
+    };
+    if (item_has_wide(tile_wide, w.nkv)) tiles(std::true_type{}); else tiles(std::false_type{});
+    if (ok) ok = __all_sync(0xffffffffu, wait_or_abort(bars.o_final(t), it & 1, abort_flag));
+    if (!ok) break;
+    {
       tc::fence_after();
       // A row with no allowed key has l = 0 exactly (every weight is ex2 of
       // -inf). A NaN l (a NaN logit, or 0 * inf) is not empty: it reaches O
       // and the LSE.
       const bool empty = l == 0.f;
       const float inv = empty ? 0.f : 1.f / l;
-      const size_t orow_idx = PAGED ? size_t(q_tok0 + row) * h + hq : size_t(hq) * T + row;
-      // O leaves through this warp's quarter of its head's Q tile (the head's
-      // last S MMA, Q's last reader, completed before o_final). Each thread
-      // writes its row there in 16-byte chunks, chunk index XOR (row mod 8) so
-      // the 8 rows of a store phase hit distinct banks; then the warp stores
-      // whole rows, 256 (d_h = 128) or 128 contiguous bytes per row, instead of
-      // 32 rows x 16 bytes per instruction.
+      const size_t orow_idx = PAGED ? size_t(w.q_tok0 + row) * h + hq : size_t(hq) * T + row;
+      // O leaves through this warp's quarter of a V stage: head 0 uses the
+      // stage of the item's second-to-last key tile, head 1 that of the last
+      // (every P V MMA on the first completed before head 0's o_final, on the
+      // second before head 1's; the producer's next load into either waits
+      // for stage_free). Q stays untouched, so the next item's Q can load
+      // meanwhile. Paged rows (one item per CTA) use the head's Q tile, whose
+      // last reader, the head's last S MMA, completed before o_final. Each
+      // thread writes its row there in 16-byte chunks, chunk index XOR (row
+      // mod 8) so the 8 rows of a store phase hit distinct banks; then the
+      // warp stores whole rows, 256 (d_h = 128) or 128 contiguous bytes per
+      // row, instead of 32 rows x 16 bytes per instruction.
       constexpr int RB = D * 2;    // bytes per O row
       constexpr int CH = RB / 16;  // 16-byte chunks per row
       constexpr int RPI = 32 / CH; // rows per warp store instruction
-      uint8_t* stage = smem + C::Q_OFF + t * C::QTILE + wq * (32 * RB);
+      const int gl = g0 + w.nkv - 1;
+      // With one key tile, head 0's stage (that of tile gl - 1) is the one
+      // head 1 of the previous item staged in; it may still be reading it.
+      if (!PAGED && t == 0 && w.nkv == 1 && it > 0 &&
+          !__all_sync(0xffffffffu,
+                      wait_or_abort(bars.stage_free((it - 1) & 1), ((it - 1) >> 1) & 1, abort_flag)))
+        break;
+      uint8_t* stage =
+          PAGED ? smem + C::Q_OFF + t * C::QTILE + wq * (32 * RB)
+                : smem + C::V_OFF + ((t == 0 ? gl - 1 + NSV : gl) % NSV) * C::KTILE + wq * (32 * RB);
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t ov[32];
@@ -705,17 +957,25 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
 #pragma unroll
         for (int it = 0; it < 32 / RPI; ++it) {
           const int rr = it * RPI + lane / CH;  // row within this warp's 32
-          const int qrow = qb * kBM + wq * 32 + rr;
-          if (PAGED ? qrow < q_len : qrow < T) {
+          const int qrow = w.qb * kBM + wq * 32 + rr;
+          if (PAGED ? qrow < w.q_len : qrow < T) {
             const uint4 x =
                 *reinterpret_cast<const uint4*>(stage + rr * RB + ((ch ^ (rr & 7)) << 4));
-            const size_t oi = PAGED ? size_t(q_tok0 + qrow) * h + hq : size_t(hq) * T + qrow;
+            const size_t oi = PAGED ? size_t(w.q_tok0 + qrow) * h + hq : size_t(hq) * T + qrow;
             *reinterpret_cast<uint4*>(o + oi * D + ch * 8) = x;
           }
         }
       }
       if (row_valid && lse != nullptr)
         lse[orow_idx] = empty ? -INFINITY : (m_ref + log2f(l)) * kLn2;
+      // The warp's rows have left the stage (each lane's loads completed
+      // before its stores issued); the fence orders these generic accesses
+      // before the producer's next TMA write there.
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars.stage_free(it & 1));
+    }
+    g0 += w.nkv;
     }
   }
 
@@ -733,8 +993,11 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
 // with an absolute error below 2^-25. One CTA per tile, 16-byte accesses.
 __global__ void __launch_bounds__(256)
     v_to_f16_kernel(const uint4* __restrict__ v, uint4* __restrict__ v16, int* __restrict__ vwide,
-                    int T, int chunks_per_row, int n_tiles) {
+                    int* __restrict__ sched, int T, int chunks_per_row, int n_tiles) {
   const int tile = blockIdx.x, kvh = blockIdx.y;
+  // The attention kernel's item counter starts from zero for every call; it
+  // reads the counter only after waiting for this grid.
+  if (sched != nullptr && tile == 0 && kvh == 0 && threadIdx.x == 0) *sched = 0;
   // The attention kernel (a programmatic dependent) may start its CTAs'
   // set-up and Q, K loads now; it waits for this grid before touching V.
   pdl_trigger();
@@ -842,8 +1105,8 @@ __global__ void __launch_bounds__(256)
 
 template <int D, int NQ, int NSK, int NSV>
 cudaError_t launch(const void* q, const void* k, const void* v, const void* v16, const int* vwide,
-                   void* o, float* lse, int T, int h, int h_kv, int causal, float scale,
-                   cudaStream_t stream) {
+                   int* sched, void* o, float* lse, int T, int h, int h_kv, int causal,
+                   float scale, cudaStream_t stream) {
   using C = PfCfg<D, NQ, NSK, NSV>;
   static_assert(C::SMEM <= 232448, "shared memory budget");
   CUtensorMap tq, tk, tv, tv16;
@@ -874,18 +1137,27 @@ cudaError_t launch(const void* q, const void* k, const void* v, const void* v16,
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   const int n_qblk = (T + kBM - 1) / kBM;
-  if (n_qblk > 65535) return cudaErrorNotSupported;  // query tiles index grid y
-  const dim3 grid(h / NQ, n_qblk);
+  // Persistent grid: one CTA per SM (the shared memory admits one), each
+  // walking its share of the (head group, query block) items.
+  const long long n_items = static_cast<long long>(h / NQ) * n_qblk;
+  if (n_items <= 0) return cudaSuccess;
+  if (n_items > INT_MAX / 2) return cudaErrorNotSupported;
+  int dev = 0, sms = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const dim3 grid(static_cast<unsigned>(n_items < sms ? n_items : sms));
   // After the V pass the kernel is its programmatic dependent (it waits for
   // that grid before reading V or the flags); without one it follows
   // whatever precedes it on the stream in plain order.
   if (v16)
     return launch_pdl(kern, grid, dim3(C::THREADS), C::SMEM, stream, tq, tk, tv, tv16, vwide,
                       static_cast<__nv_bfloat16*>(o), lse, T, h, h_kv, causal, scale * kLog2e,
-                      n_qblk, PagedArgs{});
+                      n_qblk, sched, PagedArgs{});
   kern<<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tv16, nullptr,
                                                static_cast<__nv_bfloat16*>(o), lse, T, h, h_kv,
-                                               causal, scale * kLog2e, n_qblk, PagedArgs{});
+                                               causal, scale * kLog2e, n_qblk, nullptr,
+                                               PagedArgs{});
   return cudaGetLastError();
 }
 
@@ -973,7 +1245,8 @@ cudaError_t launch_paged(const PagedPrefill& a, cudaStream_t stream) {
                a.B,           a.max_blocks, a.num_blocks, max_tiles};
   kern<<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tv16, a.v16 ? a.vwide : nullptr,
                                                static_cast<__nv_bfloat16*>(a.o), a.lse, 0, a.h,
-                                               a.h_kv, a.causal, a.scale * kLog2e, 0, pa);
+                                               a.h_kv, a.causal, a.scale * kLog2e, 0, nullptr,
+                                               pa);
   return cudaGetLastError();
 }
 
@@ -983,7 +1256,8 @@ PrefillLayout prefill_layout(int T, int h_kv, int d_h) {
   PrefillLayout L;
   L.v16_off = 0;
   L.flags_off = align256(size_t(h_kv) * T * d_h * 2);
-  L.total = L.flags_off + align256(size_t(h_kv) * ((T + kBN - 1) / kBN) * sizeof(int));
+  L.sched_off = L.flags_off + align256(size_t(h_kv) * ((T + kBN - 1) / kBN) * sizeof(int));
+  L.total = L.sched_off + 256;  // the attention kernel's item counter
   return L;
 }
 
@@ -994,23 +1268,26 @@ cudaError_t launch_prefill_bf16(const void* q, const void* k, const void* v, voi
   const bool pair = (g % 2) == 0;
   void* v16 = nullptr;
   int* vwide = nullptr;
+  int* sched = nullptr;
   if (workspace) {
     const PrefillLayout L = prefill_layout(T, h_kv, d_h);
     v16 = static_cast<uint8_t*>(workspace) + L.v16_off;
     vwide = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + L.flags_off);
+    sched = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + L.sched_off);
     const int n_tiles = (T + kBN - 1) / kBN;
     v_to_f16_kernel<<<dim3(n_tiles, h_kv), 256, 0, stream>>>(
-        static_cast<const uint4*>(v), static_cast<uint4*>(v16), vwide, T, d_h / 8, n_tiles);
+        static_cast<const uint4*>(v), static_cast<uint4*>(v16), vwide, sched, T, d_h / 8,
+        n_tiles);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   // Stage counts fill the shared memory next to the Q tiles (<= 227 KB).
   if (d_h == 128) {
-    return pair ? launch<128, 2, 2, 3>(q, k, v, v16, vwide, o, lse, T, h, h_kv, causal, scale, stream)
-                : launch<128, 1, 3, 3>(q, k, v, v16, vwide, o, lse, T, h, h_kv, causal, scale, stream);
+    return pair ? launch<128, 2, 2, 3>(q, k, v, v16, vwide, sched, o, lse, T, h, h_kv, causal, scale, stream)
+                : launch<128, 1, 3, 3>(q, k, v, v16, vwide, sched, o, lse, T, h, h_kv, causal, scale, stream);
   }
-  return pair ? launch<64, 2, 4, 4>(q, k, v, v16, vwide, o, lse, T, h, h_kv, causal, scale, stream)
-              : launch<64, 1, 4, 4>(q, k, v, v16, vwide, o, lse, T, h, h_kv, causal, scale, stream);
+  return pair ? launch<64, 2, 4, 4>(q, k, v, v16, vwide, sched, o, lse, T, h, h_kv, causal, scale, stream)
+              : launch<64, 1, 4, 4>(q, k, v, v16, vwide, sched, o, lse, T, h, h_kv, causal, scale, stream);
 }
 
 cudaError_t launch_prefill_paged(const PagedPrefill& a, cudaStream_t stream) {

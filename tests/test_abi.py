@@ -161,7 +161,7 @@ def test_prefill_host_scratch_bytes(lib):
     T, h, h_kv, d = 333, 8, 2, 64
     qb, kb, lb = h * T * d * 2, h_kv * T * d * 2, h * T * 4
     ws = lib.attn_prefill_workspace_bytes(T, h_kv, d, 1)
-    assert ws == 85248 + 256
+    assert ws == 85248 + 256 + 256  # V copy, tile flags, work counter
     assert f(T, h, h_kv, d, 1) == a(qb) + 2 * a(kb) + a(qb) + a(lb) + ws
     assert f(256, 1, 1, 64, 0) == 2 * a(256 * 64 * 4) + 2 * a(256 * 64 * 4) + a(256 * 4)  # fp32: no workspace
     assert f(0, h, h_kv, d, 1) == 0
@@ -188,9 +188,10 @@ def test_prefill_paged_v16_workspace_bytes(lib):
 
 
 def test_prefill_workspace_bytes(lib):
-    """fp16 copy of V (256-byte aligned) followed by one int per (KV head, 128-key tile)."""
-    assert lib.attn_prefill_workspace_bytes(8192, 8, 128, 1) == 8 * 8192 * 128 * 2 + 2048  # then 8 x 64 ints
-    assert lib.attn_prefill_workspace_bytes(333, 2, 64, 1) == 85248 + 256  # 2*333*64*2, then 6 ints
+    """fp16 copy of V (256-byte aligned), one int per (KV head, 128-key tile),
+    then 256 bytes for the work counter."""
+    assert lib.attn_prefill_workspace_bytes(8192, 8, 128, 1) == 8 * 8192 * 128 * 2 + 2048 + 256  # 8 x 64 ints
+    assert lib.attn_prefill_workspace_bytes(333, 2, 64, 1) == 85248 + 256 + 256  # 2*333*64*2, then 6 ints
     assert lib.attn_prefill_workspace_bytes(8192, 8, 128, 0) == 0  # fp32 SIMT path: none
     assert lib.attn_prefill_workspace_bytes(0, 8, 128, 1) == 0
     none = (1 << 64) - 1
