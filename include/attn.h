@@ -84,6 +84,9 @@ typedef enum { ATTN_DTYPE_F32 = 0, ATTN_DTYPE_BF16 = 1 } attn_dtype_t;
 #define ATTN_DEVERR_BAD_PAGE 0x2u     /* block_table entry outside the cache */
 #define ATTN_DEVERR_TMEM 0x4u         /* tensor-memory allocation failed     */
 #define ATTN_DEVERR_BAD_SEQ_LEN 0x8u  /* seq_len < 0 or beyond the table row  */
+/* Builds compiled with -DATTN_DEBUG only: an index or offset check failed;
+ * the access it guarded was skipped (release builds carry no such checks). */
+#define ATTN_DEVERR_DEBUG_INDEX 0x10u
 
 /* Human-readable name of a status code; never NULL. */
 const char* attn_status_string(attn_status_t status);

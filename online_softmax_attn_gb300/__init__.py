@@ -36,8 +36,12 @@ __all__ = [
  ATTN_ERR_DEVICE_TIMEOUT) = range(6)
 ATTN_DTYPE_F32, ATTN_DTYPE_BF16 = 0, 1
 ATTN_MAX_SPLITS = 1024
+# Device error bits (attn_get_device_error), as in attn.h.
+(ATTN_DEVERR_WAIT_TIMEOUT, ATTN_DEVERR_BAD_PAGE, ATTN_DEVERR_TMEM, ATTN_DEVERR_BAD_SEQ_LEN,
+ ATTN_DEVERR_DEBUG_INDEX) = (0x1, 0x2, 0x4, 0x8, 0x10)
 DEVERR_NAMES = {0x1: "wait timeout", 0x2: "page index outside cache",
-                0x4: "tensor-memory allocation", 0x8: "seq_len outside table row"}
+                0x4: "tensor-memory allocation", 0x8: "seq_len outside table row",
+                0x10: "index check failed (debug build)"}
 
 _lib = None
 

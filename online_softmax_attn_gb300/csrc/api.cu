@@ -453,12 +453,14 @@ attn_status_t attn_selftest_delayed_copy(int32_t* dst, const int32_t* src, int n
 attn_status_t attn_get_device_error(void* stream, unsigned int* bits) {
   if (bits == nullptr) return ATTN_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e1 = cudaSuccess, e2 = cudaSuccess, e3 = cudaSuccess;
+  cudaError_t e1 = cudaSuccess, e2 = cudaSuccess, e3 = cudaSuccess, e4 = cudaSuccess;
   unsigned int v = decode_read_and_clear_error(s, &e1);
   v |= merge_read_and_clear_error(s, &e2);
   v |= prefill_read_and_clear_error(s, &e3);
+  v |= simt_read_and_clear_error(s, &e4);
   *bits = v;
-  if (e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess) return ATTN_ERR_CUDA;
+  if (e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess || e4 != cudaSuccess)
+    return ATTN_ERR_CUDA;
   return ATTN_OK;
 }
 

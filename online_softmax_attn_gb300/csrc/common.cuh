@@ -18,7 +18,29 @@
 #define ATTN_WAIT_LIMIT_NS 2000000000ull  // 2 s
 #endif
 
+// Debug builds (-DATTN_DEBUG) check indices and offsets on the kernels'
+// global stores and on the shared-memory offsets they compute:
+//   ATTN_GUARD(cond, err)  -> cond, after recording ATTN_DEVERR_DEBUG_INDEX in
+//                             *err when it is false; the caller skips the
+//                             access it guards;
+//   ATTN_DCHECK(cond, err) -> records the same bit for an invariant whose
+//                             violation cannot be skipped locally.
+// Nothing traps. Release builds compile both to nothing (the condition is not
+// evaluated).
+#ifdef ATTN_DEBUG
+#define ATTN_GUARD(cond, err) (::attn::debug_check(static_cast<bool>(cond), (err)))
+#define ATTN_DCHECK(cond, err) ((void)::attn::debug_check(static_cast<bool>(cond), (err)))
+#else
+#define ATTN_GUARD(cond, err) (true)
+#define ATTN_DCHECK(cond, err) ((void)0)
+#endif
+
 namespace attn {
+
+__device__ __forceinline__ bool debug_check(bool ok, unsigned int* err) {
+  if (!ok) atomicOr(err, ATTN_DEVERR_DEBUG_INDEX);
+  return ok;
+}
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;

@@ -179,11 +179,17 @@ __global__ void __launch_bounds__(NW * 32, 1)
   // layout of m16n8k16: a0 = (row gid, k 2tq..2tq+1), a2 = (row gid, k+8).
   uint32_t qa0[KS], qa2[KS];
   {
+    // Debug checks: the head group lies within the row's h heads, and the
+    // token within the query tokens (B, or q_rows[B] in a mixed batch).
+    const bool q_ok = ATTN_GUARD(
+        kvh * G + G <= h &&
+            q_tok < (q_rows != nullptr ? size_t(__ldcg(q_rows + gridDim.z)) : size_t(gridDim.z)),
+        &g_decode_err);
     const __nv_bfloat16* qr = q + (q_tok * h + kvh * G + min(gid, G - 1)) * D + 2 * tq;
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
-      const uint32_t x0 = __ldg(reinterpret_cast<const uint32_t*>(qr + 16 * ks));
-      const uint32_t x2 = __ldg(reinterpret_cast<const uint32_t*>(qr + 16 * ks + 8));
+      const uint32_t x0 = q_ok ? __ldg(reinterpret_cast<const uint32_t*>(qr + 16 * ks)) : 0u;
+      const uint32_t x2 = q_ok ? __ldg(reinterpret_cast<const uint32_t*>(qr + 16 * ks + 8)) : 0u;
       qa0[ks] = gid < G ? x0 : 0u;
       qa2[ks] = gid < G ? x2 : 0u;
     }
@@ -398,6 +404,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
       L = fmaf(wt, ml_s[(w * G + hh) * 2 + 1], L);
     }
     const size_t prow = (row0 + hh) * num_splits + split;
+    if (!ATTN_GUARD(prow < size_t(gridDim.z) * h * num_splits, &g_decode_err)) continue;
     o_part[prow * D + e] = A;
     if (e == 0) {
       m_part[prow] = M * kLn2;

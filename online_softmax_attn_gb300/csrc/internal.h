@@ -110,6 +110,8 @@ struct PagedPrefill {
 };
 cudaError_t launch_prefill_paged(const PagedPrefill& a, cudaStream_t stream);
 unsigned int prefill_read_and_clear_error(cudaStream_t stream, cudaError_t* st);
+// The fp32 SIMT prefill's error word (debug-build index checks only).
+unsigned int simt_read_and_clear_error(cudaStream_t stream, cudaError_t* st);
 
 // tensor maps ---------------------------------------------------------------
 // Encodes a tiled tensor map through the driver entry point (no libcuda link).

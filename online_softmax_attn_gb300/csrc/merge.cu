@@ -63,6 +63,13 @@ __global__ void __launch_bounds__(WPR > 8 ? WPR * 32 : 256)
     live = r1 - r0 == 1;
     out_row = size_t(r0) * heads_per_seq + row % heads_per_seq;
   }
+  // Debug checks: the output row lies within the output (rows, or h per
+  // query token of a mixed batch); a failed check leaves the row unwritten.
+  if (live && !ATTN_GUARD(out_row < (q_rows != nullptr
+                                          ? size_t(q_rows[rows / heads_per_seq]) * heads_per_seq
+                                          : size_t(rows)),
+                          &g_merge_err))
+    live = false;
   if (WPR == 1 && !live) return;
 
   const float* mrow = m_part + size_t(row) * S;

@@ -34,6 +34,9 @@
 
 namespace attn {
 
+// Device error word of this module (debug-build index checks).
+static __device__ unsigned int g_simt_err;
+
 namespace {
 
 constexpr int kRows = 16;
@@ -180,9 +183,11 @@ __global__ void __launch_bounds__(256)
       const bool empty = l == 0.f;  // no allowed key; a NaN l is not empty
       const float inv = empty ? 0.f : 1.f / l;
       float* orow = o + (size_t(hq) * T + row) * D;
+      if (ATTN_GUARD(hq < h, &g_simt_err)) {
 #pragma unroll
-      for (int e = 0; e < OC; ++e) orow[c + kTPR * e] = acc[e] * inv;
-      if (lse != nullptr && c == 0) lse[size_t(hq) * T + row] = empty ? -INFINITY : m + logf(l);
+        for (int e = 0; e < OC; ++e) orow[c + kTPR * e] = acc[e] * inv;
+        if (lse != nullptr && c == 0) lse[size_t(hq) * T + row] = empty ? -INFINITY : m + logf(l);
+      }
     }
     return;
   }
@@ -222,7 +227,7 @@ __global__ void __launch_bounds__(256)
       if (w[i] != 0.f) L += w[i] * *cluster.map_shared_rank(l_s + rl, i);
     }
     const bool empty = M == -INFINITY;  // no CTA saw an allowed key; NaN states propagate
-    if (grow < T) {
+    if (grow < T && ATTN_GUARD(hq < h, &g_simt_err)) {
       float* orow = o + (size_t(hq) * T + grow) * D;
       for (int col = col0; col < D; col += tpr) {
         float x = 0.f;
@@ -271,6 +276,18 @@ cudaError_t launch(const float* q, const float* k, const float* v, float* o, flo
 }
 
 }  // namespace
+
+unsigned int simt_read_and_clear_error(cudaStream_t stream, cudaError_t* st) {
+  unsigned int v = 0, zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_simt_err, sizeof(v), 0,
+                                            cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess)
+    e = cudaMemcpyToSymbolAsync(g_simt_err, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice,
+                                stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (st) *st = e;
+  return v;
+}
 
 cudaError_t launch_prefill_f32(const float* q, const float* k, const float* v, float* o,
                                float* lse, int T, int h, int h_kv, int d_h, int causal,

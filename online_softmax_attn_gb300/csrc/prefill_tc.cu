@@ -729,6 +729,10 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
     const int item = next_item(it);
     if (item < 0) break;
     const Work w = work_at(item);
+    ATTN_DCHECK(w.hq0 + NQ <= h && w.kvh < h_kv && w.nkv >= 1 &&
+                    w.nkv <= (PAGED ? pa.max_tiles : w.n_kv_all) &&
+                    (PAGED || w.qb < n_qblk),
+                &g_prefill_err);
     const int* tile_wide = wide_flags(w);
     const int row = w.qb * kBM + r;  // query index within the row (paged) or the sequence
     const int hq = w.hq0 + t;
@@ -911,6 +915,11 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
       const bool empty = l == 0.f;
       const float inv = empty ? 0.f : 1.f / l;
       const size_t orow_idx = PAGED ? size_t(w.q_tok0 + row) * h + hq : size_t(hq) * T + row;
+      // Output rows (debug checks): h * T, or h per packed query token.
+      auto out_rows = [&]() -> size_t {
+        return PAGED ? size_t(pa.cu_q[pa.B]) * h : size_t(h) * T;
+      };
+      (void)out_rows;
       // O leaves through this warp's quarter of a V stage: head 0 uses the
       // stage of the item's second-to-last key tile, head 1 that of the last
       // (every P V MMA on the first completed before head 0's o_final, on the
@@ -935,6 +944,9 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
       uint8_t* stage =
           PAGED ? smem + C::Q_OFF + t * C::QTILE + wq * (32 * RB)
                 : smem + C::V_OFF + ((t == 0 ? gl - 1 + NSV : gl) % NSV) * C::KTILE + wq * (32 * RB);
+      ATTN_DCHECK(stage >= smem + (PAGED ? C::Q_OFF : C::V_OFF) &&
+                      stage + 32 * RB <= smem + (PAGED ? C::K_OFF : C::BAR_OFF),
+                  &g_prefill_err);
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t ov[32];
@@ -962,11 +974,12 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
             const uint4 x =
                 *reinterpret_cast<const uint4*>(stage + rr * RB + ((ch ^ (rr & 7)) << 4));
             const size_t oi = PAGED ? size_t(w.q_tok0 + qrow) * h + hq : size_t(hq) * T + qrow;
-            *reinterpret_cast<uint4*>(o + oi * D + ch * 8) = x;
+            if (ATTN_GUARD(oi < out_rows(), &g_prefill_err))
+              *reinterpret_cast<uint4*>(o + oi * D + ch * 8) = x;
           }
         }
       }
-      if (row_valid && lse != nullptr)
+      if (row_valid && lse != nullptr && ATTN_GUARD(orow_idx < out_rows(), &g_prefill_err))
         lse[orow_idx] = empty ? -INFINITY : (m_ref + log2f(l)) * kLn2;
       // The warp's rows have left the stage (each lane's loads completed
       // before its stores issued); the fence orders these generic accesses
@@ -1029,13 +1042,15 @@ __global__ void __launch_bounds__(256)
         y.y = pack_f16x2(bf16lo(x[u].y), bf16hi(x[u].y));
         y.z = pack_f16x2(bf16lo(x[u].z), bf16hi(x[u].z));
         y.w = pack_f16x2(bf16lo(x[u].w), bf16hi(x[u].w));
-        v16[base + i] = y;
+        if (ATTN_GUARD(base + i < size_t(gridDim.y) * T * chunks_per_row, &g_prefill_err))
+          v16[base + i] = y;
       }
     }
   }
   // bf16 bits 0x4780 = 2^16: the first magnitude fp16 cannot hold.
   const int wide = __syncthreads_or((mx & 0xffffu) >= 0x4780u || (mx >> 16) >= 0x4780u);
-  if (threadIdx.x == 0) vwide[size_t(kvh) * n_tiles + tile] = wide;
+  if (threadIdx.x == 0 && ATTN_GUARD(tile < n_tiles && kvh < int(gridDim.y), &g_prefill_err))
+    vwide[size_t(kvh) * n_tiles + tile] = wide;
 }
 
 // Paged V -> a copy of the keys each row uses, token-contiguous per row:
@@ -1098,9 +1113,14 @@ __global__ void __launch_bounds__(256)
       y.z = pack_f16x2(bf16lo(x[u].z), bf16hi(x[u].z));
       y.w = pack_f16x2(bf16lo(x[u].w), bf16hi(x[u].w));
     }
-    v16[((size_t(b) * max_tiles * kBN + size_t(jt) * kBN + tok) * h_kv + kvh) * CPR + c] = y;
+    const size_t vi = ((size_t(b) * max_tiles * kBN + size_t(jt) * kBN + tok) * h_kv + kvh) * CPR + c;
+    if (ATTN_GUARD(tok < kBN && vi < size_t(gridDim.y) * max_tiles * kBN * h_kv * CPR,
+                   &g_prefill_err))
+      v16[vi] = y;
   }
-  if (threadIdx.x == 0) vwide[(size_t(b) * h_kv + kvh) * max_tiles + jt] = wide;
+  if (threadIdx.x == 0 &&
+      ATTN_GUARD(jt < max_tiles && b < int(gridDim.y) && kvh < h_kv, &g_prefill_err))
+    vwide[(size_t(b) * h_kv + kvh) * max_tiles + jt] = wide;
 }
 
 template <int D, int NQ, int NSK, int NSV>

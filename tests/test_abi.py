@@ -353,3 +353,17 @@ def test_core_signatures_are_the_minimal_ones_plus_documented_additions():
         m = re.search(rf"{name}\s+([\w, ]+?)\s*\(after", note)
         assert m, name
         assert [x.strip() for x in m.group(1).split(",")] == extra, (name, m.group(1))
+
+
+def test_device_error_bits_match_the_header():
+    """The binding's ATTN_DEVERR_* constants are the header's #defines."""
+    import re
+
+    import online_softmax_attn_gb300 as attn
+
+    text = open(os.path.join(ROOT, "include", "attn.h")).read()
+    bits = dict(re.findall(r"#define (ATTN_DEVERR_\w+) (0x[0-9a-fA-F]+)u", text))
+    assert bits, "no ATTN_DEVERR_* bits in attn.h"
+    for name, value in bits.items():
+        assert getattr(attn, name) == int(value, 16), name
+    assert set(attn.DEVERR_NAMES) == {int(v, 16) for v in bits.values()}
