@@ -54,20 +54,20 @@ KERNEL_FILES["merge_pair"] = ["online_softmax_attn_gb300/csrc/merge.cu", "online
                               "online_softmax_attn_gb300/csrc/pdl.cuh"]
 NCU_TRAFFIC = {
     # kind: (dram read + write bytes per launch, sha256[:16] of the kernel's files)
-    # prefill_bf16_kernel, causal T=8192 layer, full-size capture: 102.4 MB read
-    # (compulsory Q, K, fp16 V) + 33.6 MB of the 67.1 MB output written back by exit
-    "prefill": (136.06e6, "4b09c590f008c803"),
+    # prefill_bf16_kernel, causal T=8192 layer, full-size capture: 102.6 MB read
+    # (compulsory Q, K, fp16 V) + 30.9 MB of the 67.1 MB output written back by exit
+    "prefill": (133.53e6, "13ee916037866cb8"),
     # prefill_bf16_kernel, causal T=2048 layer, full-size capture: the compulsory
-    # 25.2 MB read; the 16.8 MB output is still in L2 when the kernel exits
-    "prefill_T2048": (25.24e6, "4b09c590f008c803"),
+    # 25.3 MB read; the 16.8 MB output is still in L2 when the kernel exits
+    "prefill_T2048": (25.26e6, "13ee916037866cb8"),
     # prefill_bf16_kernel (paged), 8 rows x 1024 queries over 8192 keys, full-size capture
-    "prefill_paged": (467.01e6, "4b09c590f008c803"),
-    # decode_split_kernel: a 16-row capture (303.9 MB for 299.5 MB algorithmic) scaled by
+    "prefill_paged": (468.08e6, "13ee916037866cb8"),
+    # decode_split_kernel: a 16-row capture (304.0 MB for 299.5 MB algorithmic) scaled by
     # the KV bytes to the 66-row batch
-    "decode": (2.1517e9, "c7756d32f7037510"),
+    "decode": (2.1520e9, "61652ac3d8eae098"),
     # merge_pair_kernel, 262144 rows x 128 bf16, full-size capture: reads are the compulsory
     # 136.3 MB, writes 37.4 MB of the 68.2 MB output (the rest still in L2 at exit)
-    "merge_pair": (173.73e6, "1d1116a09f523c2d"),
+    "merge_pair": (173.71e6, "b69c2e0580ea7eaf"),
 }
 
 
