@@ -83,6 +83,7 @@ struct PfCfg {
   // p_full[NQ], o_final[NQ], mma_done, q_empty, stage_free[2], item_full[2]
   static constexpr int NBAR = 1 + 2 * NSK + 2 * NSV + 3 * NQ + 1 + 5;
   static_assert(NSV >= 3, "the epilogue stages O in two V stages the next item does not load first");
+  static_assert(NBAR <= 32, "one warp initialises the barriers, one per lane");
   // tensor-memory slot, abort flag, tail tile (2 ints), item slots (2 ints)
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int SMEM = MISC_OFF + 32 + 1024;  // + alignment slack
@@ -404,21 +405,31 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
     return any != 0;
   };
 
+  // The tensor maps' descriptors are fetched while the CTA sets up, not on
+  // the first TMA issue (any thread may issue the prefetch).
   if (threadIdx.x == 0) {
-    // p_full collects one arrival per softmax thread, stage_free one per
-    // softmax warp; the others take one.
-    for (int i = 0; i < C::NBAR; ++i) {
-      const uint32_t bar = bars.base + 8 * i;
+    prefetch_tmap(&tmap_q);
+    prefetch_tmap(&tmap_k);
+    prefetch_tmap(&tmap_v);
+    if (vwide) prefetch_tmap(&tmap_v16);
+  }
+  if (warp == 0) {
+    // One barrier per lane. p_full collects one arrival per softmax thread,
+    // stage_free one per softmax warp; the others take one.
+    if (lane < C::NBAR) {
+      const uint32_t bar = bars.base + 8 * lane;
       const bool is_p = bar >= bars.p_full(0) && bar < bars.p_full(0) + 8 * NQ;
       const bool is_stage = bar == bars.stage_free(0) || bar == bars.stage_free(1);
       mbar_init(bar, is_p ? 128u : is_stage ? uint32_t(NQ * 4) : 1u);
+      fence_barrier_init();
     }
-    *abort_flag = 0;
-    if constexpr (PAGED && !PCOPY) {
-      tail_info[0] = pw.ctx % 16 != 0 ? pw.ctx / kBN : -1;
-      tail_info[1] = (pw.ctx % kBN) | ((16 - pw.ctx % 16) << 8);
+    if (lane == 0) {
+      *abort_flag = 0;
+      if constexpr (PAGED && !PCOPY) {
+        tail_info[0] = pw.ctx % 16 != 0 ? pw.ctx / kBN : -1;
+        tail_info[1] = (pw.ctx % kBN) | ((16 - pw.ctx % 16) << 8);
+      }
     }
-    fence_barrier_init();
   }
   if (warp == C::MMA_WARP) tc::alloc(smem_u32(tmem_slot), C::TMEM_COLS);
   tc::fence_before();
@@ -445,10 +456,6 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
   if (warp == C::PRODUCER_WARP) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      prefetch_tmap(&tmap_q);
-      prefetch_tmap(&tmap_k);
-      prefetch_tmap(&tmap_v);
-      if (vwide) prefetch_tmap(&tmap_v16);
       // Loads issued so far (K and V tiles counted over all of this CTA's
       // items: tile g uses stage g % NS, phase (g / NS) & 1).
       int k_issued = 0, v_issued = 0, q_issued = 0;
