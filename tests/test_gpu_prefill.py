@@ -160,6 +160,38 @@ def test_gqa_T2048_causal_full():
     check_lse(lse, L_ref, "bench T2048 causal lse")
 
 
+@pytest.mark.parametrize("causal", [True, False])
+def test_more_items_than_sms_without_workspace(causal):
+    """Without a workspace the persistent kernel has no work counter: its CTAs
+    take the layer's items in fixed rounds (in order, then in reverse). With
+    16 head pairs x 16 query blocks = 256 items on at most 152 CTAs, several
+    CTAs run a second round, reversed. Every third head against the oracle,
+    and the whole output bitwise against the counter-ordered call (the order
+    in which CTAs take items changes nothing in an item's arithmetic)."""
+    shape = W.PrefillShape("t", 32, 8, 128, 2048, torch.bfloat16, causal)
+    q, k, v = W.prefill_inputs(shape, 17)
+    o, lse = attn.attn_prefill(q.cuda(), k.cuda(), v.cuda(), causal, shape.scale, workspace=None)
+    torch.cuda.synchronize()
+    assert attn.attn_get_device_error() == 0
+    heads = list(range(0, shape.h, 3))  # every third head: each KV head, both heads of a pair
+    O_ref, L_ref = oracle.attention_heads_ref(q, k, v, shape.scale, causal, heads,
+                                              threads=_oracle_threads())
+    check_out(o[heads], O_ref, torch.bfloat16, f"no-workspace T2048 {'causal' if causal else 'full'}")
+    check_lse(lse[heads], L_ref)
+    # With every key tile flagged wide, the call with a workspace runs the
+    # same per-item arithmetic (two-term bf16 P against the bf16 V) in the
+    # counter's order: the results are bitwise those of the fixed rounds.
+    ws = torch.empty(attn.attn_prefill_workspace_bytes(shape.T, shape.h_kv, shape.d_h),
+                     dtype=torch.uint8, device="cuda")
+    v_wide = v.clone()
+    v_wide[:, ::128, 0] = 1e5  # one value fp16 cannot hold in every 128-key tile
+    o1, _ = attn.attn_prefill(q.cuda(), k.cuda(), v_wide.cuda(), causal, shape.scale, workspace=None)
+    o2, _ = attn.attn_prefill(q.cuda(), k.cuda(), v_wide.cuda(), causal, shape.scale, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2)
+    assert attn.attn_get_device_error() == 0
+
+
 @pytest.mark.parametrize("shape", [W.GQA_T8192_CAUSAL, W.GQA_T8192_FULL], ids=lambda s: s.name)
 def test_gqa_T8192_every_element(shape):
     """The T = 8192 layer the benchmark times (Q, K x3), causal and not:
