@@ -192,6 +192,59 @@ def test_more_items_than_sms_without_workspace(causal):
     assert attn.attn_get_device_error() == 0
 
 
+@pytest.mark.parametrize("h,h_kv,d,T,causal", [
+    (16, 4, 64, 4096, True),    # d_h = 64: four V stages; 8 x 32 = 256 items
+    (6, 2, 128, 4096, True),    # g = 3: one head per item; 6 x 32 = 192 items
+    (3, 1, 64, 8192, False),    # d_h = 64, one head per item, equal items; 3 x 64 = 192
+])
+def test_persistent_walk_other_instances(h, h_kv, d, T, causal):
+    """More items than SMs in the kernel instances the benchmark layers do not
+    use (d_h = 64 with four V stages; groups of odd size, one head per item):
+    CTAs take several items each, so the rings, the O staging in V stages and
+    the item hand-over run across items. Every element of every other head
+    against the oracle."""
+    shape = W.PrefillShape("t", h, h_kv, d, T, torch.bfloat16, causal)
+    q, k, v = W.prefill_inputs(shape, 21)
+    o, lse = run(q, k, v, causal, shape.scale)
+    assert attn.attn_get_device_error() == 0
+    heads = list(range(0, h, 2))
+    O_ref, L_ref = oracle.attention_heads_ref(q, k, v, shape.scale, causal, heads,
+                                              threads=_oracle_threads())
+    check_out(o[heads], O_ref, torch.bfloat16, f"persistent h{h} kv{h_kv} d{d} T{T}")
+    check_lse(lse[heads], L_ref)
+
+
+def test_graph_replays_with_new_inputs():
+    """A CUDA graph of one prefill call (V pass, which also zeroes the work
+    counter, then the persistent kernel), replayed after new inputs are copied
+    into its buffers: every replay equals an ordinary call on those inputs,
+    bitwise."""
+    shape = W.PrefillShape("t", 32, 8, 128, 2048, torch.bfloat16, True)
+    q, k, v = (t.cuda() for t in W.prefill_inputs(shape, 5))
+    ws = torch.empty(attn.attn_prefill_workspace_bytes(shape.T, shape.h_kv, shape.d_h),
+                     dtype=torch.uint8, device="cuda")
+    o = torch.empty_like(q)
+    lse = torch.empty((shape.h, shape.T), dtype=torch.float32, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        attn.attn_prefill(q, k, v, True, shape.scale, o=o, lse=lse, workspace=ws)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            attn.attn_prefill(q, k, v, True, shape.scale, o=o, lse=lse, workspace=ws)
+    torch.cuda.synchronize()
+    for seed in (6, 7, 8):
+        q2, k2, v2 = (t.cuda() for t in W.prefill_inputs(shape, seed))
+        q.copy_(q2), k.copy_(k2), v.copy_(v2)
+        g.replay()
+        torch.cuda.synchronize()
+        o_ref, lse_ref = attn.attn_prefill(q2, k2, v2, True, shape.scale)
+        torch.cuda.synchronize()
+        assert torch.equal(o, o_ref), seed
+        assert torch.equal(lse, lse_ref), seed
+    assert attn.attn_get_device_error() == 0
+
+
 @pytest.mark.parametrize("shape", [W.GQA_T8192_CAUSAL, W.GQA_T8192_FULL], ids=lambda s: s.name)
 def test_gqa_T8192_every_element(shape):
     """The T = 8192 layer the benchmark times (Q, K x3), causal and not:
