@@ -91,7 +91,7 @@ typedef enum { ATTN_DTYPE_F32 = 0, ATTN_DTYPE_BF16 = 1 } attn_dtype_t;
 /* Human-readable name of a status code; never NULL. */
 const char* attn_status_string(attn_status_t status);
 
-/* Library ABI version (major * 100 + minor): 300. */
+/* Library ABI version (major * 100 + minor): 301. */
 int attn_version(void);
 
 /*
@@ -549,6 +549,21 @@ attn_status_t attn_get_last_device_error(void* stream);
  * ATTN_ERR_CUDA if the launch fails.
  */
 attn_status_t attn_selftest_wait_timeout(unsigned int limit_us, void* stream);
+
+/*
+ * attn_selftest_prefill_stall -- exercise the bf16 prefill's abort path
+ * without a fault; builds compiled with -DATTN_DEBUG only. From the next
+ * contiguous tensor-core prefill on, every CTA skips loading K for the
+ * key_tile-th key tile it visits (counted over its work items; nothing is
+ * requested for that tile), so the MMA warp's bounded wait for it gives up
+ * after 2 s and raises ATTN_DEVERR_WAIT_TIMEOUT; every role of the CTA then
+ * stops, drains the copies and MMAs it issued, frees tensor memory and
+ * exits, and the call's outputs are undefined. key_tile < 0 turns it off.
+ * Device-wide (the current device) until turned off; synchronous. Errors:
+ * ATTN_ERR_UNSUPPORTED in release builds, ATTN_ERR_CUDA if the device write
+ * fails.
+ */
+attn_status_t attn_selftest_prefill_stall(int key_tile);
 
 /*
  * attn_selftest_delayed_copy -- test aid for the decode kernels' reads before

@@ -27,6 +27,7 @@ __all__ = [
     "attn_decode_workspace_bytes",
     "attn_get_device_error",
     "attn_get_last_device_error",
+    "attn_selftest_prefill_stall",
     "attn_status_string",
     "library",
     "ATTN_MAX_SPLITS",
@@ -108,6 +109,8 @@ def library() -> ctypes.CDLL:
     lib.attn_merge_lse_pair.restype = I
     lib.attn_selftest_delayed_copy.argtypes = [P, P, I, ctypes.c_uint, P]
     lib.attn_selftest_delayed_copy.restype = I
+    lib.attn_selftest_prefill_stall.argtypes = [I]
+    lib.attn_selftest_prefill_stall.restype = I
     lib.attn_get_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint)]
     lib.attn_get_device_error.restype = I
     lib.attn_get_last_device_error.argtypes = [P]
@@ -529,6 +532,14 @@ def attn_selftest_delayed_copy(dst, src, delay_us: int = 20, stream=None) -> Non
     _check("attn_selftest_delayed_copy",
            library().attn_selftest_delayed_copy(_ptr(dst), _ptr(src), dst.numel(), int(delay_us),
                                                 _stream(stream)))
+
+
+def attn_selftest_prefill_stall(key_tile: int) -> None:
+    """Debug builds only: make every CTA of the next contiguous bf16 prefills
+    skip loading K for its key_tile-th key tile, so that a bounded wait gives
+    up and the kernel takes its abort path (key_tile < 0: off). Raises
+    AttnError (UNSUPPORTED) on a release build."""
+    _check("attn_selftest_prefill_stall", library().attn_selftest_prefill_stall(int(key_tile)))
 
 
 def attn_get_device_error(stream=None) -> int:

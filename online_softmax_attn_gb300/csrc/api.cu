@@ -64,7 +64,7 @@ const char* attn_status_string(attn_status_t status) {
   return "unknown status";
 }
 
-int attn_version(void) { return 300; }
+int attn_version(void) { return 301; }
 
 int attn_decode_split_plan(int seq_len, int page_size, int num_splits, int* pages_per_split) {
   if (seq_len < 0 || page_size < 1 || num_splits < 1) return -1;
@@ -438,6 +438,12 @@ attn_status_t attn_selftest_wait_timeout(unsigned int limit_us, void* stream) {
   if (limit_us < 1 || limit_us > 1000000) return ATTN_ERR_INVALID_ARG;
   return from_cuda(launch_wait_timeout_selftest(uint64_t(limit_us) * 1000ull,
                                                 static_cast<cudaStream_t>(stream)));
+}
+
+attn_status_t attn_selftest_prefill_stall(int key_tile) {
+  const cudaError_t e = attn::prefill_set_stall(key_tile < 0 ? -1 : key_tile);
+  if (e == cudaErrorNotSupported) return ATTN_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 attn_status_t attn_selftest_delayed_copy(int32_t* dst, const int32_t* src, int n,

@@ -110,6 +110,9 @@ struct PagedPrefill {
 };
 cudaError_t launch_prefill_paged(const PagedPrefill& a, cudaStream_t stream);
 unsigned int prefill_read_and_clear_error(cudaStream_t stream, cudaError_t* st);
+// Debug builds: the key tile each prefill CTA skips loading K for (-1: none);
+// cudaErrorNotSupported in release builds.
+cudaError_t prefill_set_stall(int key_tile);
 // The fp32 SIMT prefill's error word (debug-build index checks only).
 unsigned int simt_read_and_clear_error(cudaStream_t stream, cudaError_t* st);
 

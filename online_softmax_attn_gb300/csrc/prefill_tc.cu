@@ -53,6 +53,11 @@
 namespace attn {
 
 static __device__ unsigned int g_prefill_err;
+#ifdef ATTN_DEBUG
+// Self-test of the abort path: the key tile (counted over a CTA's items) whose
+// K each CTA does not load, or -1.
+static __device__ int g_prefill_stall_tile = -1;
+#endif
 
 namespace {
 
@@ -464,6 +469,11 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
       // it waits for that item's stage_free. stage_waited items have been
       // waited for; the last tiles of the (at most two) others are kept.
       int stage_waited = 0, gl_even = 0, gl_odd = 0;
+#ifdef ATTN_DEBUG
+      const int stall = g_prefill_stall_tile;
+#else
+      constexpr int stall = -1;
+#endif
       int g0 = 0, it = 0, rr = 0;
       bool ok = true;
       int cur = PAGED ? 0 : int(blockIdx.x);  // this item (grid size <= n_items)
@@ -536,8 +546,10 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(bars.k_full(sk), C::KTILE);
-          load_tile(sbase + C::K_OFF + sk * C::KTILE, &tmap_k, bars.k_full(sk), j);
+          if (g != stall) {  // (the abort-path self-test requests nothing for one tile)
+            mbar_arrive_expect_tx(bars.k_full(sk), C::KTILE);
+            load_tile(sbase + C::K_OFF + sk * C::KTILE, &tmap_k, bars.k_full(sk), j);
+          }
           k_issued = g + 1;
           if (g >= NSV && !wait_or_abort(bars.v_empty(sv), ((g / NSV) - 1) & 1, abort_flag)) {
             ok = false;
@@ -601,7 +613,7 @@ __global__ void __launch_bounds__(PfCfg<D, NQ, NSK, NSV>::THREADS, 1)
         // be in flight. Bounded waits, error already recorded.
         if (q_issued > 0) (void)mbar_wait(bars.q_full(), (q_issued - 1) & 1, &g_prefill_err);
         for (int g = max(0, k_issued - NSK); g < k_issued; ++g)
-          (void)mbar_wait(bars.k_full(g % NSK), (g / NSK) & 1, &g_prefill_err);
+          if (g != stall) (void)mbar_wait(bars.k_full(g % NSK), (g / NSK) & 1, &g_prefill_err);
         for (int g = max(0, v_issued - NSV); g < v_issued; ++g)
           (void)mbar_wait(bars.v_full(g % NSV), (g / NSV) & 1, &g_prefill_err);
       }
@@ -1322,6 +1334,15 @@ cudaError_t launch_prefill_paged(const PagedPrefill& a, cudaStream_t stream) {
   if (a.d_h == 128)
     return pair ? launch_paged<128, 2, 2, 3>(a, stream) : launch_paged<128, 1, 3, 3>(a, stream);
   return pair ? launch_paged<64, 2, 4, 4>(a, stream) : launch_paged<64, 1, 4, 4>(a, stream);
+}
+
+cudaError_t prefill_set_stall(int key_tile) {
+#ifdef ATTN_DEBUG
+  return cudaMemcpyToSymbol(g_prefill_stall_tile, &key_tile, sizeof(key_tile));
+#else
+  (void)key_tile;
+  return cudaErrorNotSupported;
+#endif
 }
 
 unsigned int prefill_read_and_clear_error(cudaStream_t stream, cudaError_t* st) {

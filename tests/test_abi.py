@@ -273,7 +273,7 @@ def test_selftest_wait_timeout_arguments(lib):
 
 def test_version(lib):
     lib.attn_version.restype = ctypes.c_int
-    assert lib.attn_version() == 300
+    assert lib.attn_version() == 301
 
 
 def test_prefill_host_checks_limits_before_queueing(lib):
@@ -367,3 +367,12 @@ def test_device_error_bits_match_the_header():
     for name, value in bits.items():
         assert getattr(attn, name) == int(value, 16), name
     assert set(attn.DEVERR_NAMES) == {int(v, 16) for v in bits.values()}
+
+
+def test_prefill_stall_selftest_is_debug_only(lib):
+    """The release library refuses the abort-path self-test without touching
+    the device."""
+    lib.attn_selftest_prefill_stall.argtypes = [ctypes.c_int]
+    lib.attn_selftest_prefill_stall.restype = ctypes.c_int
+    assert lib.attn_selftest_prefill_stall(2) == 2  # ATTN_ERR_UNSUPPORTED
+    assert lib.attn_selftest_prefill_stall(-1) == 2

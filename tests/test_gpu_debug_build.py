@@ -12,6 +12,7 @@ only."""
 import itertools
 
 import pytest
+import torch
 
 import online_softmax_attn_gb300 as attn
 import test_gpu_decode as D
@@ -122,3 +123,30 @@ def test_case_under_debug_checks(fn, kw):
 def test_debug_build_is_the_library_in_use(debug_library):
     assert attn.library() is debug_library
     assert attn.library()._name.endswith("libattn_gb300_debug.so")
+
+
+def test_prefill_abort_path_after_a_stalled_load(debug_library):
+    """The bf16 prefill's abort path, without a fault: with one key tile's K
+    never requested in every CTA, the MMA warp's bounded wait gives up after
+    2 s and raises ATTN_DEVERR_WAIT_TIMEOUT; every role stops, drains what it
+    issued, frees tensor memory and exits. The next call on the same context,
+    with the stall off, is exact."""
+    import oracle
+    import workloads as W
+    from parity import check_lse, check_out
+
+    shape = W.PrefillShape("t", 8, 2, 128, 1024, torch.bfloat16, True)
+    q, k, v = W.prefill_inputs(shape, 31)
+    attn.attn_selftest_prefill_stall(2)
+    try:
+        attn.attn_prefill(q.cuda(), k.cuda(), v.cuda(), True, shape.scale)
+        bits = attn.attn_get_device_error()
+    finally:
+        attn.attn_selftest_prefill_stall(-1)
+    assert bits & attn.ATTN_DEVERR_WAIT_TIMEOUT, f"bits {bits:#x}"
+    assert bits & attn.ATTN_DEVERR_DEBUG_INDEX == 0
+    o, lse = P.run(q, k, v, True, shape.scale)
+    assert attn.attn_get_device_error() == 0
+    O_ref, L_ref = oracle.attention_ref(q, k, v, shape.scale, True)
+    check_out(o, O_ref, torch.bfloat16, "after the abort")
+    check_lse(lse, L_ref)
