@@ -55,13 +55,13 @@ KERNEL_FILES["merge_pair"] = ["online_softmax_attn_gb300/csrc/merge.cu", "online
 NCU_TRAFFIC = {
     # kind: (dram read + write bytes per launch, sha256[:16] of the kernel's files)
     # prefill_bf16_kernel, causal T=8192 layer, full-size capture: 102.5 MB read
-    # (compulsory Q, K, fp16 V) + 31.2 MB of the 67.1 MB output written back by exit
-    "prefill": (133.63e6, "7e0f2129ef10512c"),
+    # (compulsory Q, K, fp16 V) + 30.6 MB of the 67.1 MB output written back by exit
+    "prefill": (133.14e6, "b157eca97be5ddc7"),
     # prefill_bf16_kernel, causal T=2048 layer, full-size capture: the compulsory
     # 25.3 MB read; the 16.8 MB output is still in L2 when the kernel exits
-    "prefill_T2048": (25.26e6, "7e0f2129ef10512c"),
+    "prefill_T2048": (25.26e6, "b157eca97be5ddc7"),
     # prefill_bf16_kernel (paged), 8 rows x 1024 queries over 8192 keys, full-size capture
-    "prefill_paged": (471.96e6, "7e0f2129ef10512c"),
+    "prefill_paged": (473.54e6, "b157eca97be5ddc7"),
     # decode_split_kernel: a 16-row capture (304.0 MB for 299.5 MB algorithmic) scaled by
     # the KV bytes to the 66-row batch
     "decode": (2.1520e9, "61652ac3d8eae098"),
