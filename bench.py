@@ -347,6 +347,77 @@ def run_reference(args, world, rank):
 # GPU arm
 # ---------------------------------------------------------------------------
 
+def g4(x):
+    return None if x is None else float(f"{x:.4g}")
+
+
+def bench_line(*, world, steps, warmup, value, dec_value, dec_frac, step_ms, S, pre_achieved,
+               tc_peak, traffic, e2e, cpu, cpu_rows_n, launches, clk, dec_avg, dec_e2e=None,
+               det=None, adaptive=None, prefill_2048=None, prefill_paged=None, merge_pair=None,
+               mixed=None, decode_b1=None) -> dict:
+    """The one JSON line rank 0 prints: the step's prefill and decode figures,
+    the roofline of the prefill kernel, e2e, the CPU baseline and clocks, and
+    the measurements outside the step as a compact ``x`` object (the line
+    stays short enough for a log tail to hold it whole)."""
+    extras = {"decode_ms": g4(dec_avg)}
+    if dec_e2e:
+        extras["decode_e2e_gbs"] = g4(dec_e2e["value"])
+    if det:
+        extras["det_gbs"] = g4(det["value"])
+    if adaptive:
+        extras["adaptive_gbs"] = g4(adaptive["value"])
+    if prefill_2048:
+        extras["t2048_tflops"] = g4(prefill_2048["value"])
+        extras["t2048_frac"] = g4(prefill_2048["roofline"]["frac"])
+    if prefill_paged:
+        extras["paged_prefill_tflops"] = g4(prefill_paged["value"])
+        extras["paged_prefill_frac"] = g4(prefill_paged["roofline"]["frac"])
+    if merge_pair:
+        extras["merge_pair_gbs"] = g4(merge_pair["value"])
+    if mixed:
+        extras["mixed_prefill_tflops"] = g4(mixed["prefill_tflops"])
+        extras["mixed_decode_gbs"] = g4(mixed["decode_rows_gbs"])
+        extras["mixed_decode_alone_gbs"] = g4(mixed["decode_alone_gbs"])
+    if decode_b1:
+        for key, short in ((W.DECODE_S32K.name, "b1_h32"), (W.DECODE_70B_TP8.name, "b1_70b_tp8")):
+            if key in decode_b1:
+                extras[f"{short}_us"] = g4(decode_b1[key]["us_per_call"])
+                extras[f"{short}_frac"] = g4(decode_b1[key]["frac_of_hbm"])
+    return {
+        "metric": METRIC,
+        "value": g4(value),
+        "unit": "TFLOP/s",
+        "decode_gbs": g4(dec_value),
+        "decode_frac": g4(dec_frac),
+        "n_gpus": world,
+        "steps": steps,
+        "warmup": warmup,
+        "ms_per_step": g4(step_ms),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": "causal GQA prefill T8192 h32 kv8 d128 + paged decode 66 rows",
+            "decode_splits": S,
+            "l2": "flush 512MiB; decode KV 2.1GB>L2",
+            "parallelism": f"replicas x{world}",
+        },
+        "roofline": {"bound": "tensor", "achieved": g4(pre_achieved), "peak": tc_peak, "unit": "TFLOP/s",
+                     "frac": g4(pre_achieved / tc_peak), "traffic": traffic},
+        "e2e": None if e2e is None else {k: (g4(v) if isinstance(v, float) else v)
+                                         for k, v in e2e.items() if k != "ms"},
+        "cpu_baseline": None if cpu is None else {
+            "value": g4(cpu["value"]), "unit": cpu["unit"], "cores": cpu["cores"], "kind": "oracle",
+            "sample": f"{cpu_rows_n}x64 rows of one T8192 head"},
+        "gpu_launches": launches,
+        "clocks": None if clk is None else {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"],
+                                            "reasons": clk["reasons"], "samples": clk["samples"]},
+        "x": extras,
+    }
+
+
 def run_gpu(args, world, rank, local):
     import online_softmax_attn_gb300 as attn
     from online_softmax_attn_gb300 import build as attn_build
@@ -622,67 +693,14 @@ def run_gpu(args, world, rank, local):
     # The full record goes to stderr; stdout carries one short line.
     print("bench detail: " + json.dumps(detail), file=sys.stderr, flush=True)
 
-    def g4(x):
-        return None if x is None else float(f"{x:.4g}")
-
-    extras = {"decode_ms": g4(dec_avg)}
-    if dec_e2e:
-        extras["decode_e2e_gbs"] = g4(dec_e2e["value"])
-    if det:
-        extras["det_gbs"] = g4(det["value"])
-    if adaptive:
-        extras["adaptive_gbs"] = g4(adaptive["value"])
-    if prefill_2048:
-        extras["t2048_tflops"] = g4(prefill_2048["value"])
-        extras["t2048_frac"] = g4(prefill_2048["roofline"]["frac"])
-    if prefill_paged:
-        extras["paged_prefill_tflops"] = g4(prefill_paged["value"])
-        extras["paged_prefill_frac"] = g4(prefill_paged["roofline"]["frac"])
-    if merge_pair:
-        extras["merge_pair_gbs"] = g4(merge_pair["value"])
-    if mixed:
-        extras["mixed_prefill_tflops"] = g4(mixed["prefill_tflops"])
-        extras["mixed_decode_gbs"] = g4(mixed["decode_rows_gbs"])
-        extras["mixed_decode_alone_gbs"] = g4(mixed["decode_alone_gbs"])
-    if decode_b1:
-        for key, short in ((W.DECODE_S32K.name, "b1_h32"), (W.DECODE_70B_TP8.name, "b1_70b_tp8")):
-            if key in decode_b1:
-                extras[f"{short}_us"] = g4(decode_b1[key]["us_per_call"])
-                extras[f"{short}_frac"] = g4(decode_b1[key]["frac_of_hbm"])
-    line = {
-        "metric": METRIC,
-        "value": g4(value),
-        "unit": "TFLOP/s",
-        "decode_gbs": g4(dec_value),
-        "decode_frac": g4(dec_achieved / hbm_peak),
-        "n_gpus": world,
-        "steps": args.steps,
-        "warmup": args.warmup,
-        "ms_per_step": g4(step_ms),
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": "bf16",
-        "data": "synthetic",
-        "config": {
-            "workload": "causal GQA prefill T8192 h32 kv8 d128 + paged decode 66 rows",
-            "decode_splits": S,
-            "l2": "flush 512MiB; decode KV 2.1GB>L2",
-            "parallelism": f"replicas x{world}",
-        },
-        "roofline": {"bound": "tensor", "achieved": g4(pre_achieved), "peak": tc_peak, "unit": "TFLOP/s",
-                     "frac": g4(pre_achieved / tc_peak), "traffic": traffic_for("prefill")},
-        "e2e": None if e2e is None else {k: (g4(v) if isinstance(v, float) else v)
-                                         for k, v in e2e.items() if k != "ms"},
-        "cpu_baseline": None if cpu is None else {
-            "value": g4(cpu["value"]), "unit": cpu["unit"], "cores": cpu["cores"], "kind": "oracle",
-            "sample": f"{cpu_rows_n}x64 rows of one T8192 head"},
+    line = bench_line(
+        world=world, steps=args.steps, warmup=args.warmup, value=value, dec_value=dec_value,
+        dec_frac=dec_achieved / hbm_peak, step_ms=step_ms, S=S, pre_achieved=pre_achieved,
+        tc_peak=tc_peak, traffic=traffic_for("prefill"), e2e=e2e, cpu=cpu, cpu_rows_n=cpu_rows_n,
         # prefill: V-to-fp16 pass + attention kernel; decode: split kernel + merge
-        "gpu_launches": (2 * int(do_pre) + 2 * int(do_dec)) * args.steps,
-        "clocks": None if clk is None else {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"],
-                                            "reasons": clk["reasons"], "samples": clk["samples"]},
-        "x": extras,
-    }
+        launches=(2 * int(do_pre) + 2 * int(do_dec)) * args.steps, clk=clk, dec_avg=dec_avg,
+        dec_e2e=dec_e2e, det=det, adaptive=adaptive, prefill_2048=prefill_2048,
+        prefill_paged=prefill_paged, merge_pair=merge_pair, mixed=mixed, decode_b1=decode_b1)
     print(json.dumps(line), flush=True)
 
 
